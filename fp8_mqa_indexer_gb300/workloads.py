@@ -1,0 +1,233 @@
+"""Seeded synthetic inputs for MQA logits scoring.
+
+This module only draws random numbers and lays them out: it holds none of the
+scoring arithmetic, and both the CUDA path and the CPU oracle are fed from it.
+Every tensor is created on the CPU from a seeded ``torch.Generator`` so the
+oracle and the GPU see identical bytes.  FP8 values are produced with torch's
+own ``float8_e4m3fn`` cast (round to nearest even) and handed over as raw bytes.
+
+The shapes and distributions follow the workloads the pages describe:
+  * the dense call of the instagit DeepGEMM article, section "Implementing
+    Standard MQA Logits Computation" (S_q=2048, S_kv=4096, H=32, D=64, ranges
+    [i, S_kv));
+  * the H=64 / D=128 timing shapes of "[PR #435] Improve SM100 MX MQA logits
+    clean-output performance", section "Performance" (Q/KV 2048/32768 and
+    8192/65536, each row using [0, KV - Q + row));
+  * paged decode as in the article's "Implementing Paged MQA Logits Computation
+    for Decoding" with next_n and 64-token blocks as in "[PR #314] fix: SM90
+    paged MQA logits IMA on next_n=4".
+The datasets behind those numbers are not public inputs; these synthetic
+tensors stand in for them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+E4M3 = torch.float8_e4m3fn
+
+
+@dataclass
+class DenseCase:
+    name: str
+    q: torch.Tensor          # [S_q, H, D] uint8 (E4M3 bytes)
+    kv: torch.Tensor         # [S_kv, D] uint8 (E4M3 bytes)
+    kv_scale: torch.Tensor   # [S_kv] float32
+    weights: torch.Tensor    # [S_q, H] float32
+    k_start: torch.Tensor    # [S_q] int32
+    k_end: torch.Tensor      # [S_q] int32
+    ldo: int
+    clean: bool = True
+    compressed: bool = False
+
+    @property
+    def S_q(self):
+        return self.q.shape[0]
+
+    @property
+    def H(self):
+        return self.q.shape[1]
+
+    @property
+    def D(self):
+        return self.q.shape[2]
+
+    @property
+    def S_kv(self):
+        return self.kv.shape[0]
+
+    def valid_counts(self) -> torch.Tensor:
+        """Number of scored keys per row (range clipped to [0, S_kv))."""
+        lo = self.k_start.clamp(min=0).to(torch.int64)
+        hi = self.k_end.clamp(max=self.S_kv).to(torch.int64)
+        return (hi - lo).clamp(min=0)
+
+
+@dataclass
+class PagedCase:
+    name: str
+    q: torch.Tensor            # [B*next_n, H, D] uint8
+    kv_cache: torch.Tensor     # [num_blocks, block_kv, D] uint8
+    kv_scales: torch.Tensor    # [num_blocks, block_kv] float32
+    weights: torch.Tensor      # [B*next_n, H] float32
+    context_lens: torch.Tensor  # [B] int32
+    block_table: torch.Tensor  # [B, max_blocks_per_seq] int32 (-1 = unused)
+    next_n: int
+    ldo: int
+    clean: bool = True
+
+    @property
+    def B(self):
+        return self.context_lens.shape[0]
+
+    @property
+    def H(self):
+        return self.q.shape[1]
+
+    @property
+    def D(self):
+        return self.q.shape[2]
+
+    @property
+    def block_kv(self):
+        return self.kv_cache.shape[1]
+
+    @property
+    def num_blocks(self):
+        return self.kv_cache.shape[0]
+
+    @property
+    def max_blocks_per_seq(self):
+        return self.block_table.shape[1]
+
+    def valid_counts(self) -> torch.Tensor:
+        ctx = self.context_lens.to(torch.int64).repeat_interleave(self.next_n)
+        t = torch.arange(self.next_n, dtype=torch.int64).repeat(self.B)
+        return (ctx - self.next_n + t + 1).clamp(min=0)
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator()
+    g.manual_seed(seed)
+    return g
+
+
+def e4m3_normal(shape, g: torch.Generator, clamp: Optional[float] = None,
+                chunk: int = 1 << 24) -> torch.Tensor:
+    """E4M3 bytes of N(0,1) samples (optionally clamped), drawn in chunks."""
+    n = 1
+    for s in shape:
+        n *= s
+    out = torch.empty(n, dtype=torch.uint8)
+    for k in range(0, n, chunk):
+        m = min(chunk, n - k)
+        x = torch.randn(m, generator=g)
+        if clamp is not None:
+            x = x.clamp(-clamp, clamp)
+        out[k:k + m] = x.to(E4M3).view(torch.uint8)
+    return out.view(*shape)
+
+
+def uniform(shape, lo: float, hi: float, g: torch.Generator) -> torch.Tensor:
+    return torch.rand(shape, generator=g) * (hi - lo) + lo
+
+
+def dense_case(S_q: int, S_kv: int, H: int, D: int, *, seed: int, ranges: str = "causal_tail",
+               w_std: float = 1.0, clamp: Optional[float] = None, name: str = "dense",
+               compressed: bool = False, clean: bool = True, ldo: Optional[int] = None,
+               k_start=None, k_end=None) -> DenseCase:
+    """A dense case with one of the pages' range shapes.
+
+    ranges: "causal_tail" -> [0, S_kv - S_q + i)       (reproducer of PR #435)
+            "causal_tail_inclusive" -> [0, S_kv - S_q + i + 1)
+            "suffix" -> [i, S_kv)                        (instagit dense example)
+            "full" -> [0, S_kv)
+            "custom" -> k_start / k_end given
+    """
+    g = _gen(seed)
+    q = e4m3_normal((S_q, H, D), g, clamp)
+    kv = e4m3_normal((S_kv, D), g, clamp)
+    kv_scale = uniform((S_kv,), 0.5, 2.0, g)
+    weights = torch.randn((S_q, H), generator=g) * w_std
+    i = torch.arange(S_q, dtype=torch.int32)
+    if ranges == "causal_tail":
+        ks, ke = torch.zeros_like(i), S_kv - S_q + i
+    elif ranges == "causal_tail_inclusive":
+        ks, ke = torch.zeros_like(i), S_kv - S_q + i + 1
+    elif ranges == "suffix":
+        ks, ke = i.clone(), torch.full_like(i, S_kv)
+    elif ranges == "full":
+        ks, ke = torch.zeros_like(i), torch.full_like(i, S_kv)
+    elif ranges == "custom":
+        ks = torch.as_tensor(k_start, dtype=torch.int32)
+        ke = torch.as_tensor(k_end, dtype=torch.int32)
+    else:
+        raise ValueError(ranges)
+    ks, ke = ks.to(torch.int32).contiguous(), ke.to(torch.int32).contiguous()
+    if ldo is None:
+        if compressed:
+            lens = (ke.clamp(max=S_kv) - ks.clamp(min=0)).clamp(min=0)
+            ldo = max(1, int(lens.max().item()) if S_q else 1)
+        else:
+            ldo = S_kv
+    return DenseCase(name, q, kv, kv_scale, weights, ks, ke, ldo, clean, compressed)
+
+
+# Named workloads.  Index order is the order the benchmark configuration lists them.
+DENSE_CONFIGS = {
+    "dense_tiny": dict(S_q=128, S_kv=512, H=8, D=64, ranges="causal_tail_inclusive", clamp=4.0,
+                       seed=1000),
+    "dense_2k_4k_h32_d64": dict(S_q=2048, S_kv=4096, H=32, D=64, ranges="suffix", seed=1001),
+    "dense_2k_32k_h64_d128": dict(S_q=2048, S_kv=32768, H=64, D=128, ranges="causal_tail",
+                                  w_std=0.125, seed=1002),
+    "dense_8k_64k_h64_d128": dict(S_q=8192, S_kv=65536, H=64, D=128, ranges="causal_tail",
+                                  w_std=0.125, seed=1003),
+    "dense_8k_64k_h64_d128_compressed": dict(S_q=8192, S_kv=65536, H=64, D=128,
+                                             ranges="causal_tail", w_std=0.125, seed=1003,
+                                             compressed=True),
+}
+
+
+def dense_config(name: str) -> DenseCase:
+    return dense_case(name=name, **DENSE_CONFIGS[name])
+
+
+def paged_case(B: int, next_n: int, H: int, D: int, *, seed: int, ctx_lo: int, ctx_hi: int,
+               block_kv: int = 64, num_blocks: int = 70000, max_blocks_per_seq: Optional[int] = None,
+               name: str = "paged", context_lens=None) -> PagedCase:
+    """Paged decode case: random context lengths in [ctx_lo, ctx_hi], pages of
+    ``block_kv`` keys handed out by a random permutation of the physical blocks."""
+    g = _gen(seed)
+    if context_lens is None:
+        ctx = torch.randint(ctx_lo, ctx_hi + 1, (B,), generator=g, dtype=torch.int64)
+    else:
+        ctx = torch.as_tensor(context_lens, dtype=torch.int64)
+    pages = (ctx.clamp(min=0) + block_kv - 1) // block_kv
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = max(1, (ctx_hi + block_kv - 1) // block_kv)
+    assert int(pages.sum()) <= num_blocks and int(pages.max()) <= max_blocks_per_seq
+    perm = torch.randperm(num_blocks, generator=g).to(torch.int32)
+    table = torch.full((B, max_blocks_per_seq), -1, dtype=torch.int32)
+    off = 0
+    for b in range(B):
+        n = int(pages[b])
+        table[b, :n] = perm[off:off + n]
+        off += n
+    kv_cache = e4m3_normal((num_blocks, block_kv, D), g)
+    kv_scales = uniform((num_blocks, block_kv), 0.5, 2.0, g)
+    q = e4m3_normal((B * next_n, H, D), g)
+    weights = torch.randn((B * next_n, H), generator=g)
+    ldo = max_blocks_per_seq * block_kv
+    return PagedCase(name, q, kv_cache, kv_scales, weights, ctx.to(torch.int32), table, next_n, ldo)
+
+
+PAGED_CONFIGS = {
+    "paged_b64_n2_h64_d128": dict(B=64, next_n=2, H=64, D=128, ctx_lo=4096, ctx_hi=65536,
+                                  block_kv=64, num_blocks=70000, seed=1004),
+}
+
+
+def paged_config(name: str) -> PagedCase:
+    return paged_case(name=name, **PAGED_CONFIGS[name])

@@ -1,0 +1,260 @@
+/*
+ * mqa_oracle.c -- plain, slow CPU oracle for MQA logits scoring.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file: only the tests, the smoke check and the CPU-baseline leg of the
+ * benchmark do.  It shares no header, constant or helper with the CUDA library.
+ *
+ * What it computes (sources are the four web pages this project is built from):
+ *
+ *   "How to Implement MQA (Multi-Query Attention) Logits Computation with
+ *    DeepGEMM" (instagit), section "Core Architecture Components":
+ *      - the score of query token i against KV token j is the per-head dot
+ *        product of q[i,h,:] with the single KV head kv[j,:], passed through a
+ *        ReLU, multiplied by the per-head weight w[i,h] and summed over heads
+ *        ("Math Warp Reduction");
+ *      - per-token fp32 KV scales are applied to the dot product (FAQ "How does
+ *        DeepGEMM handle quantization scales");
+ *      - compressed logits keep only [k_start, k_end) of each row
+ *        ("Compressed Logits").
+ *   "[PR #435] Improve SM100 MX MQA logits clean-output performance", section
+ *   "Standalone performance reproducer": positions outside a row's range are
+ *   -inf in clean mode, and all-zero inputs give exactly 0 inside the range.
+ *
+ * Written out, for k_start[i] <= j < k_end[i]:
+ *
+ *     logits[i, j] = sum_h  w[i,h] * max(0, s[j] * sum_d q[i,h,d] * kv[j,d])
+ *
+ * with q and kv decoded exactly from FP8 E4M3 (torch.float8_e4m3fn), and every
+ * step in double precision.  The inner dot product is exact in double: each
+ * product of two E4M3 values is a multiple of 2^-18 below 2^18, so any partial
+ * sum of up to 2^16 terms is an integer multiple of 2^-18 below 2^34, which a
+ * 53-bit significand holds exactly (D above 2^16 is rejected).  The head sum
+ * is rounded once to fp32 at the end.
+ *
+ * Readings this oracle takes where the pages are silent or disagree:
+ *   - fill value outside the range is -inf (the reproducer's isneginf assert),
+ *     not the zero-fill one sentence of the instagit article mentions;
+ *   - the scale sits inside the ReLU, exactly as in the formula above;
+ *   - a range is intersected with [0, S_kv); start >= end is an empty row;
+ *   - the paged decode row t of sequence b scores keys [0, ctx_b - next_n + t + 1);
+ *   - in non-clean mode positions outside the range are left untouched.
+ *
+ * Parity pins for every function here live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#define ORACLE_CLEAN 1u
+#define ORACLE_COMPRESSED 2u
+
+/* ---------------------------------------------------------------------------
+ * FP8 E4M3 ("fn" variant, as torch.float8_e4m3fn): 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits, no infinities, codes 0x7F / 0xFF are NaN.
+ *   exponent field 0      : subnormal, value = mantissa * 2^-9
+ *   exponent field 1..15  : normal,    value = (8 + mantissa) * 2^(exp - 10)
+ * The largest finite value is (8 + 6) * 2^5 = 448.
+ * ------------------------------------------------------------------------- */
+static double e4m3_decode(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int expo = (code >> 3) & 0xF;
+    int mant = code & 0x7;
+    double mag;
+    if (expo == 0xF && mant == 0x7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)mant, -9);
+    else
+        mag = ldexp((double)(8 + mant), expo - 10);
+    return sign ? -mag : mag;
+}
+
+int oracle_e4m3_table(double *out256)
+{
+    for (int c = 0; c < 256; ++c)
+        out256[c] = e4m3_decode((uint8_t)c);
+    return 0;
+}
+
+/* Exact dot product of two E4M3 vectors of length D (see header comment). */
+static double e4m3_dot(const uint8_t *a, const uint8_t *b, int D)
+{
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d)
+        acc += e4m3_decode(a[d]) * e4m3_decode(b[d]);
+    return acc;
+}
+
+/* One logit and its tolerance term sum_h |w * s * x|. */
+static float one_logit(const uint8_t *q_row /* [H, D] */, const uint8_t *kv_row /* [D] */,
+                       double s, const float *w_row /* [H] */, int H, int D, double *abs_sum)
+{
+    double sum = 0.0, asum = 0.0;
+    for (int h = 0; h < H; ++h) {
+        double x = e4m3_dot(q_row + (size_t)h * D, kv_row, D);
+        double sx = s * x;
+        double r = sx > 0.0 ? sx : 0.0;
+        sum += (double)w_row[h] * r;
+        asum += fabs((double)w_row[h] * sx);
+    }
+    if (abs_sum)
+        *abs_sum = asum;
+    return (float)sum;
+}
+
+/*
+ * Dense MQA logits for rows [row_begin, row_end).
+ *   q        [S_q, H, D] E4M3 bytes      kv       [S_kv, D] E4M3 bytes
+ *   kv_scale [S_kv] fp32                 weights  [S_q, H] fp32
+ *   k_start, k_end [S_q] int32
+ *   logits   points at row row_begin of an [.., ldo] fp32 matrix
+ *   tol      (nullable) same layout as logits, receives 1e-3*sum_h|w s x| + 1e-5
+ *            at every written logit position
+ * Uncompressed: row i has S_kv columns (ldo >= S_kv).  Compressed: column c of
+ * row i holds key k_start[i] + c; clean mode fills c in [len_i, ldo) with -inf.
+ * Returns 0, or -1 on invalid arguments.
+ */
+int oracle_mqa_logits(const uint8_t *q, const uint8_t *kv, const float *kv_scale,
+                      const float *weights, const int32_t *k_start, const int32_t *k_end,
+                      int S_q, int S_kv, int H, int D, int64_t ldo, unsigned flags,
+                      int row_begin, int row_end, float *logits, double *tol)
+{
+    int clean = (flags & ORACLE_CLEAN) != 0;
+    int compressed = (flags & ORACLE_COMPRESSED) != 0;
+    if (S_q < 0 || S_kv < 0 || H <= 0 || D <= 0 || D > 65536 || row_begin < 0 || row_end > S_q ||
+        row_begin > row_end)
+        return -1;
+    if (!compressed && ldo < S_kv)
+        return -1;
+    if (compressed && ldo < 0)
+        return -1;
+    for (int i = row_begin; i < row_end; ++i) {
+        float *out = logits + (size_t)(i - row_begin) * (size_t)ldo;
+        double *tout = tol ? tol + (size_t)(i - row_begin) * (size_t)ldo : NULL;
+        int lo = k_start[i] < 0 ? 0 : k_start[i];
+        int hi = k_end[i] > S_kv ? S_kv : k_end[i];
+        if (hi < lo)
+            hi = lo;
+        if (compressed && (int64_t)(hi - lo) > ldo)
+            return -1;
+        int64_t width = compressed ? ldo : S_kv;
+        for (int64_t c = 0; c < width; ++c) {
+            int j = compressed ? (int)(lo + c) : (int)c;
+            int valid = compressed ? (c < hi - lo) : (j >= lo && j < hi);
+            if (valid) {
+                double asum;
+                out[c] = one_logit(q + (size_t)i * H * D, kv + (size_t)j * D, (double)kv_scale[j],
+                                   weights + (size_t)i * H, H, D, &asum);
+                if (tout)
+                    tout[c] = 1e-3 * asum + 1e-5;
+            } else if (clean) {
+                out[c] = -INFINITY;
+                if (tout)
+                    tout[c] = 0.0;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Paged decode MQA logits ("Implementing Paged MQA Logits Computation for
+ * Decoding" of the instagit article; next_n and block_kv as in "[PR #314] fix:
+ * SM90 paged MQA logits IMA on next_n=4").  Rows are r = b * next_n + t.
+ *   q          [B * next_n, H, D] E4M3      weights [B * next_n, H] fp32
+ *   kv_cache   [num_blocks, block_kv, D] E4M3
+ *   kv_scales  [num_blocks, block_kv] fp32
+ *   context_lens [B] int32
+ *   block_table  [B, max_blocks_per_seq] int32: logical page -> physical block
+ * Row r scores key positions j in [0, context_lens[b] - next_n + t + 1); key j
+ * lives in block block_table[b, j / block_kv], slot j % block_kv.  A row has
+ * max_blocks_per_seq * block_kv columns; clean mode writes -inf elsewhere.
+ * Returns 0, or -1 on invalid arguments (including a block id out of range or a
+ * context longer than the block table).
+ */
+int oracle_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_cache, const float *kv_scales,
+                            const float *weights, const int32_t *context_lens,
+                            const int32_t *block_table, int max_blocks_per_seq, int B, int next_n,
+                            int H, int D, int block_kv, int num_blocks, int64_t ldo,
+                            unsigned flags, int row_begin, int row_end, float *logits, double *tol)
+{
+    int clean = (flags & ORACLE_CLEAN) != 0;
+    int64_t width = (int64_t)max_blocks_per_seq * block_kv;
+    if (B < 0 || next_n <= 0 || H <= 0 || D <= 0 || D > 65536 || block_kv <= 0 || num_blocks < 0 ||
+        max_blocks_per_seq < 0 || ldo < width || row_begin < 0 || row_end > B * next_n ||
+        row_begin > row_end || (flags & ORACLE_COMPRESSED))
+        return -1;
+    for (int r = row_begin; r < row_end; ++r) {
+        int b = r / next_n, t = r % next_n;
+        int ctx = context_lens[b];
+        if (ctx < 0 || (int64_t)ctx > width)
+            return -1;
+        int end = ctx - next_n + t + 1;
+        if (end < 0)
+            end = 0;
+        float *out = logits + (size_t)(r - row_begin) * (size_t)ldo;
+        double *tout = tol ? tol + (size_t)(r - row_begin) * (size_t)ldo : NULL;
+        for (int64_t j = 0; j < width; ++j) {
+            if (j < end) {
+                int32_t blk = block_table[(size_t)b * max_blocks_per_seq + j / block_kv];
+                if (blk < 0 || blk >= num_blocks)
+                    return -1;
+                size_t tok = (size_t)blk * block_kv + (size_t)(j % block_kv);
+                double asum;
+                out[j] = one_logit(q + (size_t)r * H * D, kv_cache + tok * D, (double)kv_scales[tok],
+                                   weights + (size_t)r * H, H, D, &asum);
+                if (tout)
+                    tout[j] = 1e-3 * asum + 1e-5;
+            } else if (clean) {
+                out[j] = -INFINITY;
+                if (tout)
+                    tout[j] = 0.0;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Paged work schedule.  The pages fix its shape -- num_sms + 1 entries, entry k
+ * saying where SM k starts and entry num_sms marking the end ("[PR #314] ...",
+ * section "a97b74d", "Fix": schedule_meta sized num_sms + 1) -- but not the unit
+ * of work.  This library's reading: a unit is one sequence's next_n queries
+ * against one 128-key tile, sequence b owns ceil(max(ctx_b, 0) / 128) units,
+ * units are numbered sequence by sequence, and SM k starts at unit
+ * floor(k * U / num_sms) of U in total.  Entry k is the pair (b, tile) of that
+ * unit; the end entry, and any start at U, is (B, 0).
+ * next_n and block_kv do not change the split (a whole sequence is one query
+ * atom); they are validated only.  Returns 0, or -1 on invalid arguments.
+ */
+int oracle_paged_mqa_logits_metadata(const int32_t *context_lens, int B, int next_n, int block_kv,
+                                     int num_sms, int32_t *schedule_meta /* [num_sms + 1, 2] */)
+{
+    if (B < 0 || next_n <= 0 || block_kv <= 0 || 128 % block_kv != 0 || num_sms <= 0)
+        return -1;
+    int64_t total = 0;
+    for (int b = 0; b < B; ++b) {
+        int ctx = context_lens[b] > 0 ? context_lens[b] : 0;
+        total += (ctx + 127) / 128;
+    }
+    for (int k = 0; k <= num_sms; ++k) {
+        int64_t u = (int64_t)k * total / num_sms;
+        int64_t before = 0;
+        int b = 0;
+        int32_t tile = 0;
+        for (; b < B; ++b) {
+            int ctx = context_lens[b] > 0 ? context_lens[b] : 0;
+            int64_t n = (ctx + 127) / 128;
+            if (u < before + n) {
+                tile = (int32_t)(u - before);
+                break;
+            }
+            before += n;
+        }
+        schedule_meta[2 * k] = b;            /* b == B when u == total */
+        schedule_meta[2 * k + 1] = b < B ? tile : 0;
+    }
+    return 0;
+}
