@@ -43,8 +43,10 @@
  * Parity pins for every function here live in tests/test_oracle_pins.py.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <stdlib.h>
 
 #define ORACLE_CLEAN 1u
 #define ORACLE_COMPRESSED 2u
@@ -71,29 +73,56 @@ static double e4m3_decode(uint8_t code)
     return sign ? -mag : mag;
 }
 
-int oracle_e4m3_table(double *out256)
+/* The 256 decoded values, built once from e4m3_decode (a lookup, not a
+ * different decoding). */
+static double g_table[256];
+static pthread_once_t g_table_once = PTHREAD_ONCE_INIT;
+
+static void build_table(void)
 {
     for (int c = 0; c < 256; ++c)
-        out256[c] = e4m3_decode((uint8_t)c);
+        g_table[c] = e4m3_decode((uint8_t)c);
+}
+
+static const double *table(void)
+{
+    pthread_once(&g_table_once, build_table);
+    return g_table;
+}
+
+int oracle_e4m3_table(double *out256)
+{
+    const double *t = table();
+    for (int c = 0; c < 256; ++c)
+        out256[c] = t[c];
     return 0;
 }
 
-/* Exact dot product of two E4M3 vectors of length D (see header comment). */
-static double e4m3_dot(const uint8_t *a, const uint8_t *b, int D)
+static void decode_row(const uint8_t *src, size_t n, double *dst)
+{
+    const double *t = table();
+    for (size_t k = 0; k < n; ++k)
+        dst[k] = t[src[k]];
+}
+
+/* Exact dot product of two decoded E4M3 vectors of length D (see header
+ * comment), summed in order d = 0 .. D-1. */
+static double dot(const double *a, const double *b, int D)
 {
     double acc = 0.0;
     for (int d = 0; d < D; ++d)
-        acc += e4m3_decode(a[d]) * e4m3_decode(b[d]);
+        acc += a[d] * b[d];
     return acc;
 }
 
-/* One logit and its tolerance term sum_h |w * s * x|. */
-static float one_logit(const uint8_t *q_row /* [H, D] */, const uint8_t *kv_row /* [D] */,
-                       double s, const float *w_row /* [H] */, int H, int D, double *abs_sum)
+/* One logit and its tolerance term sum_h |w * s * x|; q_dec is the decoded
+ * [H, D] query row, kv_dec the decoded key. */
+static float one_logit(const double *q_dec, const double *kv_dec, double s, const float *w_row,
+                       int H, int D, double *abs_sum)
 {
     double sum = 0.0, asum = 0.0;
     for (int h = 0; h < H; ++h) {
-        double x = e4m3_dot(q_row + (size_t)h * D, kv_row, D);
+        double x = dot(q_dec + (size_t)h * D, kv_dec, D);
         double sx = s * x;
         double r = sx > 0.0 ? sx : 0.0;
         sum += (double)w_row[h] * r;
@@ -130,23 +159,35 @@ int oracle_mqa_logits(const uint8_t *q, const uint8_t *kv, const float *kv_scale
         return -1;
     if (compressed && ldo < 0)
         return -1;
-    for (int i = row_begin; i < row_end; ++i) {
+    double *q_dec = malloc(sizeof(double) * (size_t)H * D);
+    double *kv_dec = malloc(sizeof(double) * (size_t)D);
+    if (!q_dec || !kv_dec) {
+        free(q_dec);
+        free(kv_dec);
+        return -2;
+    }
+    int rc = 0;
+    for (int i = row_begin; i < row_end && rc == 0; ++i) {
         float *out = logits + (size_t)(i - row_begin) * (size_t)ldo;
         double *tout = tol ? tol + (size_t)(i - row_begin) * (size_t)ldo : NULL;
         int lo = k_start[i] < 0 ? 0 : k_start[i];
         int hi = k_end[i] > S_kv ? S_kv : k_end[i];
         if (hi < lo)
             hi = lo;
-        if (compressed && (int64_t)(hi - lo) > ldo)
-            return -1;
+        if (compressed && (int64_t)(hi - lo) > ldo) {
+            rc = -1;
+            break;
+        }
+        decode_row(q + (size_t)i * H * D, (size_t)H * D, q_dec);
         int64_t width = compressed ? ldo : S_kv;
         for (int64_t c = 0; c < width; ++c) {
             int j = compressed ? (int)(lo + c) : (int)c;
             int valid = compressed ? (c < hi - lo) : (j >= lo && j < hi);
             if (valid) {
                 double asum;
-                out[c] = one_logit(q + (size_t)i * H * D, kv + (size_t)j * D, (double)kv_scale[j],
-                                   weights + (size_t)i * H, H, D, &asum);
+                decode_row(kv + (size_t)j * D, (size_t)D, kv_dec);
+                out[c] = one_logit(q_dec, kv_dec, (double)kv_scale[j], weights + (size_t)i * H, H, D,
+                                   &asum);
                 if (tout)
                     tout[c] = 1e-3 * asum + 1e-5;
             } else if (clean) {
@@ -156,7 +197,9 @@ int oracle_mqa_logits(const uint8_t *q, const uint8_t *kv, const float *kv_scale
             }
         }
     }
-    return 0;
+    free(q_dec);
+    free(kv_dec);
+    return rc;
 }
 
 /*
@@ -186,11 +229,22 @@ int oracle_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_cache, const flo
         max_blocks_per_seq < 0 || ldo < width || row_begin < 0 || row_end > B * next_n ||
         row_begin > row_end || (flags & ORACLE_COMPRESSED))
         return -1;
-    for (int r = row_begin; r < row_end; ++r) {
+    double *q_dec = malloc(sizeof(double) * (size_t)H * D);
+    double *kv_dec = malloc(sizeof(double) * (size_t)D);
+    if (!q_dec || !kv_dec) {
+        free(q_dec);
+        free(kv_dec);
+        return -2;
+    }
+    int rc = 0;
+    for (int r = row_begin; r < row_end && rc == 0; ++r) {
         int b = r / next_n, t = r % next_n;
         int ctx = context_lens[b];
-        if (ctx < 0 || (int64_t)ctx > width)
-            return -1;
+        if (ctx < 0 || (int64_t)ctx > width) {
+            rc = -1;
+            break;
+        }
+        decode_row(q + (size_t)r * H * D, (size_t)H * D, q_dec);
         int end = ctx - next_n + t + 1;
         if (end < 0)
             end = 0;
@@ -199,12 +253,15 @@ int oracle_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_cache, const flo
         for (int64_t j = 0; j < width; ++j) {
             if (j < end) {
                 int32_t blk = block_table[(size_t)b * max_blocks_per_seq + j / block_kv];
-                if (blk < 0 || blk >= num_blocks)
-                    return -1;
+                if (blk < 0 || blk >= num_blocks) {
+                    rc = -1;
+                    break;
+                }
                 size_t tok = (size_t)blk * block_kv + (size_t)(j % block_kv);
                 double asum;
-                out[j] = one_logit(q + (size_t)r * H * D, kv_cache + tok * D, (double)kv_scales[tok],
-                                   weights + (size_t)r * H, H, D, &asum);
+                decode_row(kv_cache + tok * D, (size_t)D, kv_dec);
+                out[j] = one_logit(q_dec, kv_dec, (double)kv_scales[tok], weights + (size_t)r * H, H, D,
+                                   &asum);
                 if (tout)
                     tout[j] = 1e-3 * asum + 1e-5;
             } else if (clean) {
@@ -214,7 +271,9 @@ int oracle_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_cache, const flo
             }
         }
     }
-    return 0;
+    free(q_dec);
+    free(kv_dec);
+    return rc;
 }
 
 /*
