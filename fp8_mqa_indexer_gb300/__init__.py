@@ -1,5 +1,252 @@
 """GB300-native MQA logits scoring (the lightning-indexer step).
 
-The compute runs in the CUDA library ``libmqa.so`` built from ``csrc/``; this
-package is a thin binding over its C ABI (see ``include/mqa.h``).
+Thin Python binding over the C ABI of ``libmqa.so`` (declared in
+``include/mqa.h``).  Every function here only marshals arguments -- tensor
+pointers, sizes, strides, the current CUDA stream -- and calls the library with
+the same name; all arithmetic runs in the library's CUDA kernels.  There is no
+CPU fallback: if the library is missing or no GPU is present the calls raise.
+
+    logits = mqa_logits(q, kv, kv_scale, weights, k_start, k_end)          # dense
+    meta = paged_mqa_logits_metadata(context_lens, next_n=2, block_kv=64)  # paged
+    logits = paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens,
+                              block_table, meta)
 """
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+__all__ = [
+    "MQAError", "mqa_logits", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
+    "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
+    "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS",
+]
+
+MQA_CLEAN = 1
+MQA_COMPRESSED = 2
+MQA_CHECK_BOUNDS = 4
+
+STATUS_NAMES = {0: "MQA_OK", 1: "MQA_ERR_INVALID_ARG", 2: "MQA_ERR_UNSUPPORTED", 3: "MQA_ERR_CUDA",
+                4: "MQA_ERR_TIMEOUT", 5: "MQA_ERR_BAD_INPUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+_lock = threading.Lock()
+
+
+class MQAError(RuntimeError):
+    """A non-OK ``mqa_status`` from the library."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{self.status_name}: {message}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libmqa.so")
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libmqa.so (built by ``python -m fp8_mqa_indexer_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m fp8_mqa_indexer_gb300.build`"
+                               " (this package has no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        P, I, I64, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint
+        ULL = ctypes.c_ulonglong
+        sig = {
+            "mqa_logits": ([P, P, P, P, P, P, P, I, I, I, I, I64, U, P], I),
+            "paged_mqa_logits_metadata": ([P, I, I, I, I, P, P], I),
+            "paged_mqa_logits": ([P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I64, U, P], I),
+            "mqa_get_num_sms": ([I], I),
+            "mqa_device_status": ([P], I),
+            "mqa_set_wait_limit": ([ULL], I),
+            "mqa_selftest_wait_timeout": ([ULL, P], I),
+            "mqa_status_string": ([I], ctypes.c_char_p),
+            "mqa_last_error_message": ([], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = load_library().mqa_last_error_message().decode(errors="replace")
+        raise MQAError(status, msg)
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t, name: str, dtypes) -> None:
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _fp8_types():
+    import torch
+    return (torch.float8_e4m3fn, torch.uint8)
+
+
+def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: bool = True,
+               compressed: bool = False, ldo: Optional[int] = None, check_bounds: bool = False,
+               stream=None):
+    """Dense MQA logits (C ABI ``mqa_logits``).
+
+    q [S_q, H, D] and kv [S_kv, D] are E4M3 (float8_e4m3fn or raw uint8 bytes),
+    kv_scale [S_kv] and weights [S_q, H] float32, k_start / k_end [S_q] int32.
+    Returns ``logits`` [S_q, ldo] float32 (allocated when not given; ``ldo``
+    defaults to S_kv and must be given for compressed output).
+    """
+    import torch
+    f8 = _fp8_types()
+    _dev(q, "q", f8)
+    _dev(kv, "kv", f8)
+    _dev(kv_scale, "kv_scale", (torch.float32,))
+    _dev(weights, "weights", (torch.float32,))
+    _dev(k_start, "k_start", (torch.int32,))
+    _dev(k_end, "k_end", (torch.int32,))
+    S_q, H, D = q.shape
+    S_kv = kv.shape[0]
+    if kv.dim() != 2 or kv.shape[1] != D or weights.shape != (S_q, H):
+        raise ValueError("shape mismatch between q, kv and weights")
+    if kv_scale.shape != (S_kv,) or k_start.shape != (S_q,) or k_end.shape != (S_q,):
+        raise ValueError("shape mismatch in kv_scale / k_start / k_end")
+    if logits is None:
+        if ldo is None:
+            if compressed:
+                raise ValueError("compressed output needs ldo (the longest range) or a logits buffer")
+            ldo = S_kv
+        logits = torch.empty((S_q, ldo), dtype=torch.float32, device=q.device)
+    else:
+        _dev_out = logits
+        if not (_dev_out.is_cuda and _dev_out.dtype == torch.float32 and _dev_out.dim() == 2
+                and _dev_out.stride(1) == 1 and _dev_out.shape[0] == S_q):
+            raise ValueError("logits must be a CUDA float32 [S_q, ldo] matrix with unit column stride")
+        ldo = _dev_out.stride(0) if ldo is None else ldo
+    flags = (MQA_CLEAN if clean else 0) | (MQA_COMPRESSED if compressed else 0) | \
+            (MQA_CHECK_BOUNDS if check_bounds else 0)
+    with torch.cuda.device(q.device):
+        _check(load_library().mqa_logits(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights),
+                                         _ptr(k_start), _ptr(k_end), _ptr(logits), S_q, S_kv, H, D,
+                                         ldo, flags, _stream_handle(stream)))
+    return logits
+
+
+def get_num_sms(device=None) -> int:
+    import torch
+    dev = torch.cuda.current_device() if device is None else torch.device(device).index or 0
+    n = load_library().mqa_get_num_sms(dev)
+    if n < 0:
+        raise MQAError(3, "cannot query the SM count")
+    return n
+
+
+def paged_mqa_logits_metadata(context_lens, *, next_n: int, block_kv: int,
+                              num_sms: Optional[int] = None, out=None, stream=None):
+    """Paged work schedule (C ABI ``paged_mqa_logits_metadata``): an int32
+    [num_sms + 1, 2] tensor of (sequence, 128-key tile) start points."""
+    import torch
+    _dev(context_lens, "context_lens", (torch.int32,))
+    if num_sms is None:
+        num_sms = get_num_sms(context_lens.device)
+    if out is None:
+        out = torch.empty((num_sms + 1, 2), dtype=torch.int32, device=context_lens.device)
+    elif out.shape != (num_sms + 1, 2) or out.dtype != torch.int32 or not out.is_contiguous():
+        raise ValueError("schedule_meta must be a contiguous int32 [num_sms + 1, 2] tensor")
+    with torch.cuda.device(context_lens.device):
+        _check(load_library().paged_mqa_logits_metadata(_ptr(context_lens), context_lens.shape[0],
+                                                        next_n, block_kv, num_sms, _ptr(out),
+                                                        _stream_handle(stream)))
+    return out
+
+
+def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table, schedule_meta,
+                     logits=None, *, next_n: Optional[int] = None, clean: bool = True,
+                     check_bounds: bool = False, stream=None):
+    """Paged decode MQA logits (C ABI ``paged_mqa_logits``).
+
+    q [B*next_n, H, D] E4M3, kv_cache [num_blocks, block_kv, D] E4M3, kv_scales
+    [num_blocks, block_kv] f32, weights [B*next_n, H] f32, context_lens [B]
+    int32, block_table [B, max_blocks_per_seq] int32, schedule_meta from
+    ``paged_mqa_logits_metadata``.  Returns logits [B*next_n, ldo] f32 with
+    ldo >= max_blocks_per_seq * block_kv.
+    """
+    import torch
+    f8 = _fp8_types()
+    _dev(q, "q", f8)
+    _dev(kv_cache, "kv_cache", f8)
+    _dev(kv_scales, "kv_scales", (torch.float32,))
+    _dev(weights, "weights", (torch.float32,))
+    _dev(context_lens, "context_lens", (torch.int32,))
+    _dev(block_table, "block_table", (torch.int32,))
+    _dev(schedule_meta, "schedule_meta", (torch.int32,))
+    R, H, D = q.shape
+    B = context_lens.shape[0]
+    if next_n is None:
+        if B == 0 or R % B:
+            raise ValueError("cannot infer next_n from q and context_lens")
+        next_n = R // B
+    num_blocks, block_kv, D2 = kv_cache.shape
+    max_blocks = block_table.shape[1]
+    if D2 != D or R != B * next_n or weights.shape != (R, H) or kv_scales.shape != (num_blocks, block_kv):
+        raise ValueError("shape mismatch between paged inputs")
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per sequence")
+    num_sms = schedule_meta.shape[0] - 1
+    width = max_blocks * block_kv
+    if logits is None:
+        logits = torch.empty((R, width), dtype=torch.float32, device=q.device)
+    elif not (logits.dtype == torch.float32 and logits.dim() == 2 and logits.stride(1) == 1
+              and logits.shape[0] == R):
+        raise ValueError("logits must be a float32 [B*next_n, ldo] matrix with unit column stride")
+    ldo = logits.stride(0)
+    flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0)
+    with torch.cuda.device(q.device):
+        _check(load_library().paged_mqa_logits(_ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights),
+                                               _ptr(context_lens), _ptr(block_table), max_blocks,
+                                               _ptr(schedule_meta), _ptr(logits), B, next_n, H, D,
+                                               block_kv, num_blocks, num_sms, ldo, flags,
+                                               _stream_handle(stream)))
+    return logits
+
+
+def device_status(stream=None) -> int:
+    """Synchronize and return (and clear) the kernel status word as an
+    ``mqa_status`` code (0 = OK, 4 = a wait timed out, 5 = a bounds check failed)."""
+    return load_library().mqa_device_status(_stream_handle(stream))
+
+
+def set_wait_limit(cycles: int) -> None:
+    _check(load_library().mqa_set_wait_limit(cycles))
+
+
+def selftest_wait_timeout(cycles: int, stream=None) -> None:
+    _check(load_library().mqa_selftest_wait_timeout(cycles, _stream_handle(stream)))

@@ -1,0 +1,601 @@
+// mqa_api.cu -- the C ABI declared in include/mqa.h: argument validation, TMA
+// tensor-map encoding, the paged work-schedule kernel, the optional on-device
+// bounds check, the device status word, and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "mqa.h"
+#include "launch.h"
+
+using namespace mqa;
+
+// ------------------------------------------------------------ device state
+// Kernel status word (bit flags from ptx.cuh).  Lives in the module's global
+// memory: no allocation is made for it.
+__device__ unsigned g_mqa_status;
+
+namespace {
+
+thread_local char t_msg[512] = "";
+
+mqa_status fail(mqa_status s, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+mqa_status cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(MQA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::atomic<unsigned long long> g_wait_limit{4000000000ull};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int g_num_sms[kMaxDevices];
+unsigned* g_status_ptr[kMaxDevices];
+
+mqa_status device_state(int* dev_out, unsigned** status_out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(MQA_ERR_UNSUPPORTED, "device index %d too large", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_status_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_mqa_status);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        g_status_ptr[dev] = static_cast<unsigned*>(ptr);
+    }
+    if (!g_num_sms[dev]) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        g_num_sms[dev] = n;
+    }
+    *dev_out = dev;
+    *status_out = g_status_ptr[dev];
+    return MQA_OK;
+}
+
+// ---------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D map over a row-major [rows, cols] matrix of `esize`-byte elements with a
+// [box_rows, box_cols] box.
+mqa_status make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                       unsigned long long rows, unsigned long long cols, unsigned box_rows,
+                       unsigned box_cols, CUtensorMapSwizzle swz, const char* what)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * (unsigned long long)esize};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+    return MQA_OK;
+}
+
+mqa_status make_map_1d_f32(CUtensorMap* m, const void* base, unsigned long long n, unsigned box,
+                           const char* what)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[1] = {n};
+    cuuint32_t boxd[1] = {box};
+    cuuint32_t estr[1] = {1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<void*>(base), dims, nullptr,
+                    boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+    return MQA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// ---------------------------------------------------------- small kernels
+// Paged work schedule (see paged_mqa_logits_metadata in mqa.h).  One CTA:
+// each thread owns a contiguous chunk of sequences, a block-wide scan gives
+// the chunk's first unit, and each thread then emits the schedule entries whose
+// start unit falls inside its chunk.  With `check` set, entries are compared
+// with `meta` instead of written, and a mismatch raises kDevErrBadSchedule.
+constexpr int kMetaThreads = 1024;
+
+__global__ void __launch_bounds__(kMetaThreads)
+    paged_schedule_kernel(const int* __restrict__ ctx, int B, int num_sms, int* meta, int check,
+                          unsigned* status)
+{
+    __shared__ long long warp_tot[kMetaThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int chunk = (B + kMetaThreads - 1) / kMetaThreads;
+    const int c0 = min(tid * chunk, B), c1 = min(c0 + chunk, B);
+    long long local = 0;
+    for (int b = c0; b < c1; ++b)
+        local += paged_tiles(ctx[b]);
+    long long incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    if (lane == 31)
+        warp_tot[warp] = incl;
+    __syncthreads();
+    long long before = 0, U = 0;
+    for (int k = 0; k < kMetaThreads / 32; ++k) {
+        if (k < warp)
+            before += warp_tot[k];
+        U += warp_tot[k];
+    }
+    const long long P = before + incl - local;   // first unit of this chunk
+    auto emit = [&](int k, int b, int t) {
+        if (check) {
+            if (meta[2 * k] != b || meta[2 * k + 1] != t)
+                atomicOr(status, kDevErrBadSchedule);
+        } else {
+            meta[2 * k] = b;
+            meta[2 * k + 1] = t;
+        }
+    };
+    // entries whose start unit u_k = floor(k*U/num_sms) lies in [P, P + local)
+    if (local > 0) {
+        // smallest k with k*U >= P*num_sms
+        long long k = (P * num_sms + U - 1) / U;
+        int b = c0;
+        long long base = P;
+        for (; k <= num_sms; ++k) {
+            const long long u = k * U / num_sms;
+            if (u >= P + local)
+                break;
+            while (u >= base + paged_tiles(ctx[b])) {
+                base += paged_tiles(ctx[b]);
+                ++b;
+            }
+            emit((int)k, b, (int)(u - base));
+        }
+    }
+    // entries at u == U mark the end: (B, 0)
+    for (int k = tid; k <= num_sms; k += kMetaThreads) {
+        const long long u = U == 0 ? 0 : (long long)k * U / num_sms;
+        if (u >= U)
+            emit(k, B, 0);
+    }
+}
+
+__global__ void check_dense_kernel(const int* __restrict__ ks, const int* __restrict__ ke, int S_q,
+                                   int S_kv, long long ldo, int compressed, unsigned* status)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < S_q; i += gridDim.x * blockDim.x) {
+        const int a = ks[i], b = ke[i];
+        if (a < 0 || b > S_kv || a > b || (compressed && (long long)(b - a) > ldo))
+            atomicOr(status, kDevErrBadRange);
+    }
+}
+
+__global__ void check_paged_kernel(const int* __restrict__ ctx, const int* __restrict__ table, int B,
+                                   int max_blocks, int block_kv, int num_blocks, unsigned* status)
+{
+    const long long width = (long long)max_blocks * block_kv;
+    const long long total = (long long)B * max_blocks;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int b = (int)(e / max_blocks), pg = (int)(e % max_blocks);
+        const int c = ctx[b];
+        if (pg == 0 && (c < 0 || c > width))
+            atomicOr(status, kDevErrBadContext);
+        if (c > 0 && (long long)pg * block_kv < min((long long)c, width)) {
+            const int id = table[e];
+            if (id < 0 || id >= num_blocks)
+                atomicOr(status, kDevErrBadBlock);
+        }
+    }
+}
+
+__global__ void fill_rows_kernel(float* out, int rows, long long ldo, long long c0, long long c1)
+{
+    for (int r = blockIdx.x; r < rows; r += gridDim.x)
+        for (long long c = c0 + threadIdx.x; c < c1; c += blockDim.x)
+            out[r * ldo + c] = __int_as_float(0xff800000u);
+}
+
+__global__ void selftest_wait_kernel(long long limit, unsigned* status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    WaitCtx w{&abort_flag, status, limit};
+    if (threadIdx.x == 0)
+        wait_bounded(smem_u32(&bar), 0, w);   // nothing ever arrives
+    __syncthreads();
+}
+
+mqa_status read_and_clear_status(cudaStream_t stream, unsigned* value)
+{
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_mqa_status, sizeof(v));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyFromSymbol(status)");
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_mqa_status, &zero, sizeof(zero));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyToSymbol(status)");
+    }
+    *value = v;
+    return MQA_OK;
+}
+
+mqa_status status_from_word(unsigned v)
+{
+    if (v & kDevErrTimeout)
+        return fail(MQA_ERR_TIMEOUT, "a kernel wait ran out of its cycle budget");
+    if (v)
+        return fail(MQA_ERR_BAD_INPUT, "device bounds check failed (flags 0x%x)", v);
+    return MQA_OK;
+}
+
+int grid_for(int n)
+{
+    return n < 1 ? 1 : (n > 1184 ? 1184 : n);
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+extern "C" {
+
+const char* mqa_status_string(mqa_status s)
+{
+    switch (s) {
+    case MQA_OK: return "MQA_OK";
+    case MQA_ERR_INVALID_ARG: return "MQA_ERR_INVALID_ARG";
+    case MQA_ERR_UNSUPPORTED: return "MQA_ERR_UNSUPPORTED";
+    case MQA_ERR_CUDA: return "MQA_ERR_CUDA";
+    case MQA_ERR_TIMEOUT: return "MQA_ERR_TIMEOUT";
+    case MQA_ERR_BAD_INPUT: return "MQA_ERR_BAD_INPUT";
+    }
+    return "unknown mqa_status";
+}
+
+const char* mqa_last_error_message(void)
+{
+    return t_msg;
+}
+
+int mqa_get_num_sms(int device)
+{
+    if (device < 0 || device >= kMaxDevices)
+        return -1;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (g_num_sms[device])
+            return g_num_sms[device];
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return -1;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    g_num_sms[device] = n;
+    return n;
+}
+
+mqa_status mqa_set_wait_limit(unsigned long long cycles)
+{
+    g_wait_limit.store(cycles ? cycles : 4000000000ull);
+    return MQA_OK;
+}
+
+mqa_status mqa_device_status(mqa_stream_t stream)
+{
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+    unsigned v = 0;
+    s = read_and_clear_status((cudaStream_t)stream, &v);
+    if (s != MQA_OK)
+        return s;
+    return status_from_word(v);
+}
+
+mqa_status mqa_selftest_wait_timeout(unsigned long long cycles, mqa_stream_t stream)
+{
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+    selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)cycles, st);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MQA_OK : cuda_fail(e, "selftest launch");
+}
+
+mqa_status paged_mqa_logits_metadata(const int32_t* context_lens, int B, int next_n, int block_kv,
+                                     int num_sms, int32_t* schedule_meta, mqa_stream_t stream)
+{
+    if (B < 0 || next_n < 1 || num_sms < 1)
+        return fail(MQA_ERR_INVALID_ARG, "need B >= 0, next_n >= 1, num_sms >= 1");
+    if (block_kv != 32 && block_kv != 64 && block_kv != 128)
+        return fail(MQA_ERR_UNSUPPORTED, "block_kv must be 32, 64 or 128 (got %d)", block_kv);
+    if (!schedule_meta || (B > 0 && !context_lens))
+        return fail(MQA_ERR_INVALID_ARG, "null pointer");
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+    paged_schedule_kernel<<<1, kMetaThreads, 0, (cudaStream_t)stream>>>(context_lens, B, num_sms,
+                                                                        schedule_meta, 0, st);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MQA_OK : cuda_fail(e, "paged schedule launch");
+}
+
+mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, const float* weights,
+                      const int32_t* k_start, const int32_t* k_end, float* logits, int S_q,
+                      int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    const bool compressed = (flags & MQA_COMPRESSED) != 0;
+    const bool clean = (flags & MQA_CLEAN) != 0;
+    if (flags & ~(unsigned)(MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS))
+        return fail(MQA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+    if (S_q < 0 || S_kv < 0)
+        return fail(MQA_ERR_INVALID_ARG, "S_q and S_kv must be >= 0");
+    if (D != 64 && D != 128)
+        return fail(MQA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", D);
+    if (H != 8 && H != 32 && H != 64)
+        return fail(MQA_ERR_UNSUPPORTED, "H must be 8, 32 or 64 (got %d)", H);
+    if ((long long)S_q * H >= INT_MAX)
+        return fail(MQA_ERR_INVALID_ARG, "S_q * H too large");
+    if (!compressed && ldo < S_kv)
+        return fail(MQA_ERR_INVALID_ARG, "ldo (%lld) < S_kv (%d)", (long long)ldo, S_kv);
+    if (compressed && ldo < 1)
+        return fail(MQA_ERR_INVALID_ARG, "compressed output needs ldo >= 1");
+    if (S_q == 0)
+        return MQA_OK;
+    if (!q || !weights || !k_start || !k_end || !logits || (S_kv > 0 && (!kv || !kv_scale)))
+        return fail(MQA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(q, 16) || !aligned(weights, 16) || (S_kv > 0 && (!aligned(kv, 16) ||
+                                                                   !aligned(kv_scale, 16))))
+        return fail(MQA_ERR_INVALID_ARG, "q, kv, kv_scale and weights must be 16-byte aligned");
+    if (!aligned(logits, 4) || !aligned(k_start, 4) || !aligned(k_end, 4))
+        return fail(MQA_ERR_INVALID_ARG, "logits, k_start, k_end must be 4-byte aligned");
+
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+    const int num_sms = g_num_sms[dev];
+
+    if (flags & MQA_CHECK_BOUNDS) {
+        unsigned v = 0;
+        s = read_and_clear_status(stream, &v);   // start from a clean word
+        if (s != MQA_OK)
+            return s;
+        check_dense_kernel<<<grid_for((S_q + 255) / 256), 256, 0, stream>>>(
+            k_start, k_end, S_q, S_kv, (long long)ldo, compressed, st);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "bounds-check launch");
+        s = read_and_clear_status(stream, &v);
+        if (s != MQA_OK)
+            return s;
+        if (v)
+            return fail(MQA_ERR_BAD_INPUT, "a row range is outside [0, S_kv] or longer than ldo");
+    }
+
+    if (S_kv == 0) {
+        // no keys: every row is empty; only compressed clean rows have padding
+        if (compressed && clean) {
+            fill_rows_kernel<<<grid_for(S_q), 256, 0, stream>>>(logits, S_q, (long long)ldo, 0,
+                                                                (long long)ldo);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess)
+                return cuda_fail(e, "fill launch");
+        }
+        return MQA_OK;
+    }
+
+    LaunchArgs a;
+    memset(&a, 0, sizeof(a));
+    const int tok = kMaxN / H;
+    const int N = tok * H;
+    const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if ((s = make_map_2d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (unsigned long long)S_q * H, D,
+                         N, D, swz, "q")) != MQA_OK ||
+        (s = make_map_2d(&a.tm_kv, kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, S_kv, D, kBlockKV, D, swz,
+                         "kv")) != MQA_OK ||
+        (s = make_map_1d_f32(&a.tm_scale, kv_scale, S_kv, kBlockKV, "kv_scale")) != MQA_OK ||
+        (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, S_q, H, tok, H,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, "weights")) != MQA_OK)
+        return s;
+    Params& p = a.p;
+    p.logits = logits;
+    p.ldo = ldo;
+    p.flags = (clean ? kFlagClean : 0u) | (compressed ? kFlagCompressed : 0u);
+    p.S_q = S_q;
+    p.S_kv = S_kv;
+    p.k_start = k_start;
+    p.k_end = k_end;
+    p.width = S_kv;
+    p.tok = tok;
+    p.num_q_blocks = (S_q + tok - 1) / tok;
+    p.rows = S_q;
+    p.wait_limit = (long long)g_wait_limit.load();
+    p.status = st;
+    a.grid = num_sms;
+    a.stream = stream;
+    cudaError_t e = launch_dense(H, D, a);
+    if (e == cudaErrorNotSupported)
+        return fail(MQA_ERR_UNSUPPORTED, "no dense kernel for H=%d D=%d", H, D);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "dense kernel launch");
+    return MQA_OK;
+}
+
+mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv_scales,
+                            const float* weights, const int32_t* context_lens,
+                            const int32_t* block_table, int max_blocks_per_seq,
+                            const int32_t* schedule_meta, float* logits, int B, int next_n, int H,
+                            int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
+                            unsigned flags, mqa_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (flags & ~(unsigned)(MQA_CLEAN | MQA_CHECK_BOUNDS))
+        return fail((flags & MQA_COMPRESSED) ? MQA_ERR_UNSUPPORTED : MQA_ERR_INVALID_ARG,
+                    "paged logits take only MQA_CLEAN and MQA_CHECK_BOUNDS (flags 0x%x)", flags);
+    if (B < 0 || next_n < 1 || num_blocks < 1 || max_blocks_per_seq < 1 || num_sms < 1)
+        return fail(MQA_ERR_INVALID_ARG,
+                    "need B >= 0, next_n >= 1, num_blocks >= 1, max_blocks_per_seq >= 1, num_sms >= 1");
+    if (D != 64 && D != 128)
+        return fail(MQA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", D);
+    if (H != 16 && H != 32 && H != 64)
+        return fail(MQA_ERR_UNSUPPORTED, "H must be 16, 32 or 64 (got %d)", H);
+    if (next_n * H > kMaxN || (next_n * H) % 16 != 0)
+        return fail(MQA_ERR_UNSUPPORTED, "next_n * H must be a multiple of 16 and <= 256");
+    if (block_kv != 32 && block_kv != 64 && block_kv != 128)
+        return fail(MQA_ERR_UNSUPPORTED, "block_kv must be 32, 64 or 128 (got %d)", block_kv);
+    const long long width = (long long)max_blocks_per_seq * block_kv;
+    if (ldo < width)
+        return fail(MQA_ERR_INVALID_ARG, "ldo (%lld) < max_blocks_per_seq * block_kv (%lld)",
+                    (long long)ldo, width);
+    if (width >= INT_MAX || (long long)num_blocks * block_kv >= INT_MAX ||
+        (long long)B * next_n * H >= INT_MAX)
+        return fail(MQA_ERR_INVALID_ARG, "size too large");
+    if (B == 0)
+        return MQA_OK;
+    if (!q || !kv_cache || !kv_scales || !weights || !context_lens || !block_table ||
+        !schedule_meta || !logits)
+        return fail(MQA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(kv_scales, 16) || !aligned(weights, 16))
+        return fail(MQA_ERR_INVALID_ARG,
+                    "q, kv_cache, kv_scales and weights must be 16-byte aligned");
+    if (!aligned(logits, 4) || !aligned(context_lens, 4) || !aligned(block_table, 4) ||
+        !aligned(schedule_meta, 4))
+        return fail(MQA_ERR_INVALID_ARG, "int and float arrays must be 4-byte aligned");
+
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+
+    if (flags & MQA_CHECK_BOUNDS) {
+        unsigned v = 0;
+        s = read_and_clear_status(stream, &v);
+        if (s != MQA_OK)
+            return s;
+        const long long total = (long long)B * max_blocks_per_seq;
+        check_paged_kernel<<<grid_for((int)min(total / 256 + 1, 100000LL)), 256, 0, stream>>>(
+            context_lens, block_table, B, max_blocks_per_seq, block_kv, num_blocks, st);
+        paged_schedule_kernel<<<1, kMetaThreads, 0, stream>>>(
+            context_lens, B, num_sms, const_cast<int32_t*>(schedule_meta), 1, st);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "bounds-check launch");
+        s = read_and_clear_status(stream, &v);
+        if (s != MQA_OK)
+            return s;
+        if (v)
+            return fail(MQA_ERR_BAD_INPUT,
+                        "bad paged input (flags 0x%x: 4 context length, 8 block id, 16 schedule)", v);
+    }
+
+    LaunchArgs a;
+    memset(&a, 0, sizeof(a));
+    const int N = next_n * H;
+    const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if ((s = make_map_2d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                         (unsigned long long)B * next_n * H, D, N, D, swz, "q")) != MQA_OK ||
+        (s = make_map_2d(&a.tm_kv, kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                         (unsigned long long)num_blocks * block_kv, D, block_kv, D, swz,
+                         "kv_cache")) != MQA_OK ||
+        (s = make_map_1d_f32(&a.tm_scale, kv_scales, (unsigned long long)num_blocks * block_kv,
+                             block_kv, "kv_scales")) != MQA_OK ||
+        (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                         (unsigned long long)B * next_n, H, next_n, H, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         "weights")) != MQA_OK)
+        return s;
+    Params& p = a.p;
+    p.logits = logits;
+    p.ldo = ldo;
+    p.flags = (flags & MQA_CLEAN) ? kFlagClean : 0u;
+    p.context_lens = context_lens;
+    p.block_table = block_table;
+    p.schedule_meta = schedule_meta;
+    p.B = B;
+    p.next_n = next_n;
+    p.block_kv = block_kv;
+    p.max_blocks = max_blocks_per_seq;
+    p.width = width;
+    p.tok = next_n;
+    p.num_q_blocks = B;
+    p.rows = B * next_n;
+    p.wait_limit = (long long)g_wait_limit.load();
+    p.status = st;
+    a.grid = num_sms;
+    a.stream = stream;
+    cudaError_t e = launch_paged(H, D, a);
+    if (e == cudaErrorNotSupported)
+        return fail(MQA_ERR_UNSUPPORTED, "no paged kernel for H=%d D=%d", H, D);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "paged kernel launch");
+    return MQA_OK;
+}
+
+}  // extern "C"

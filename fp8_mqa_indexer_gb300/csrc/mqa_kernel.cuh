@@ -1,0 +1,693 @@
+// mqa_kernel.cuh -- the MQA logits kernel for sm_103a (dense and paged KV).
+//
+// What it computes ("How to Implement MQA (Multi-Query Attention) Logits
+// Computation with DeepGEMM", section "Core Architecture Components"): for
+// query token i and key j in its range,
+//     logits[i, j] = sum_h w[i,h] * ReLU(s[j] * <q[i,h,:], kv[j,:]>)
+// with E4M3 q/kv, fp32 per-key scale s and per-head weight w, fp32 output, and
+// -inf outside the range in clean mode ("[PR #435] Improve SM100 MX MQA logits
+// clean-output performance", section "Standalone performance reproducer").
+//
+// Design (this library's own, for GB300):
+//  * Keys sit on the MMA M dimension: one 128-key tile of kv is the A operand
+//    (128 TMEM lanes = 128 keys) and a block of `tok` query tokens x H heads is
+//    the B operand (N = tok * H <= 256 columns).  Both are K-major (D
+//    contiguous) exactly as they lie in HBM, so TMA copies them unchanged into
+//    swizzled shared memory and tcgen05.mma (kind::f8f6f4, E4M3 x E4M3 -> F32)
+//    accumulates x[key, (token, head)] in TMEM.
+//  * Epilogue threads each own one key (one TMEM lane) and reduce over heads in
+//    registers: acc = sum_h w[h] * max(x, 0), then multiply by s[j] once (exact
+//    rewrite of ReLU(s x) for s >= 0; warps that see a negative scale take a
+//    second path that keeps the literal ReLU(s x)).  For a fixed token the 128
+//    threads of a warp group write 128 consecutive floats: coalesced rows.
+//  * One persistent CTA per SM walks a contiguous slice of the (query block,
+//    key tile) work list: dense slices come from an in-kernel prefix sum over
+//    the query blocks; paged slices come from the schedule written by
+//    paged_mqa_logits_metadata.
+//  * Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+//    owner, warps 2-3 write -inf into the columns no tile covers (clean mode),
+//    warps 4-11 are two epilogue warp groups splitting the N columns.
+//  * Pipelines: a ring of key tiles (+ their scales and a small work record),
+//    two query-block buffers (+ weights and per-token ranges) and two TMEM
+//    accumulators of 256 columns; every hand-off is an mbarrier, every wait is
+//    bounded (ptx.cuh, wait_bounded).
+#pragma once
+#include <climits>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace mqa {
+
+constexpr int kBlockKV = 128;      // keys per tile == MMA M == TMEM lanes
+constexpr int kMaxN = 256;         // TMEM columns per accumulator buffer
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;       // epilogue warps 4..11
+constexpr int kNumEpiWarps = 8;
+
+enum : unsigned { kFlagClean = 1u, kFlagCompressed = 2u };
+enum : int { kFirstOfBlock = 1, kLastOfBlock = 2 };
+
+struct UnitInfo {
+    int b;        // query block (dense) or sequence (paged)
+    int t;        // key tile: keys [t*128, t*128+128)
+    int qbuf;     // which query-block buffer holds block b
+    int flags;    // kFirstOfBlock | kLastOfBlock (within this CTA's slice)
+};
+
+struct Params {
+    float* logits;
+    long long ldo;
+    unsigned flags;
+    // dense
+    int S_q;
+    int S_kv;
+    const int* k_start;
+    const int* k_end;
+    // paged
+    const int* context_lens;
+    const int* block_table;
+    const int* schedule_meta;
+    int B;
+    int next_n;
+    int block_kv;
+    int max_blocks;
+    // shared
+    long long width;     // logical columns of an uncompressed row
+    int tok;             // query tokens per work unit
+    int num_q_blocks;    // dense: ceil(S_q / tok); paged: B
+    int rows;            // output rows: S_q or B * next_n
+    long long wait_limit;
+    unsigned* status;
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int kStages = (D == 128) ? 8 : 12;
+    static constexpr int kKVTileBytes = kBlockKV * D;
+    static constexpr int kQTileBytes = kMaxN * D;
+};
+
+template <int D>
+struct __align__(1024) Smem {
+    uint8_t q[2][Cfg<D>::kQTileBytes];
+    uint8_t kv[Cfg<D>::kStages][Cfg<D>::kKVTileBytes];
+    float scale[Cfg<D>::kStages][kBlockKV];
+    float w[2][kMaxN];
+    int2 range[2][32];
+    UnitInfo info[Cfg<D>::kStages];
+    uint64_t full[Cfg<D>::kStages];
+    uint64_t empty[Cfg<D>::kStages];
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int start_b;
+    int start_t;
+    int n_units;
+    long long scan[kThreads / 32];
+};
+
+// ----------------------------------------------------------------- ranges
+// Dense range of row i, intersected with [0, S_kv): returns [lo, hi), lo <= hi.
+__device__ __forceinline__ int2 dense_range(const Params& p, int i)
+{
+    int lo = min(max(__ldg(p.k_start + i), 0), p.S_kv);
+    int hi = min(max(__ldg(p.k_end + i), lo), p.S_kv);
+    return make_int2(lo, hi);
+}
+
+// Paged range of token t of sequence with context ctx: [0, ctx - next_n + t + 1)
+// intersected with [0, width).
+__device__ __forceinline__ int2 paged_range(const Params& p, int ctx, int t)
+{
+    long long hi = (long long)ctx - p.next_n + t + 1;
+    hi = hi < 0 ? 0 : (hi > p.width ? p.width : hi);
+    return make_int2(0, (int)hi);
+}
+
+__device__ __forceinline__ int paged_tiles(int ctx)
+{
+    return ctx > 0 ? (ctx + kBlockKV - 1) / kBlockKV : 0;
+}
+
+// Key tiles [tlo, thi) touched by dense query block b (one thread).
+__device__ __forceinline__ void dense_block_tiles(const Params& p, int b, int& tlo, int& thi)
+{
+    const int r0 = b * p.tok;
+    const int r1 = min(r0 + p.tok, p.S_q);
+    int mn = INT_MAX, mx = 0;
+    for (int i = r0; i < r1; ++i) {
+        int2 r = dense_range(p, i);
+        if (r.y > r.x) {
+            mn = min(mn, r.x);
+            mx = max(mx, r.y);
+        }
+    }
+    if (mx == 0) {
+        tlo = thi = 0;
+    } else {
+        tlo = mn / kBlockKV;
+        thi = (mx + kBlockKV - 1) / kBlockKV;
+    }
+}
+
+// Same, cooperatively by a full warp (tok <= 32); lane k also returns token
+// k's range in `mine`.
+__device__ __forceinline__ void dense_block_tiles_warp(const Params& p, int b, int lane, int& tlo,
+                                                       int& thi, int2& mine)
+{
+    const int i = b * p.tok + lane;
+    int2 r = make_int2(0, 0);
+    if (lane < p.tok && i < p.S_q)
+        r = dense_range(p, i);
+    mine = r;
+    const bool ne = r.y > r.x;
+    const int mn = __reduce_min_sync(0xffffffffu, ne ? r.x : INT_MAX);
+    const int mx = __reduce_max_sync(0xffffffffu, ne ? r.y : 0);
+    if (mx == 0) {
+        tlo = thi = 0;
+    } else {
+        tlo = mn / kBlockKV;
+        thi = (mx + kBlockKV - 1) / kBlockKV;
+    }
+}
+
+__device__ __forceinline__ long long block_units(const Params& p, bool paged, int b)
+{
+    if (paged)
+        return paged_tiles(__ldg(p.context_lens + b));
+    int tlo, thi;
+    dense_block_tiles(p, b, tlo, thi);
+    return thi - tlo;
+}
+
+// -------------------------------------------------------- -inf fill of rows
+// Writes -inf to row[c0, c1) with one warp: scalar head to a 16-byte boundary,
+// float4 body, scalar tail.
+__device__ __forceinline__ void warp_fill_neg_inf(float* row, long long c0, long long c1, int lane)
+{
+    if (c0 >= c1)
+        return;
+    const float ninf = __int_as_float(0xff800000u);
+    const long long mis = (long long)((reinterpret_cast<uintptr_t>(row + c0) >> 2) & 3u);
+    const long long head = min((4 - mis) & 3, c1 - c0);
+    if (lane < head)
+        row[c0 + lane] = ninf;
+    long long a = c0 + head;
+    const long long nvec = (c1 - a) >> 2;
+    float4* v = reinterpret_cast<float4*>(row + a);
+    const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
+    for (long long k = lane; k < nvec; k += 32)
+        v[k] = f4;
+    a += nvec << 2;
+    if (lane < c1 - a)
+        row[a + lane] = ninf;
+}
+
+// A bounded wait taken by a whole warp: every lane gets the same answer, so a
+// timeout never splits the warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w)
+{
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, w));
+}
+
+// ------------------------------------------------------------------ kernel
+template <int H, int D, bool PAGED>
+__global__ void __launch_bounds__(kThreads, 1)
+    mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_kv,
+                      const __grid_constant__ CUtensorMap tm_scale,
+                      const __grid_constant__ CUtensorMap tm_w, const Params p)
+{
+    using C = Cfg<D>;
+    constexpr int S = C::kStages;
+    constexpr int kTPWMax = 128 / H;               // tokens per epilogue warp group, max
+    constexpr int kNP = (H >= 32) ? 4 : 1;         // partial accumulators per token
+    static_assert(H >= 8 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two in [8,128]");
+    static_assert(D == 64 || D == 128, "D must be 64 or 128");
+
+    extern __shared__ uint8_t smem_raw[];
+    Smem<D>& sm = *reinterpret_cast<Smem<D>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int G = gridDim.x;
+    const int cta = blockIdx.x;
+    const int N = p.tok * H;
+
+    // ------------------------------------------------------------ set-up
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1 + kNumEpiWarps);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(smem_u32(&sm.q_full[k]), 1);
+            mbar_init(smem_u32(&sm.q_empty[k]), 1 + kNumEpiWarps);
+            mbar_init(smem_u32(&sm.acc_full[k]), 1);
+            mbar_init(smem_u32(&sm.acc_empty[k]), kNumEpiWarps);
+        }
+        mbar_init(smem_u32(&sm.mma_done), 1);
+        sm.abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_kv);
+        tma_prefetch_desc(&tm_scale);
+        tma_prefetch_desc(&tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sm.tmem_base), 512);
+        tmem_relinquish();
+    }
+
+    // Work slice of this CTA: start (block, tile) and number of units.
+    if (!PAGED) {
+        // Prefix sum of per-block tile counts over all threads, then locate
+        // units [cta*U/G, (cta+1)*U/G).
+        const int NB = p.num_q_blocks;
+        const int chunk = (NB + kThreads - 1) / kThreads;
+        const int b_lo = min(tid * chunk, NB);
+        const int b_hi = min(b_lo + chunk, NB);
+        long long local = 0;
+        for (int b = b_lo; b < b_hi; ++b)
+            local += block_units(p, false, b);
+        long long incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += v;
+        }
+        if (lane == 31)
+            sm.scan[warp] = incl;
+        __syncthreads();
+        long long before = 0, total = 0;
+        for (int k = 0; k < kThreads / 32; ++k) {
+            if (k < warp)
+                before += sm.scan[k];
+            total += sm.scan[k];
+        }
+        const long long excl = before + incl - local;
+        const long long u0 = (long long)cta * total / G;
+        const long long u1 = (long long)(cta + 1) * total / G;
+        if (tid == 0)
+            sm.n_units = (int)(u1 - u0);
+        if (u0 < u1 && u0 >= excl && u0 < excl + local) {
+            long long acc = excl;
+            for (int b = b_lo; b < b_hi; ++b) {
+                int tlo, thi;
+                dense_block_tiles(p, b, tlo, thi);
+                if (u0 < acc + (thi - tlo)) {
+                    sm.start_b = b;
+                    sm.start_t = tlo + (int)(u0 - acc);
+                    break;
+                }
+                acc += thi - tlo;
+            }
+        }
+    } else {
+        const int b0 = __ldg(p.schedule_meta + 2 * cta);
+        const int t0 = __ldg(p.schedule_meta + 2 * cta + 1);
+        const int b1 = __ldg(p.schedule_meta + 2 * cta + 2);
+        const int t1 = __ldg(p.schedule_meta + 2 * cta + 3);
+        bool ok = b0 >= 0 && b0 <= b1 && b1 <= p.B && t0 >= 0 && t1 >= 0;
+        if (ok)
+            ok = (b0 < p.B ? t0 <= paged_tiles(__ldg(p.context_lens + b0)) : t0 == 0) &&
+                 (b1 < p.B ? t1 <= paged_tiles(__ldg(p.context_lens + b1)) : t1 == 0) &&
+                 (b0 < b1 || t0 <= t1);
+        if (!ok && tid == 0)
+            atomicOr(p.status, kDevErrBadSchedule);
+        long long local = 0;
+        if (ok)
+            for (int b = b0 + tid; b < b1; b += kThreads)
+                local += paged_tiles(__ldg(p.context_lens + b));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            local += __shfl_xor_sync(0xffffffffu, local, o);
+        if (lane == 0)
+            sm.scan[warp] = local;
+        __syncthreads();
+        if (tid == 0) {
+            long long tot = 0;
+            for (int k = 0; k < kThreads / 32; ++k)
+                tot += sm.scan[k];
+            long long n = ok ? tot - t0 + t1 : 0;
+            sm.n_units = (int)(n > 0 ? n : 0);
+            sm.start_b = b0;
+            sm.start_t = t0;
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = sm.tmem_base;
+    const int n_units = sm.n_units;
+    WaitCtx wctx{&sm.abort_flag, p.status, p.wait_limit};
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        regs_dec<56>();
+        int b = sm.start_b;
+        int t = sm.start_t;
+        int k_block = 0;
+        int tlo = 0, thi = 0;
+        int2 myrange = make_int2(0, 0);
+        int ctx = 0;
+        // page-id window (paged): lane L holds the physical block of logical
+        // pages wbase+L (win0) and wbase+32+L (win1, prefetched).
+        int wbase = 0, win0 = -1, win1 = -1, npages = 0;
+        const int ppt = PAGED ? kBlockKV / p.block_kv : 1;
+        auto page_id = [&](int pg) -> int {
+            return (pg >= 0 && pg < npages)
+                       ? __ldg(p.block_table + (long long)b * p.max_blocks + pg)
+                       : -1;
+        };
+        auto enter_block = [&]() {
+            if (PAGED) {
+                ctx = b < p.B ? max(__ldg(p.context_lens + b), 0) : 0;
+                tlo = 0;
+                thi = paged_tiles(ctx);
+                myrange = (lane < p.tok) ? paged_range(p, ctx, lane) : make_int2(0, 0);
+                npages = min((int)((min((long long)ctx, p.width) + p.block_kv - 1) / p.block_kv),
+                             p.max_blocks);
+                wbase = (t * ppt) & ~31;
+                win0 = page_id(wbase + lane);
+                win1 = page_id(wbase + 32 + lane);
+            } else {
+                dense_block_tiles_warp(p, b, lane, tlo, thi, myrange);
+            }
+        };
+        if (n_units > 0)
+            enter_block();
+        bool first = true;
+        int n_issued = 0, q_issued = 0;
+        for (int u = 0; u < n_units; ++u) {
+            if (first) {
+                const int qb = k_block & 1;
+                if (!warp_wait(smem_u32(&sm.q_empty[qb]), ((k_block >> 1) & 1) ^ 1, wctx))
+                    break;
+                if (lane < p.tok)
+                    sm.range[qb][lane] = myrange;
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t bar = smem_u32(&sm.q_full[qb]);
+                    mbar_arrive_expect_tx(bar, (uint32_t)(N * D + p.tok * H * 4));
+                    tma_load_2d(smem_u32(sm.q[qb]), &tm_q, bar, 0, b * N);
+                    tma_load_2d(smem_u32(sm.w[qb]), &tm_w, bar, 0, b * p.tok);
+                }
+                ++q_issued;
+            }
+            const int stage = u % S;
+            if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx))
+                break;
+            const bool last = (u + 1 == n_units) || (t + 1 >= thi);
+            const UnitInfo info{b, t, k_block & 1,
+                                (first ? kFirstOfBlock : 0) | (last ? kLastOfBlock : 0)};
+            if (PAGED) {
+                // gather the pages of tile t through the block table
+                const long long keys = min((long long)ctx, p.width);
+                int ids[4];
+                uint32_t bytes = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    ids[k] = -1;
+                    if (k < ppt) {
+                        const int pg = t * ppt + k;
+                        if (pg < wbase || pg >= wbase + 32) {   // not sequential: reload
+                            wbase = pg & ~31;
+                            win0 = page_id(wbase + lane);
+                            win1 = page_id(wbase + 32 + lane);
+                        }
+                        const int id = __shfl_sync(0xffffffffu, win0, pg - wbase);
+                        if ((long long)pg * p.block_kv < keys && pg < p.max_blocks) {
+                            ids[k] = id;
+                            bytes += (uint32_t)(p.block_kv * (D + 4));
+                        }
+                    }
+                }
+                if (lane == 0) {
+                    sm.info[stage] = info;
+                    const uint32_t bar = smem_u32(&sm.full[stage]);
+                    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (k < ppt && ids[k] >= 0) {
+                            tma_load_2d(smem_u32(sm.kv[stage]) + k * p.block_kv * D, &tm_kv, bar, 0,
+                                        ids[k] * p.block_kv);
+                            tma_load_1d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale, bar,
+                                        ids[k] * p.block_kv);
+                        }
+                    }
+                }
+                // slide the window: the prefetched half becomes current
+                if ((t + 1) * ppt >= wbase + 32) {
+                    wbase += 32;
+                    win0 = win1;
+                    win1 = page_id(wbase + 32 + lane);
+                }
+            } else {
+                if (lane == 0) {
+                    sm.info[stage] = info;
+                    const uint32_t bar = smem_u32(&sm.full[stage]);
+                    mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * D + kBlockKV * 4));
+                    tma_load_2d(smem_u32(sm.kv[stage]), &tm_kv, bar, 0, t * kBlockKV);
+                    tma_load_1d(smem_u32(sm.scale[stage]), &tm_scale, bar, t * kBlockKV);
+                }
+            }
+            ++n_issued;
+            // advance to the next unit, skipping blocks with no work
+            first = false;
+            ++t;
+            if (t >= thi && u + 1 < n_units) {
+                do {
+                    ++b;
+                    t = 0;
+                    enter_block();
+                    t = tlo;
+                } while (thi <= tlo && b + 1 < p.num_q_blocks);
+                if (thi <= tlo)   // ran off the end: the slice disagrees with the inputs
+                    break;
+                ++k_block;
+                first = true;
+            }
+        }
+        // Drain: every copy this warp issued must have landed before exit.
+        if (lane == 0) {
+            for (int u = max(0, n_issued - S); u < n_issued; ++u)
+                wait_bounded(smem_u32(&sm.full[u % S]), (u / S) & 1, wctx);
+            for (int k = max(0, q_issued - 2); k < q_issued; ++k)
+                wait_bounded(smem_u32(&sm.q_full[k & 1]), (k >> 1) & 1, wctx);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        regs_dec<56>();
+        if (lane == 0) {
+            const uint32_t idesc = idesc_e4m3_f32(kBlockKV, (uint32_t)N);
+            int k_block = -1;
+            for (int u = 0; u < n_units; ++u) {
+                const int stage = u % S;
+                if (!wait_bounded(smem_u32(&sm.full[stage]), (u / S) & 1, wctx))
+                    break;
+                const UnitInfo info = sm.info[stage];
+                if (info.flags & kFirstOfBlock) {
+                    ++k_block;
+                    if (!wait_bounded(smem_u32(&sm.q_full[info.qbuf]), (k_block >> 1) & 1, wctx))
+                        break;
+                }
+                const int buf = u & 1;
+                if (!wait_bounded(smem_u32(&sm.acc_empty[buf]), ((u >> 1) & 1) ^ 1, wctx))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kMaxN);
+                const uint32_t a0 = smem_u32(sm.kv[stage]);
+                const uint32_t b0 = smem_u32(sm.q[info.qbuf]);
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k)
+                    mma_f8f6f4(d_tmem, smem_desc(a0 + 32 * k, D), smem_desc(b0 + 32 * k, D), idesc,
+                               k > 0 ? 1u : 0u);
+                mma_commit(smem_u32(&sm.empty[stage]));
+                mma_commit(smem_u32(&sm.acc_full[buf]));
+                if (info.flags & kLastOfBlock)
+                    mma_commit(smem_u32(&sm.q_empty[info.qbuf]));
+            }
+            // every MMA issued above has completed once this barrier flips
+            mma_commit(smem_u32(&sm.mma_done));
+            wait_bounded(smem_u32(&sm.mma_done), 0, wctx);
+        }
+        __syncwarp();
+    } else if (warp < kEpiWarp0) {
+        // ================================================= -inf fill
+        regs_dec<56>();
+        if (p.flags & kFlagClean) {
+            const int fw = warp - 2;   // 0 or 1
+            for (int r = cta + fw * G; r < p.rows; r += 2 * G) {
+                float* row = p.logits + (long long)r * p.ldo;
+                if (PAGED) {
+                    const int c = max(__ldg(p.context_lens + r / p.next_n), 0);
+                    const long long covered = min((long long)paged_tiles(c) * kBlockKV, p.width);
+                    warp_fill_neg_inf(row, covered, p.width, lane);
+                } else if (p.flags & kFlagCompressed) {
+                    const int2 rg = dense_range(p, r);
+                    warp_fill_neg_inf(row, (long long)(rg.y - rg.x), p.ldo, lane);
+                } else {
+                    int tlo, thi;
+                    int2 mine;
+                    dense_block_tiles_warp(p, r / p.tok, lane, tlo, thi, mine);
+                    if (thi <= tlo) {
+                        warp_fill_neg_inf(row, 0, p.S_kv, lane);
+                    } else {
+                        warp_fill_neg_inf(row, 0, (long long)tlo * kBlockKV, lane);
+                        warp_fill_neg_inf(row, min((long long)thi * kBlockKV, (long long)p.S_kv),
+                                          p.S_kv, lane);
+                    }
+                }
+            }
+        }
+    } else {
+        // ================================================= epilogue
+        regs_inc<224>();
+        const int g = (warp - kEpiWarp0) >> 2;         // warp group 0 / 1
+        const int quad = warp & 3;                      // TMEM lane quadrant
+        const int row = quad * 32 + lane;               // key within the tile
+        const int tok_lo = (p.tok + 1) >> 1;
+        const int tok0 = g == 0 ? 0 : tok_lo;
+        const int ntok = g == 0 ? tok_lo : p.tok - tok_lo;
+        const int col0 = tok0 * H;
+        const int ncols = ntok * H;
+        const bool clean = (p.flags & kFlagClean) != 0;
+        const bool compressed = (p.flags & kFlagCompressed) != 0;
+        const float ninf = __int_as_float(0xff800000u);
+        float wr[128];
+#pragma unroll
+        for (int k = 0; k < 128; ++k)
+            wr[k] = 0.f;
+        int k_block = -1;
+        int qb = 0;
+        for (int u = 0; u < n_units; ++u) {
+            const int stage = u % S;
+            if (!warp_wait(smem_u32(&sm.full[stage]), (u / S) & 1, wctx))
+                break;
+            const UnitInfo info = sm.info[stage];
+            const float s = sm.scale[stage][row];
+            if (info.flags & kFirstOfBlock) {
+                ++k_block;
+                qb = info.qbuf;
+                if (!warp_wait(smem_u32(&sm.q_full[qb]), (k_block >> 1) & 1, wctx))
+                    break;
+                const float4* w4 = reinterpret_cast<const float4*>(&sm.w[qb][col0]);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    if (4 * k < ncols) {
+                        const float4 v = w4[k];
+                        wr[4 * k] = v.x;
+                        wr[4 * k + 1] = v.y;
+                        wr[4 * k + 2] = v.z;
+                        wr[4 * k + 3] = v.w;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&sm.empty[stage]));
+
+            const int buf = u & 1;
+            if (!warp_wait(smem_u32(&sm.acc_full[buf]), (u >> 1) & 1, wctx))
+                break;
+            tc_fence_after();
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * kMaxN + col0);
+            const bool negw = __any_sync(0xffffffffu, s < 0.f);
+
+            float acc[kTPWMax][kNP];
+            float accx[kTPWMax];
+#pragma unroll
+            for (int a = 0; a < kTPWMax; ++a) {
+                accx[a] = 0.f;
+#pragma unroll
+                for (int c = 0; c < kNP; ++c)
+                    acc[a][c] = 0.f;
+            }
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                if (ch * 32 < ncols) {
+                    float x[32];
+                    tmem_ld32(taddr + ch * 32, x);
+                    if (!negw) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int col = ch * 32 + k;
+                            acc[col / H][k % kNP] =
+                                fmaf(wr[col], fmaxf(x[k], 0.f), acc[col / H][k % kNP]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int col = ch * 32 + k;
+                            acc[col / H][k % kNP] =
+                                fmaf(wr[col], fmaxf(x[k], 0.f), acc[col / H][k % kNP]);
+                            accx[col / H] = fmaf(wr[col], x[k], accx[col / H]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&sm.acc_empty[buf]));
+
+            // ---- range-masked stores
+            const long long j = (long long)info.t * kBlockKV + row;
+#pragma unroll
+            for (int a = 0; a < kTPWMax; ++a) {
+                if (a < ntok) {
+                    const int tk = tok0 + a;
+                    const int r = info.b * p.tok + tk;   // output row (both paths)
+                    if (r < p.rows) {
+                        float sum = 0.f;
+#pragma unroll
+                        for (int c = 0; c < kNP; ++c)
+                            sum += acc[a][c];
+                        // ReLU(s x) = s * max(x, 0) for s >= 0, s * (x - max(x, 0)) for s < 0
+                        const float v = (s >= 0.f) ? s * sum : s * (accx[a] - sum);
+                        const int2 rg = sm.range[qb][tk];
+                        const bool valid = j >= rg.x && j < rg.y;
+                        float* out = p.logits + (long long)r * p.ldo;
+                        if (compressed) {
+                            if (valid && j - rg.x < p.ldo)
+                                out[j - rg.x] = v;
+                        } else if (j < p.width) {
+                            if (valid)
+                                out[j] = v;
+                            else if (clean)
+                                out[j] = ninf;
+                        }
+                    }
+                }
+            }
+            if (info.flags & kLastOfBlock) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&sm.q_empty[qb]));
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace mqa

@@ -1,0 +1,172 @@
+/*
+ * mqa.h -- C ABI of libmqa.so: FP8 MQA logits scoring (the "lightning indexer"
+ * step) on GB300 (sm_103a).
+ *
+ * The operation ("How to Implement MQA (Multi-Query Attention) Logits
+ * Computation with DeepGEMM", instagit article, section "Core Architecture
+ * Components": TMA staging, UMMA on E4M3 Q and KV, per-token KV scales, a math
+ * reduction that applies ReLU, multiplies by the per-head weight and sums over
+ * heads; section "Compressed Logits"):
+ *
+ *   for query token i and key j with k_start[i] <= j < k_end[i]
+ *     logits[i, j] = sum_{h<H} weights[i,h] * ReLU(kv_scale[j] * <q[i,h,:], kv[j,:]>)
+ *
+ * Positions outside a row's range hold -inf in clean mode ("[PR #435] Improve
+ * SM100 MX MQA logits clean-output performance", section "Standalone
+ * performance reproducer", which asserts isneginf outside the valid mask and
+ * exact zeros inside it for all-zero inputs).
+ *
+ * Conventions for every call:
+ *  - All pointers are DEVICE pointers owned by the caller; the library keeps no
+ *    reference after the call returns and allocates no device memory.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously, except under MQA_CHECK_BOUNDS (below).
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns MQA_ERR_INVALID_ARG / MQA_ERR_UNSUPPORTED and
+ *    launches nothing.  mqa_last_error_message() explains the last failure of
+ *    the calling thread.
+ *  - Without MQA_CHECK_BOUNDS, data-dependent inputs are clamped, never trusted:
+ *    ranges are intersected with [0, S_kv) (start >= end is an empty row),
+ *    context lengths with the block table's capacity, and a block id outside
+ *    [0, num_blocks) reads zeros.  No input can make a kernel read or write out
+ *    of bounds.
+ *  - Kernels never spin without bound: a pipeline wait that runs past its
+ *    budget (see mqa_set_wait_limit) stops the kernel and records
+ *    MQA_ERR_TIMEOUT, which mqa_device_status() reports.
+ */
+#ifndef MQA_H
+#define MQA_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MQA_API __attribute__((visibility("default")))
+#else
+#define MQA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *mqa_stream_t;
+
+typedef enum {
+    MQA_OK = 0,
+    MQA_ERR_INVALID_ARG = 1, /* bad pointer, size, stride or alignment */
+    MQA_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for */
+    MQA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
+    MQA_ERR_TIMEOUT = 4,     /* a kernel wait ran out (reported by mqa_device_status) */
+    MQA_ERR_BAD_INPUT = 5    /* MQA_CHECK_BOUNDS found an out-of-range input value */
+} mqa_status;
+
+enum {
+    /* Write -inf to every position of a row that is outside its range (clean
+     * logits).  Without it, such positions are left untouched. */
+    MQA_CLEAN = 1u,
+    /* Dense only: row i stores key k_start[i] + c at column c, c < k_end[i] -
+     * k_start[i]; columns [length, ldo) are padding (-inf when MQA_CLEAN). */
+    MQA_COMPRESSED = 2u,
+    /* Validate data-dependent inputs on the device first (ranges, context
+     * lengths, block ids, schedule).  The call then synchronizes `stream` and
+     * returns MQA_ERR_BAD_INPUT without computing if any check fails.  Not for
+     * use inside CUDA graph capture. */
+    MQA_CHECK_BOUNDS = 4u
+};
+
+/*
+ * Dense MQA logits ("Implementing Standard MQA Logits Computation" of the
+ * instagit article; argument order (q, kv, scales, weights, starts, ends) as in
+ * the PR #435 reproducer's call).
+ *
+ *   q         [S_q, H, D]  FP8 E4M3 bytes, row-major, 16-byte aligned
+ *   kv        [S_kv, D]    FP8 E4M3 bytes (one KV head), 16-byte aligned
+ *   kv_scale  [S_kv]       fp32 per-key scale, 16-byte aligned
+ *   weights   [S_q, H]     fp32 per-(token, head) weight, 16-byte aligned
+ *   k_start, k_end [S_q]   int32 half-open key range of each query row
+ *   logits    [S_q, ldo]   fp32 output, 4-byte aligned.  Uncompressed: row i
+ *             has S_kv columns and ldo >= S_kv (columns [S_kv, ldo) are never
+ *             written).  Compressed: ldo >= every row's range length.
+ *   H in {8, 32, 64}, D in {64, 128}; S_q, S_kv >= 0; S_q * H < 2^31.
+ *   flags     MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS
+ */
+MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_scale, const float *weights,
+                      const int32_t *k_start, const int32_t *k_end, float *logits, int S_q,
+                      int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
+
+/*
+ * Work schedule for paged_mqa_logits ("[PR #314] fix: SM90 paged MQA logits
+ * IMA on next_n=4", sections "a97b74d" Root cause / Fix: schedule_meta holds
+ * num_sms + 1 entries and host and kernel must agree on the query atom).
+ *
+ * A work unit is one sequence's next_n query tokens against one 128-key tile;
+ * sequence b owns ceil(max(context_lens[b], 0) / 128) units, numbered sequence
+ * by sequence.  SM k starts at unit floor(k * U / num_sms) of U in total and
+ * entry k is that unit's (sequence, tile) pair; entry num_sms, and any entry at
+ * U, is (B, 0).  next_n and block_kv only select validation here.
+ *
+ *   context_lens  [B] int32 (device)
+ *   schedule_meta [num_sms + 1][2] int32 (device), written by this call
+ *   block_kv in {32, 64, 128}; num_sms >= 1 (normally mqa_get_num_sms()).
+ */
+MQA_API mqa_status paged_mqa_logits_metadata(const int32_t *context_lens, int B, int next_n, int block_kv,
+                                     int num_sms, int32_t *schedule_meta, mqa_stream_t stream);
+
+/*
+ * Paged decode MQA logits ("Implementing Paged MQA Logits Computation for
+ * Decoding" of the instagit article; next_n queries per sequence and block_kv
+ * pages as in "[PR #314] ...", section "12cb7c0").
+ *
+ *   q            [B * next_n, H, D] FP8 E4M3 bytes, 16-byte aligned; row
+ *                r = b * next_n + t is query t of sequence b
+ *   kv_cache     [num_blocks, block_kv, D] FP8 E4M3 bytes, 16-byte aligned
+ *   kv_scales    [num_blocks, block_kv] fp32, 16-byte aligned
+ *   weights      [B * next_n, H] fp32, 16-byte aligned
+ *   context_lens [B] int32
+ *   block_table  [B, max_blocks_per_seq] int32: logical page p of sequence b
+ *                lives in physical block block_table[b, p]
+ *   schedule_meta the output of paged_mqa_logits_metadata for the same
+ *                context_lens, next_n, block_kv and num_sms
+ *   logits       [B * next_n, ldo] fp32; a row has max_blocks_per_seq *
+ *                block_kv columns, ldo >= that.  Row r scores key positions
+ *                [0, context_lens[b] - next_n + t + 1); key position j is slot
+ *                j % block_kv of block block_table[b, j / block_kv].
+ *   H in {16, 32, 64}, D in {64, 128}, next_n * H a multiple of 16 and at
+ *   most 256, block_kv in {32, 64, 128}.
+ *   flags        MQA_CLEAN | MQA_CHECK_BOUNDS (MQA_COMPRESSED is rejected)
+ */
+MQA_API mqa_status paged_mqa_logits(const void *q, const void *kv_cache, const float *kv_scales,
+                            const float *weights, const int32_t *context_lens,
+                            const int32_t *block_table, int max_blocks_per_seq,
+                            const int32_t *schedule_meta, float *logits, int B, int next_n, int H,
+                            int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
+                            unsigned flags, mqa_stream_t stream);
+
+/* Number of SMs of `device` (cached), or -1 on error. */
+MQA_API int mqa_get_num_sms(int device);
+
+/* Synchronizes `stream`, then returns and clears the current device's kernel
+ * status word: MQA_ERR_TIMEOUT if a kernel wait ran out, MQA_ERR_BAD_INPUT if
+ * a bounds check failed, MQA_OK otherwise. */
+MQA_API mqa_status mqa_device_status(mqa_stream_t stream);
+
+/* Budget, in SM clock cycles, of every pipeline wait in kernels launched after
+ * this call (default 4e9, about two seconds).  0 restores the default. */
+MQA_API mqa_status mqa_set_wait_limit(unsigned long long cycles);
+
+/* Test hook for the timeout path: launches one CTA that waits, with the given
+ * budget, on a barrier nothing ever signals.  The wait runs out, the kernel
+ * exits cleanly and the next mqa_device_status() returns MQA_ERR_TIMEOUT. */
+MQA_API mqa_status mqa_selftest_wait_timeout(unsigned long long cycles, mqa_stream_t stream);
+
+MQA_API const char *mqa_status_string(mqa_status s);
+
+/* Human-readable reason for the last non-OK status returned to this thread. */
+MQA_API const char *mqa_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQA_H */

@@ -1,0 +1,118 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+and rejects invalid arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_mqa_indexer_gb300 as mqa
+from fp8_mqa_indexer_gb300 import build as mqa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mqa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mqa_build.build()
+    return mqa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"MQA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_three_entry_points():
+    names = declared_functions()
+    for n in ("mqa_logits", "paged_mqa_logits", "paged_mqa_logits_metadata"):
+        assert n in names
+    assert len(names) == len(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libmqa.so does not export {name}"
+
+
+def test_library_has_no_cuda_driver_dependency():
+    # the driver entry point is fetched at run time: the library loads on a
+    # host with no CUDA driver (this container) and links cudart statically
+    import subprocess
+    out = subprocess.run(["ldd", mqa.library_path()], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out and "libcudart" not in out
+
+
+def test_status_strings(lib):
+    for code, name in mqa.STATUS_NAMES.items():
+        assert lib.mqa_status_string(code).decode() == name
+
+
+F = 16  # a fake, 16-byte aligned "device pointer": never dereferenced on these paths
+
+
+def call_dense(lib, **kw):
+    a = dict(q=F, kv=F, kv_scale=F, weights=F, k_start=F, k_end=F, logits=F, S_q=4, S_kv=256, H=64,
+             D=128, ldo=256, flags=1, stream=None)
+    a.update(kw)
+    return lib.mqa_logits(a["q"], a["kv"], a["kv_scale"], a["weights"], a["k_start"], a["k_end"],
+                          a["logits"], a["S_q"], a["S_kv"], a["H"], a["D"], a["ldo"], a["flags"],
+                          a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), 2), (dict(D=256), 2), (dict(H=16), 2), (dict(H=7), 2),
+    (dict(S_q=-1), 1), (dict(S_kv=-5), 1), (dict(ldo=255), 1), (dict(flags=64), 1),
+    (dict(flags=3, ldo=0), 1), (dict(q=None), 1), (dict(logits=None), 1),
+    (dict(q=F + 8), 1), (dict(kv_scale=F + 4), 1), (dict(logits=F + 2), 1),
+])
+def test_dense_rejects_invalid_arguments(lib, kw, status):
+    assert call_dense(lib, **kw) == status
+    assert lib.mqa_last_error_message().decode()
+
+
+def test_dense_zero_rows_is_a_no_op(lib):
+    assert call_dense(lib, S_q=0, q=None, logits=None) == 0
+
+
+def call_paged(lib, **kw):
+    a = dict(q=F, kv_cache=F, kv_scales=F, weights=F, context_lens=F, block_table=F, max_blocks=16,
+             meta=F, logits=F, B=2, next_n=2, H=64, D=128, block_kv=64, num_blocks=40, num_sms=8,
+             ldo=1024, flags=1, stream=None)
+    a.update(kw)
+    return lib.paged_mqa_logits(a["q"], a["kv_cache"], a["kv_scales"], a["weights"],
+                                a["context_lens"], a["block_table"], a["max_blocks"], a["meta"],
+                                a["logits"], a["B"], a["next_n"], a["H"], a["D"], a["block_kv"],
+                                a["num_blocks"], a["num_sms"], a["ldo"], a["flags"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=2), 2), (dict(flags=3), 2), (dict(flags=8), 1), (dict(D=32), 2), (dict(H=8), 2),
+    (dict(next_n=5), 2), (dict(block_kv=16), 2), (dict(ldo=1000), 1), (dict(num_sms=0), 1),
+    (dict(next_n=0), 1), (dict(B=-1), 1), (dict(meta=None), 1), (dict(kv_cache=F + 1), 1),
+])
+def test_paged_rejects_invalid_arguments(lib, kw, status):
+    assert call_paged(lib, **kw) == status
+
+
+def test_paged_zero_batch_is_a_no_op(lib):
+    assert call_paged(lib, B=0) == 0
+
+
+@pytest.mark.parametrize("kw,status", [(dict(block_kv=48), 2), (dict(num_sms=0), 1),
+                                       (dict(next_n=0), 1), (dict(meta=None), 1)])
+def test_metadata_rejects_invalid_arguments(lib, kw, status):
+    a = dict(ctx=F, B=3, next_n=2, block_kv=64, num_sms=8, meta=F)
+    a.update(kw)
+    assert lib.paged_mqa_logits_metadata(a["ctx"], a["B"], a["next_n"], a["block_kv"],
+                                         a["num_sms"], a["meta"], None) == status
+
+
+def test_valid_call_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU suite")
+    # passes validation, then the first CUDA runtime call fails: MQA_ERR_CUDA
+    assert call_dense(lib) == 3
+    assert lib.mqa_get_num_sms(0) == -1
