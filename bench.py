@@ -1,0 +1,355 @@
+"""Benchmark: dense FP8 MQA logits on the 2048 x 32768, H=64, D=128 workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one mqa_logits call over the whole workload (clean fp32 logits,
+rows [0, S_kv - S_q + i)).  Timing: W untimed warm-up steps, then K steps,
+each timed with CUDA events on the launching stream, L2 flushed (a 256 MiB
+write) before every step outside the events, a barrier and a device
+synchronize around the timed loop, the max over ranks.  Prints one JSON line.
+
+--impl reference times the CPU oracle (the plain double-precision reference in
+oracle/) on a bounded row sample of the same workload on this host's cores.
+Under torchrun each rank runs the whole workload on its own GPU (the rows are
+independent; no collective is on the data path) and rank 0 reports the
+aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0   # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
+KERNEL_SOURCES = ["fp8_mqa_indexer_gb300/csrc/mqa_kernel.cuh", "fp8_mqa_indexer_gb300/csrc/ptx.cuh",
+                  "fp8_mqa_indexer_gb300/csrc/launch.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f).get(workload)
+    if not rec or rec.get("kernel_hash") != kernel_hash():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def make_case(workload: str):
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    return wl.dense_config(workload)
+
+
+def oracle_sample(case, budget_s: float, max_rows: int = 4096):
+    """Time the oracle on evenly spread rows until ~budget_s of wall time."""
+    import oracle
+    oracle.build()
+    cores = max(1, len(os.sched_getaffinity(0)))
+    stride_rows = list(range(0, case.S_q, max(1, case.S_q // 256)))
+    order = stride_rows + [r for r in range(case.S_q) if r not in set(stride_rows)]
+    counts = case.valid_counts()
+    done_rows, flops = 0, 0.0
+    t0 = time.perf_counter()
+    k = 0
+    while k < len(order) and done_rows < max_rows:
+        batch = order[k:k + cores]
+        k += len(batch)
+
+        def one(r):
+            return oracle.mqa_logits(case.q, case.kv, case.kv_scale, case.weights, case.k_start,
+                                     case.k_end, ldo=case.ldo, clean=case.clean,
+                                     compressed=case.compressed, rows=(r, r + 1))
+        oracle.run_rows_parallel(one, batch, threads=cores)
+        done_rows += len(batch)
+        flops += float(sum(int(counts[r]) for r in batch)) * 2 * case.H * case.D
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    wall = time.perf_counter() - t0
+    return {"tflops": flops / wall / 1e12, "cores": cores, "rows": done_rows, "wall_s": wall,
+            "flops": flops}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    case = make_case(args.workload)
+    valid = int(case.valid_counts().sum())
+    flops_full = valid * 2.0 * case.H * case.D
+    per_step = []
+    info = None
+    for _ in range(args.warmup):
+        oracle_sample(case, budget_s=0.5, max_rows=8)
+    budget = args.ref_budget or max(1.0, min(6.0, 90.0 / max(1, args.steps)))
+    for _ in range(args.steps):
+        info = oracle_sample(case, budget_s=budget)
+        per_step.append(info["tflops"])
+    value = statistics.median(per_step)
+    ms_per_step = flops_full / (value * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": "MQA logits TFLOP/s (valid logits x 2*H*D)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (exact e4m3 decode)",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "S_q": case.S_q, "S_kv": case.S_kv, "H": case.H,
+                   "D": case.D, "valid_logits": valid, "clean": case.clean},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
+                         "sample": f"{info['rows']} of {case.S_q} rows per step, "
+                                   f"extrapolated to the full workload ({info['wall_s']:.1f} s)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dense_2k_32k_h64_d128")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
+    ap.add_argument("--ref-budget", type=float, default=None,
+                    help="oracle seconds per reference step (default: about 90 s in all)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import fp8_mqa_indexer_gb300 as mqa
+    from fp8_mqa_indexer_gb300 import build as mqa_build
+
+    assert torch.cuda.is_available(), "bench.py needs a GPU"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    if rank == 0 or world == 1:
+        mqa_build.build()
+    if pg:
+        pg.barrier()
+    mqa.load_library()
+
+    case = make_case(args.workload)
+    valid = int(case.valid_counts().sum())
+    flops = valid * 2.0 * case.H * case.D
+    q, kv = case.q.to(dev), case.kv.to(dev)
+    s, w = case.kv_scale.to(dev), case.weights.to(dev)
+    ks, ke = case.k_start.to(dev), case.k_end.to(dev)
+    out = torch.empty((case.S_q, case.ldo), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mqa.mqa_logits(q, kv, s, w, ks, ke, out, clean=case.clean, compressed=case.compressed,
+                       ldo=case.ldo)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert mqa.device_status() == 0
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    assert mqa.device_status() == 0
+    total_ms = sum(times_ms)
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    median_ms = statistics.median(times_ms)
+
+    # end to end through the public call: pinned host inputs in, logits out
+    host = {k: v.pin_memory() for k, v in dict(q=case.q, kv=case.kv, s=case.kv_scale, w=case.weights,
+                                                ks=case.k_start, ke=case.k_end).items()}
+    host_out = torch.empty((case.S_q, case.ldo), dtype=torch.float32, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * 4
+
+    def e2e_step():
+        dq = host["q"].to(dev, non_blocking=True)
+        dkv = host["kv"].to(dev, non_blocking=True)
+        ds = host["s"].to(dev, non_blocking=True)
+        dw = host["w"].to(dev, non_blocking=True)
+        dks = host["ks"].to(dev, non_blocking=True)
+        dke = host["ke"].to(dev, non_blocking=True)
+        mqa.mqa_logits(dq, dkv, ds, dw, dks, dke, out, clean=case.clean,
+                       compressed=case.compressed, ldo=case.ldo)
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+
+    peaks, peaks_src = load_peaks()
+    peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": "MQA logits TFLOP/s (valid logits x 2*H*D)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "S_q": case.S_q, "S_kv": case.S_kv, "H": case.H,
+                   "D": case.D, "valid_logits": valid, "clean": case.clean,
+                   "compressed": case.compressed, "ldo": case.ldo,
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "parallelism": f"replicas x{world} (independent rows, no collective)"},
+        "valid_logits_per_s": valid * world / (ms_per_step * 1e-3),
+        "median_ms": median_ms,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peaks_src} bf16 burst x {FP8_PER_BF16} (nominal fp8:bf16)"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        info = oracle_sample(case, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": info["tflops"], "unit": "TFLOP/s", "cores": info["cores"],
+                                "kind": "oracle",
+                                "sample": f"{info['rows']} of {case.S_q} rows ({info['wall_s']:.1f} s"
+                                          f" of oracle time), throughput extrapolated"}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -116,18 +116,22 @@ mqa_status make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt,
     return MQA_OK;
 }
 
-mqa_status make_map_1d_f32(CUtensorMap* m, const void* base, unsigned long long n, unsigned box,
-                           const char* what)
+// Map over a vector of n fp32 values with a box of `box` values, encoded as a
+// [1, n] matrix (a second dimension of extent 1 whose stride is never used for
+// addressing; it is padded to the 16-byte multiple the encoder requires).
+mqa_status make_map_vec_f32(CUtensorMap* m, const void* base, unsigned long long n, unsigned box,
+                            const char* what)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    cuuint64_t dims[1] = {n};
-    cuuint32_t boxd[1] = {box};
-    cuuint32_t estr[1] = {1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<void*>(base), dims, nullptr,
+    cuuint64_t dims[2] = {n, 1};
+    cuuint64_t strides[1] = {(n * 4 + 15) / 16 * 16};
+    cuuint32_t boxd[2] = {box, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
                     boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
     return MQA_OK;
@@ -460,7 +464,7 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
                          N, D, swz, "q")) != MQA_OK ||
         (s = make_map_2d(&a.tm_kv, kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, S_kv, D, kBlockKV, D, swz,
                          "kv")) != MQA_OK ||
-        (s = make_map_1d_f32(&a.tm_scale, kv_scale, S_kv, kBlockKV, "kv_scale")) != MQA_OK ||
+        (s = make_map_vec_f32(&a.tm_scale, kv_scale, S_kv, kBlockKV, "kv_scale")) != MQA_OK ||
         (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, S_q, H, tok, H,
                          CU_TENSOR_MAP_SWIZZLE_NONE, "weights")) != MQA_OK)
         return s;
@@ -565,8 +569,8 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
         (s = make_map_2d(&a.tm_kv, kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
                          (unsigned long long)num_blocks * block_kv, D, block_kv, D, swz,
                          "kv_cache")) != MQA_OK ||
-        (s = make_map_1d_f32(&a.tm_scale, kv_scales, (unsigned long long)num_blocks * block_kv,
-                             block_kv, "kv_scales")) != MQA_OK ||
+        (s = make_map_vec_f32(&a.tm_scale, kv_scales, (unsigned long long)num_blocks * block_kv,
+                              block_kv, "kv_scales")) != MQA_OK ||
         (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                          (unsigned long long)B * next_n, H, next_n, H, CU_TENSOR_MAP_SWIZZLE_NONE,
                          "weights")) != MQA_OK)

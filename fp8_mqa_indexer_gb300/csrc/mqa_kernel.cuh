@@ -443,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (k < ppt && ids[k] >= 0) {
                             tma_load_2d(smem_u32(sm.kv[stage]) + k * p.block_kv * D, &tm_kv, bar, 0,
                                         ids[k] * p.block_kv);
-                            tma_load_1d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale, bar,
-                                        ids[k] * p.block_kv);
+                            tma_load_2d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale, bar,
+                                        ids[k] * p.block_kv, 0);
                         }
                     }
                 }
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t bar = smem_u32(&sm.full[stage]);
                     mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * D + kBlockKV * 4));
                     tma_load_2d(smem_u32(sm.kv[stage]), &tm_kv, bar, 0, t * kBlockKV);
-                    tma_load_1d(smem_u32(sm.scale[stage]), &tm_scale, bar, t * kBlockKV);
+                    tma_load_2d(smem_u32(sm.scale[stage]), &tm_scale, bar, t * kBlockKV, 0);
                 }
             }
             ++n_issued;
