@@ -226,7 +226,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     constexpr int kTPWMax = 128 / H;               // tokens per epilogue warp group, max
-    constexpr int kNP = (H >= 32) ? 4 : 1;         // partial accumulators per token
+    constexpr int kNP2 = (H >= 32) ? 2 : 1;        // pair accumulators per token
+    constexpr int kCW = (H <= 16) ? 16 : 32;       // TMEM columns per load
+    constexpr int kMaxChunks = 128 / kCW;
+    // Register split after set-up (launch: 384 threads x 168 = 64512): the
+    // control warp group (producer, MMA, fill) gives registers to the two
+    // epilogue warp groups; 128 * ctl + 256 * epi == 64512.  The paged producer
+    // keeps a page-id window and needs a little more.
+    constexpr int kRegsCtl = PAGED ? 56 : 40;
+    constexpr int kRegsEpi = PAGED ? 224 : 232;
+    static_assert(128 * kRegsCtl + 256 * kRegsEpi <= kThreads * 168, "register split exceeds launch");
     static_assert(H >= 8 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two in [8,128]");
     static_assert(D == 64 || D == 128, "D must be 64 or 128");
 
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================================================= TMA producer
-        regs_dec<56>();
+        regs_dec<kRegsCtl>();
         int b = sm.start_b;
         int t = sm.start_t;
         int k_block = 0;
@@ -490,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ================================================= MMA issuer
-        regs_dec<56>();
+        regs_dec<kRegsCtl>();
         if (lane == 0) {
             const uint32_t idesc = idesc_e4m3_f32(kBlockKV, (uint32_t)N);
             int k_block = -1;
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         // ================================================= -inf fill
-        regs_dec<56>();
+        regs_dec<kRegsCtl>();
         if (p.flags & kFlagClean) {
             const int fw = warp - 2;   // 0 or 1
             for (int r = cta + fw * G; r < p.rows; r += 2 * G) {
@@ -555,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ================================================= epilogue
-        regs_inc<224>();
+        regs_inc<kRegsEpi>();
         const int g = (warp - kEpiWarp0) >> 2;         // warp group 0 / 1
         const int quad = warp & 3;                      // TMEM lane quadrant
         const int row = quad * 32 + lane;               // key within the tile
@@ -567,10 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool clean = (p.flags & kFlagClean) != 0;
         const bool compressed = (p.flags & kFlagCompressed) != 0;
         const float ninf = __int_as_float(0xff800000u);
-        float wr[128];
+        float2 wr2[64];
 #pragma unroll
-        for (int k = 0; k < 128; ++k)
-            wr[k] = 0.f;
+        for (int k = 0; k < 64; ++k)
+            wr2[k] = make_float2(0.f, 0.f);
         int k_block = -1;
         int qb = 0;
         for (int u = 0; u < n_units; ++u) {
@@ -589,10 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 32; ++k) {
                     if (4 * k < ncols) {
                         const float4 v = w4[k];
-                        wr[4 * k] = v.x;
-                        wr[4 * k + 1] = v.y;
-                        wr[4 * k + 2] = v.z;
-                        wr[4 * k + 3] = v.w;
+                        wr2[2 * k] = make_float2(v.x, v.y);
+                        wr2[2 * k + 1] = make_float2(v.z, v.w);
                     }
                 }
             }
@@ -608,42 +615,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * kMaxN + col0);
             const bool negw = __any_sync(0xffffffffu, s < 0.f);
 
-            float acc[kTPWMax][kNP];
+            // Head reduction in packed fp32 pairs: columns (2c, 2c+1) of a token
+            // go through one FFMA2; kNP2 independent pair-accumulators per token.
+            float2 acc2[kTPWMax][kNP2];
+#pragma unroll
+            for (int a = 0; a < kTPWMax; ++a)
+#pragma unroll
+                for (int c = 0; c < kNP2; ++c)
+                    acc2[a][c] = make_float2(0.f, 0.f);
+            // TMEM -> registers in kCW-column chunks, double-buffered: the load
+            // of chunk c+1 is in flight while chunk c is reduced.  Unless a
+            // negative scale needs a second pass, the accumulator buffer is
+            // handed back to the MMA warp once the last chunk has landed,
+            // before its arithmetic.
+            const int nch = (ncols + kCW - 1) / kCW;
+            float xa[kCW], xb[kCW];
+            tmem_ld_async<kCW>(taddr, xa);
+            tmem_wait<kCW>(xa);
+#pragma unroll
+            for (int ch = 0; ch < kMaxChunks; ++ch) {
+                if (ch < nch) {
+                    float(&xc)[kCW] = (ch & 1) ? xb : xa;
+                    float(&xn)[kCW] = (ch & 1) ? xa : xb;
+                    const bool more = ch + 1 < nch;
+                    if (more) {
+                        tmem_ld_async<kCW>(taddr + (ch + 1) * kCW, xn);
+                    } else if (!negw) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(smem_u32(&sm.acc_empty[buf]));
+                    }
+#pragma unroll
+                    for (int k = 0; k < kCW; k += 2) {
+                        const int col = ch * kCW + k;
+                        const float2 r = make_float2(fmaxf(xc[k], 0.f), fmaxf(xc[k + 1], 0.f));
+                        float2& a = acc2[col / H][(k >> 1) % kNP2];
+                        a = __ffma2_rn(wr2[col >> 1], r, a);
+                    }
+                    if (more)
+                        tmem_wait<kCW>(xn);
+                }
+            }
+            // Rare path (a warp holding a negative scale): sum_h w * x as well,
+            // from a second pass over the same TMEM columns.
             float accx[kTPWMax];
 #pragma unroll
-            for (int a = 0; a < kTPWMax; ++a) {
+            for (int a = 0; a < kTPWMax; ++a)
                 accx[a] = 0.f;
+            if (negw) {
 #pragma unroll
-                for (int c = 0; c < kNP; ++c)
-                    acc[a][c] = 0.f;
-            }
+                for (int ch = 0; ch < kMaxChunks; ++ch) {
+                    if (ch < nch) {
+                        float xc[kCW];
+                        tmem_ld_async<kCW>(taddr + ch * kCW, xc);
+                        tmem_wait<kCW>(xc);
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                if (ch * 32 < ncols) {
-                    float x[32];
-                    tmem_ld32(taddr + ch * 32, x);
-                    if (!negw) {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const int col = ch * 32 + k;
-                            acc[col / H][k % kNP] =
-                                fmaf(wr[col], fmaxf(x[k], 0.f), acc[col / H][k % kNP]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const int col = ch * 32 + k;
-                            acc[col / H][k % kNP] =
-                                fmaf(wr[col], fmaxf(x[k], 0.f), acc[col / H][k % kNP]);
-                            accx[col / H] = fmaf(wr[col], x[k], accx[col / H]);
+                        for (int k = 0; k < kCW; k += 2) {
+                            const int col = ch * kCW + k;
+                            accx[col / H] = fmaf(wr2[col >> 1].x, xc[k], accx[col / H]);
+                            accx[col / H] = fmaf(wr2[col >> 1].y, xc[k + 1], accx[col / H]);
                         }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&sm.acc_empty[buf]));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&sm.acc_empty[buf]));
 
             // ---- range-masked stores
             const long long j = (long long)info.t * kBlockKV + row;
@@ -655,8 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (r < p.rows) {
                         float sum = 0.f;
 #pragma unroll
-                        for (int c = 0; c < kNP; ++c)
-                            sum += acc[a][c];
+                        for (int c = 0; c < kNP2; ++c)
+                            sum += acc2[a][c].x + acc2[a][c].y;
                         // ReLU(s x) = s * max(x, 0) for s >= 0, s * (x - max(x, 0)) for s < 0
                         const float v = (s >= 0.f) ? s * sum : s * (accx[a] - sum);
                         const int2 rg = sm.range[qb][tk];
