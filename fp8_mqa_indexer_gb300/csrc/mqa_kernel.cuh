@@ -210,10 +210,15 @@ __device__ __forceinline__ void warp_fill_neg_inf(float* row, long long c0, long
 
 // A bounded wait taken by a whole warp: every lane gets the same answer, so a
 // timeout never splits the warp.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                          unsigned sleep_ns = 0)
 {
-    return __all_sync(0xffffffffu, wait_bounded(bar, parity, w));
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, w, sleep_ns));
 }
+
+// Back-off of waiters off the critical path (ns between polls).
+constexpr unsigned kProducerSleepNs = 256;
+constexpr unsigned kMmaSleepNs = 32;
 
 // ------------------------------------------------------------------ kernel
 template <int H, int D, bool PAGED>
@@ -402,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < n_units; ++u) {
             if (first) {
                 const int qb = k_block & 1;
-                if (!warp_wait(smem_u32(&sm.q_empty[qb]), ((k_block >> 1) & 1) ^ 1, wctx))
+                if (!warp_wait(smem_u32(&sm.q_empty[qb]), ((k_block >> 1) & 1) ^ 1, wctx,
+                               kProducerSleepNs))
                     break;
                 if (lane < p.tok)
                     sm.range[qb][lane] = myrange;
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++q_issued;
             }
             const int stage = u % S;
-            if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx))
+            if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx, kProducerSleepNs))
                 break;
             const bool last = (u + 1 == n_units) || (t + 1 >= thi);
             const UnitInfo info{b, t, k_block & 1,
@@ -505,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int k_block = -1;
             for (int u = 0; u < n_units; ++u) {
                 const int stage = u % S;
-                if (!wait_bounded(smem_u32(&sm.full[stage]), (u / S) & 1, wctx))
+                if (!wait_bounded(smem_u32(&sm.full[stage]), (u / S) & 1, wctx, kMmaSleepNs))
                     break;
                 const UnitInfo info = sm.info[stage];
                 if (info.flags & kFirstOfBlock) {
@@ -514,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                 }
                 const int buf = u & 1;
-                if (!wait_bounded(smem_u32(&sm.acc_empty[buf]), ((u >> 1) & 1) ^ 1, wctx))
+                if (!wait_bounded(smem_u32(&sm.acc_empty[buf]), ((u >> 1) & 1) ^ 1, wctx,
+                                  kMmaSleepNs))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kMaxN);
@@ -630,8 +637,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // before its arithmetic.
             const int nch = (ncols + kCW - 1) / kCW;
             float xa[kCW], xb[kCW];
-            tmem_ld_async<kCW>(taddr, xa);
-            tmem_wait<kCW>(xa);
+            if (nch > 0) {
+                tmem_ld_async<kCW>(taddr, xa);
+                tmem_wait<kCW>(xa);
+            } else if (!negw) {   // this warp group has no columns in the unit
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&sm.acc_empty[buf]));
+            }
 #pragma unroll
             for (int ch = 0; ch < kMaxChunks; ++ch) {
                 if (ch < nch) {

@@ -52,18 +52,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// try_wait suspends the thread until the phase completes or the hinted time
-// (ns) passes, so a waiting warp does not spin on the issue slots the math
-// warps need.
+// try_wait may suspend the thread for a while before reporting an incomplete
+// phase.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(20000u)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -78,20 +77,28 @@ struct WaitCtx {
     long long limit;               // clock64 cycles
 };
 
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w)
+// `sleep_ns` > 0 backs off between polls: for waiters that are not on the
+// critical path, so they leave issue slots to the math warps.  The abort flag
+// and the clock are checked every 16 polls.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                             unsigned sleep_ns = 0)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const long long t0 = clock64();
-    while (true) {
+    for (unsigned n = 1;; ++n) {
+        if (sleep_ns)
+            __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity))
             return true;
-        if (*w.abort_flag)
-            return false;
-        if (clock64() - t0 > w.limit) {
-            *w.abort_flag = 1;
-            atomicOr(w.status, kDevErrTimeout);
-            return false;
+        if ((n & 15) == 0) {
+            if (*w.abort_flag)
+                return false;
+            if (clock64() - t0 > w.limit) {
+                *w.abort_flag = 1;
+                atomicOr(w.status, kDevErrTimeout);
+                return false;
+            }
         }
     }
 }
