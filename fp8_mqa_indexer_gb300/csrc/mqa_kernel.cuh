@@ -75,6 +75,7 @@ struct Params {
     // shared
     long long width;     // logical columns of an uncompressed row
     int tok;             // query tokens per work unit
+    int tok_split;       // tokens of epilogue warp group 0 (group 1 takes the rest)
     int num_q_blocks;    // dense: ceil(S_q / tok); paged: B
     int rows;            // output rows: S_q or B * next_n
     long long wait_limit;
@@ -220,6 +221,258 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 constexpr unsigned kProducerSleepNs = 256;
 constexpr unsigned kMmaSleepNs = 32;
 
+// --------------------------------------------------------------- epilogue
+// Epilogue of one warp group: per work unit it reads its columns of the TMEM
+// accumulator (keys on lanes, (token, head) on columns), reduces
+// sum_h w[h] * max(x, 0) per token, scales by s[j] and writes the row-masked
+// logits.  Columns are read in batches of 64 (two 32-column TMEM loads)
+// double-buffered across units: the load of the next batch -- of this unit or
+// of the next one -- is in flight while the current batch is reduced.
+// Weights are read from shared memory with broadcast 16-byte loads.
+template <int H, int D>
+struct Epilogue {
+    static_assert(H >= 8 && H <= 64, "a 64-column batch must hold whole tokens");
+    using C = Cfg<D>;
+    static constexpr int S = C::kStages;
+    static constexpr int kTPB = 64 / H;   // tokens per 64-column batch
+    static constexpr int kNP2 = (H >= 32) ? 2 : 1;
+
+    struct Unit {
+        int stage;
+        int buf;
+        UnitInfo info;
+        float s;
+        bool negw;
+    };
+
+    Smem<D>& sm;
+    const Params& p;
+    const WaitCtx& wctx;
+    uint32_t tmem_base;
+    int n_units;
+    int quad;
+    int lane;
+    int tok0;
+    int ntok;
+    int k_block = -1;
+
+    __device__ __forceinline__ int row() const { return quad * 32 + lane; }
+
+    // Waits until unit v's inputs and accumulator are ready; hands the key-tile
+    // stage back to the producer (its scale has been read).
+    __device__ __forceinline__ bool begin(int v, Unit& st)
+    {
+        st.stage = v % S;
+        if (!warp_wait(smem_u32(&sm.full[st.stage]), (v / S) & 1, wctx))
+            return false;
+        st.info = sm.info[st.stage];
+        st.s = sm.scale[st.stage][row()];
+        if (st.info.flags & kFirstOfBlock) {
+            ++k_block;
+            if (!warp_wait(smem_u32(&sm.q_full[st.info.qbuf]), (k_block >> 1) & 1, wctx))
+                return false;
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&sm.empty[st.stage]));
+        st.buf = v & 1;
+        if (!warp_wait(smem_u32(&sm.acc_full[st.buf]), (v >> 1) & 1, wctx))
+            return false;
+        tc_fence_after();
+        st.negw = __any_sync(0xffffffffu, st.s < 0.f);
+        return true;
+    }
+
+    __device__ __forceinline__ uint32_t taddr(const Unit& st, int batch) const
+    {
+        return tmem_base + ((uint32_t)(quad * 32) << 16) +
+               (uint32_t)(st.buf * kMaxN + tok0 * H + batch * 64);
+    }
+
+    __device__ __forceinline__ void issue(const Unit& st, int batch, float (&x)[64])
+    {
+        float(&lo)[32] = *reinterpret_cast<float(*)[32]>(&x[0]);
+        float(&hi)[32] = *reinterpret_cast<float(*)[32]>(&x[32]);
+        tmem_ld32_async(taddr(st, batch), lo);
+        tmem_ld32_async(taddr(st, batch) + 32, hi);
+    }
+
+    __device__ __forceinline__ void land(float (&x)[64])
+    {
+        float(&lo)[32] = *reinterpret_cast<float(*)[32]>(&x[0]);
+        float(&hi)[32] = *reinterpret_cast<float(*)[32]>(&x[32]);
+        tmem_wait32(lo);
+        tmem_wait32(hi);
+    }
+
+    __device__ __forceinline__ void release(const Unit& st)
+    {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&sm.acc_empty[st.buf]));
+    }
+
+    __device__ __forceinline__ void finish(const Unit& st)
+    {
+        if (st.info.flags & kLastOfBlock) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&sm.q_empty[st.info.qbuf]));
+        }
+    }
+
+    // Reduce batch `batch` (tokens batch*kTPB .. of this group) and store it.
+    __device__ __forceinline__ void reduce_store(const Unit& st, int batch, const float (&x)[64])
+    {
+        float2 acc2[kTPB][kNP2];
+#pragma unroll
+        for (int a = 0; a < kTPB; ++a)
+#pragma unroll
+            for (int c = 0; c < kNP2; ++c)
+                acc2[a][c] = make_float2(0.f, 0.f);
+        const float4* w4 =
+            reinterpret_cast<const float4*>(&sm.w[st.info.qbuf][tok0 * H + batch * 64]);
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+            const float4 w = w4[c >> 2];
+            const float2 r0 = make_float2(fmaxf(x[c], 0.f), fmaxf(x[c + 1], 0.f));
+            const float2 r1 = make_float2(fmaxf(x[c + 2], 0.f), fmaxf(x[c + 3], 0.f));
+            float2& a0 = acc2[c / H][(c >> 1) % kNP2];
+            a0 = __ffma2_rn(make_float2(w.x, w.y), r0, a0);
+            float2& a1 = acc2[(c + 2) / H][((c + 2) >> 1) % kNP2];
+            a1 = __ffma2_rn(make_float2(w.z, w.w), r1, a1);
+        }
+        // ReLU(s x) = s * max(x, 0) for s >= 0 and s * (x - max(x, 0)) for s < 0;
+        // a warp that holds a negative scale also forms sum_h w * x.
+        float accx[kTPB];
+#pragma unroll
+        for (int a = 0; a < kTPB; ++a)
+            accx[a] = 0.f;
+        if (st.negw) {
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+                const float4 w = w4[c >> 2];
+                accx[c / H] = fmaf(w.x, x[c], accx[c / H]);
+                accx[c / H] = fmaf(w.y, x[c + 1], accx[c / H]);
+                accx[(c + 2) / H] = fmaf(w.z, x[c + 2], accx[(c + 2) / H]);
+                accx[(c + 2) / H] = fmaf(w.w, x[c + 3], accx[(c + 2) / H]);
+            }
+        }
+        const float ninf = __int_as_float(0xff800000u);
+        const bool clean = (p.flags & kFlagClean) != 0;
+        const bool compressed = (p.flags & kFlagCompressed) != 0;
+        const long long j = (long long)st.info.t * kBlockKV + row();
+#pragma unroll
+        for (int a = 0; a < kTPB; ++a) {
+            const int lt = batch * kTPB + a;          // token within this group
+            if (lt < ntok) {
+                const int tk = tok0 + lt;
+                const int r = st.info.b * p.tok + tk;
+                if (r < p.rows) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kNP2; ++c)
+                        sum += acc2[a][c].x + acc2[a][c].y;
+                    const float v = (st.s >= 0.f) ? st.s * sum : st.s * (accx[a] - sum);
+                    const int2 rg = sm.range[st.info.qbuf][tk];
+                    const bool valid = j >= rg.x && j < rg.y;
+                    float* out = p.logits + (long long)r * p.ldo;
+                    if (compressed) {
+                        if (valid && j - rg.x < p.ldo)
+                            out[j - rg.x] = v;
+                    } else if (j < p.width) {
+                        if (valid)
+                            out[j] = v;
+                        else if (clean)
+                            out[j] = ninf;
+                    }
+                }
+            }
+        }
+    }
+
+    // NB batches of 64 columns per unit (NB = 1 or 2).  Buffer use alternates
+    // x0, x1 batch by batch, so the unit loop is unrolled by 2 when NB == 1.
+    template <int NB>
+    __device__ __forceinline__ void run()
+    {
+        if (n_units <= 0)
+            return;
+        float x0[64], x1[64];
+        Unit cur, nxt;
+        if (!begin(0, cur))
+            return;
+        issue(cur, 0, x0);
+        land(x0);
+        int u = 0;
+        while (true) {
+            // ---- x0 holds batch 0 of unit u
+            if (NB == 2) {
+                issue(cur, 1, x1);
+                reduce_store(cur, 0, x0);
+                land(x1);
+                release(cur);
+                const bool more = u + 1 < n_units;
+                if (more) {
+                    if (!begin(u + 1, nxt))
+                        return;
+                    issue(nxt, 0, x0);
+                }
+                reduce_store(cur, 1, x1);
+                finish(cur);
+                if (!more)
+                    return;
+                land(x0);
+                cur = nxt;
+                ++u;
+            } else {
+                release(cur);
+                bool more = u + 1 < n_units;
+                if (more) {
+                    if (!begin(u + 1, nxt))
+                        return;
+                    issue(nxt, 0, x1);
+                }
+                reduce_store(cur, 0, x0);
+                finish(cur);
+                if (!more)
+                    return;
+                land(x1);
+                cur = nxt;
+                ++u;
+                // ---- x1 holds batch 0 of unit u
+                release(cur);
+                more = u + 1 < n_units;
+                if (more) {
+                    if (!begin(u + 1, nxt))
+                        return;
+                    issue(nxt, 0, x0);
+                }
+                reduce_store(cur, 0, x1);
+                finish(cur);
+                if (!more)
+                    return;
+                land(x0);
+                cur = nxt;
+                ++u;
+            }
+        }
+    }
+
+    // A group with no columns in the unit still takes part in every hand-off.
+    __device__ __forceinline__ void run_empty()
+    {
+        for (int u = 0; u < n_units; ++u) {
+            Unit cur;
+            if (!begin(u, cur))
+                return;
+            release(cur);
+            finish(cur);
+        }
+    }
+};
+
 // ------------------------------------------------------------------ kernel
 template <int H, int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -230,16 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
-    constexpr int kTPWMax = 128 / H;               // tokens per epilogue warp group, max
-    constexpr int kNP2 = (H >= 32) ? 2 : 1;        // pair accumulators per token
-    constexpr int kCW = (H <= 16) ? 16 : 32;       // TMEM columns per load
-    constexpr int kMaxChunks = 128 / kCW;
     // Register split after set-up (launch: 384 threads x 168 = 64512): the
     // control warp group (producer, MMA, fill) gives registers to the two
-    // epilogue warp groups; 128 * ctl + 256 * epi == 64512.  The paged producer
-    // keeps a page-id window and needs a little more.
-    constexpr int kRegsCtl = PAGED ? 56 : 40;
-    constexpr int kRegsEpi = PAGED ? 224 : 232;
+    // epilogue warp groups, whose double-buffered 2 x 64-column TMEM batches
+    // need most of them; 128 * ctl + 256 * epi == 64512.
+    constexpr int kRegsCtl = 56;
+    constexpr int kRegsEpi = 224;
     static_assert(128 * kRegsCtl + 256 * kRegsEpi <= kThreads * 168, "register split exceeds launch");
     static_assert(H >= 8 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two in [8,128]");
     static_assert(D == 64 || D == 128, "D must be 64 or 128");
@@ -572,167 +821,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ================================================= epilogue
         regs_inc<kRegsEpi>();
-        const int g = (warp - kEpiWarp0) >> 2;         // warp group 0 / 1
-        const int quad = warp & 3;                      // TMEM lane quadrant
-        const int row = quad * 32 + lane;               // key within the tile
-        const int tok_lo = (p.tok + 1) >> 1;
-        const int tok0 = g == 0 ? 0 : tok_lo;
-        const int ntok = g == 0 ? tok_lo : p.tok - tok_lo;
-        const int col0 = tok0 * H;
-        const int ncols = ntok * H;
-        const bool clean = (p.flags & kFlagClean) != 0;
-        const bool compressed = (p.flags & kFlagCompressed) != 0;
-        const float ninf = __int_as_float(0xff800000u);
-        float2 wr2[64];
-#pragma unroll
-        for (int k = 0; k < 64; ++k)
-            wr2[k] = make_float2(0.f, 0.f);
-        int k_block = -1;
-        int qb = 0;
-        for (int u = 0; u < n_units; ++u) {
-            const int stage = u % S;
-            if (!warp_wait(smem_u32(&sm.full[stage]), (u / S) & 1, wctx))
-                break;
-            const UnitInfo info = sm.info[stage];
-            const float s = sm.scale[stage][row];
-            if (info.flags & kFirstOfBlock) {
-                ++k_block;
-                qb = info.qbuf;
-                if (!warp_wait(smem_u32(&sm.q_full[qb]), (k_block >> 1) & 1, wctx))
-                    break;
-                const float4* w4 = reinterpret_cast<const float4*>(&sm.w[qb][col0]);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    if (4 * k < ncols) {
-                        const float4 v = w4[k];
-                        wr2[2 * k] = make_float2(v.x, v.y);
-                        wr2[2 * k + 1] = make_float2(v.z, v.w);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&sm.empty[stage]));
-
-            const int buf = u & 1;
-            if (!warp_wait(smem_u32(&sm.acc_full[buf]), (u >> 1) & 1, wctx))
-                break;
-            tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * kMaxN + col0);
-            const bool negw = __any_sync(0xffffffffu, s < 0.f);
-
-            // Head reduction in packed fp32 pairs: columns (2c, 2c+1) of a token
-            // go through one FFMA2; kNP2 independent pair-accumulators per token.
-            float2 acc2[kTPWMax][kNP2];
-#pragma unroll
-            for (int a = 0; a < kTPWMax; ++a)
-#pragma unroll
-                for (int c = 0; c < kNP2; ++c)
-                    acc2[a][c] = make_float2(0.f, 0.f);
-            // TMEM -> registers in kCW-column chunks, double-buffered: the load
-            // of chunk c+1 is in flight while chunk c is reduced.  Unless a
-            // negative scale needs a second pass, the accumulator buffer is
-            // handed back to the MMA warp once the last chunk has landed,
-            // before its arithmetic.
-            const int nch = (ncols + kCW - 1) / kCW;
-            float xa[kCW], xb[kCW];
-            if (nch > 0) {
-                tmem_ld_async<kCW>(taddr, xa);
-                tmem_wait<kCW>(xa);
-            } else if (!negw) {   // this warp group has no columns in the unit
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&sm.acc_empty[buf]));
-            }
-#pragma unroll
-            for (int ch = 0; ch < kMaxChunks; ++ch) {
-                if (ch < nch) {
-                    float(&xc)[kCW] = (ch & 1) ? xb : xa;
-                    float(&xn)[kCW] = (ch & 1) ? xa : xb;
-                    const bool more = ch + 1 < nch;
-                    if (more) {
-                        tmem_ld_async<kCW>(taddr + (ch + 1) * kCW, xn);
-                    } else if (!negw) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(smem_u32(&sm.acc_empty[buf]));
-                    }
-#pragma unroll
-                    for (int k = 0; k < kCW; k += 2) {
-                        const int col = ch * kCW + k;
-                        const float2 r = make_float2(fmaxf(xc[k], 0.f), fmaxf(xc[k + 1], 0.f));
-                        float2& a = acc2[col / H][(k >> 1) % kNP2];
-                        a = __ffma2_rn(wr2[col >> 1], r, a);
-                    }
-                    if (more)
-                        tmem_wait<kCW>(xn);
-                }
-            }
-            // Rare path (a warp holding a negative scale): sum_h w * x as well,
-            // from a second pass over the same TMEM columns.
-            float accx[kTPWMax];
-#pragma unroll
-            for (int a = 0; a < kTPWMax; ++a)
-                accx[a] = 0.f;
-            if (negw) {
-#pragma unroll
-                for (int ch = 0; ch < kMaxChunks; ++ch) {
-                    if (ch < nch) {
-                        float xc[kCW];
-                        tmem_ld_async<kCW>(taddr + ch * kCW, xc);
-                        tmem_wait<kCW>(xc);
-#pragma unroll
-                        for (int k = 0; k < kCW; k += 2) {
-                            const int col = ch * kCW + k;
-                            accx[col / H] = fmaf(wr2[col >> 1].x, xc[k], accx[col / H]);
-                            accx[col / H] = fmaf(wr2[col >> 1].y, xc[k + 1], accx[col / H]);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&sm.acc_empty[buf]));
-            }
-
-            // ---- range-masked stores
-            const long long j = (long long)info.t * kBlockKV + row;
-#pragma unroll
-            for (int a = 0; a < kTPWMax; ++a) {
-                if (a < ntok) {
-                    const int tk = tok0 + a;
-                    const int r = info.b * p.tok + tk;   // output row (both paths)
-                    if (r < p.rows) {
-                        float sum = 0.f;
-#pragma unroll
-                        for (int c = 0; c < kNP2; ++c)
-                            sum += acc2[a][c].x + acc2[a][c].y;
-                        // ReLU(s x) = s * max(x, 0) for s >= 0, s * (x - max(x, 0)) for s < 0
-                        const float v = (s >= 0.f) ? s * sum : s * (accx[a] - sum);
-                        const int2 rg = sm.range[qb][tk];
-                        const bool valid = j >= rg.x && j < rg.y;
-                        float* out = p.logits + (long long)r * p.ldo;
-                        if (compressed) {
-                            if (valid && j - rg.x < p.ldo)
-                                out[j - rg.x] = v;
-                        } else if (j < p.width) {
-                            if (valid)
-                                out[j] = v;
-                            else if (clean)
-                                out[j] = ninf;
-                        }
-                    }
-                }
-            }
-            if (info.flags & kLastOfBlock) {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&sm.q_empty[qb]));
-            }
-        }
+        const int g = (warp - kEpiWarp0) >> 2;          // warp group 0 / 1
+        const int tok0 = g == 0 ? 0 : p.tok_split;
+        const int ntok = g == 0 ? p.tok_split : p.tok - p.tok_split;
+        const int nb = (ntok * H + 63) >> 6;            // 64-column batches of this group
+        Epilogue<H, D> epi{sm, p, wctx, tmem_base, n_units, warp & 3, lane, tok0, ntok};
+        if (nb == 2)
+            epi.template run<2>();
+        else if (nb == 1)
+            epi.template run<1>();
+        else
+            epi.run_empty();
         tc_fence_before();
     }
 
