@@ -235,7 +235,8 @@ struct Epilogue {
     using C = Cfg<D>;
     static constexpr int S = C::kStages;
     static constexpr int kTPB = 64 / H;   // tokens per 64-column batch
-    static constexpr int kNP2 = (H >= 32) ? 2 : 1;
+    // independent pair-accumulators per token: keeps every FFMA2 chain short
+    static constexpr int kNP2 = (H >= 64) ? 8 : ((H >= 32) ? 4 : 1);
 
     struct Unit {
         int stage;
@@ -377,16 +378,12 @@ struct Epilogue {
                     const float v = (st.s >= 0.f) ? st.s * sum : st.s * (accx[a] - sum);
                     const int2 rg = sm.range[st.info.qbuf][tk];
                     const bool valid = j >= rg.x && j < rg.y;
-                    float* out = p.logits + (long long)r * p.ldo;
-                    if (compressed) {
-                        if (valid && j - rg.x < p.ldo)
-                            out[j - rg.x] = v;
-                    } else if (j < p.width) {
-                        if (valid)
-                            out[j] = v;
-                        else if (clean)
-                            out[j] = ninf;
-                    }
+                    // one predicated store: the logit, -inf (clean) or nothing
+                    const long long col = compressed ? j - rg.x : j;
+                    const bool store = compressed ? (valid && col < p.ldo)
+                                                  : (j < p.width && (valid || clean));
+                    if (store)
+                        p.logits[(long long)r * p.ldo + col] = valid ? v : ninf;
                 }
             }
         }
@@ -493,9 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(H >= 8 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two in [8,128]");
     static_assert(D == 64 || D == 128, "D must be 64 or 128");
 
-    extern __shared__ uint8_t smem_raw[];
-    Smem<D>& sm = *reinterpret_cast<Smem<D>*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // Align the dynamic shared memory to 1024 B (the 128-byte swizzle repeat)
+    // by pointer arithmetic on the shared array itself, so every access
+    // through `sm` stays a shared-memory access (no generic addressing).
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw + pad);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
