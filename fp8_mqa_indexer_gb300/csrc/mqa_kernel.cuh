@@ -222,21 +222,19 @@ constexpr unsigned kProducerSleepNs = 256;
 constexpr unsigned kMmaSleepNs = 32;
 
 // --------------------------------------------------------------- epilogue
-// Epilogue of one warp group: per work unit it reads its columns of the TMEM
-// accumulator (keys on lanes, (token, head) on columns), reduces
-// sum_h w[h] * max(x, 0) per token, scales by s[j] and writes the row-masked
-// logits.  Columns are read in batches of 64 (two 32-column TMEM loads)
-// double-buffered across units: the load of the next batch -- of this unit or
-// of the next one -- is in flight while the current batch is reduced.
-// Weights are read from shared memory with broadcast 16-byte loads.
+// Epilogue of one warp group: per work unit it copies its columns of the TMEM
+// accumulator (keys on lanes, (token, head) on columns) into registers with one
+// wait, hands the accumulator back to the MMA warp at once, then reduces
+// sum_h w[h] * max(x, 0) per token with packed FFMA2, scales by s[j] and writes
+// the row-masked logits.  Weights come from shared memory as broadcast 16-byte
+// loads.
 template <int H, int D>
 struct Epilogue {
-    static_assert(H >= 8 && H <= 64, "a 64-column batch must hold whole tokens");
+    static_assert(H >= 8 && H <= 64, "a warp group's columns must hold whole tokens");
     using C = Cfg<D>;
     static constexpr int S = C::kStages;
-    static constexpr int kTPB = 64 / H;   // tokens per 64-column batch
     // independent pair-accumulators per token: keeps every FFMA2 chain short
-    static constexpr int kNP2 = (H >= 64) ? 8 : ((H >= 32) ? 4 : 1);
+    static constexpr int kNP2 = (H >= 32) ? 4 : 1;
 
     struct Unit {
         int stage;
@@ -284,26 +282,37 @@ struct Epilogue {
         return true;
     }
 
-    __device__ __forceinline__ uint32_t taddr(const Unit& st, int batch) const
+    __device__ __forceinline__ uint32_t taddr(const Unit& st) const
     {
-        return tmem_base + ((uint32_t)(quad * 32) << 16) +
-               (uint32_t)(st.buf * kMaxN + tok0 * H + batch * 64);
+        return tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(st.buf * kMaxN + tok0 * H);
     }
 
-    __device__ __forceinline__ void issue(const Unit& st, int batch, float (&x)[64])
+    template <int C>
+    static __device__ __forceinline__ float (&chunk(float (&x)[128]))[32]
     {
-        float(&lo)[32] = *reinterpret_cast<float(*)[32]>(&x[0]);
-        float(&hi)[32] = *reinterpret_cast<float(*)[32]>(&x[32]);
-        tmem_ld32_async(taddr(st, batch), lo);
-        tmem_ld32_async(taddr(st, batch) + 32, hi);
+        return *reinterpret_cast<float(*)[32]>(&x[32 * C]);
     }
 
-    __device__ __forceinline__ void land(float (&x)[64])
+    // All NCH 32-column chunks of this group's columns of the unit, then one
+    // wait: the accumulator can be handed back right after.
+    template <int NCH>
+    __device__ __forceinline__ void load_all(const Unit& st, float (&x)[128])
     {
-        float(&lo)[32] = *reinterpret_cast<float(*)[32]>(&x[0]);
-        float(&hi)[32] = *reinterpret_cast<float(*)[32]>(&x[32]);
-        tmem_wait32(lo);
-        tmem_wait32(hi);
+        const uint32_t a = taddr(st);
+        tmem_ld32_async(a, chunk<0>(x));
+        if constexpr (NCH > 1)
+            tmem_ld32_async(a + 32, chunk<1>(x));
+        if constexpr (NCH > 2)
+            tmem_ld32_async(a + 64, chunk<2>(x));
+        if constexpr (NCH > 3)
+            tmem_ld32_async(a + 96, chunk<3>(x));
+        tmem_wait32(chunk<0>(x));
+        if constexpr (NCH > 1)
+            tmem_wait32(chunk<1>(x));
+        if constexpr (NCH > 2)
+            tmem_wait32(chunk<2>(x));
+        if constexpr (NCH > 3)
+            tmem_wait32(chunk<3>(x));
     }
 
     __device__ __forceinline__ void release(const Unit& st)
@@ -323,19 +332,21 @@ struct Epilogue {
         }
     }
 
-    // Reduce batch `batch` (tokens batch*kTPB .. of this group) and store it.
-    __device__ __forceinline__ void reduce_store(const Unit& st, int batch, const float (&x)[64])
+    // Reduce the NCH*32 loaded columns per token and store the logits.
+    template <int NCH>
+    __device__ __forceinline__ void reduce_store(const Unit& st, const float (&x)[128])
     {
-        float2 acc2[kTPB][kNP2];
+        constexpr int NC = NCH * 32;
+        constexpr int NT = (NC + H - 1) / H;   // tokens covered by the loaded columns
+        float2 acc2[NT][kNP2];
 #pragma unroll
-        for (int a = 0; a < kTPB; ++a)
+        for (int a = 0; a < NT; ++a)
 #pragma unroll
             for (int c = 0; c < kNP2; ++c)
                 acc2[a][c] = make_float2(0.f, 0.f);
-        const float4* w4 =
-            reinterpret_cast<const float4*>(&sm.w[st.info.qbuf][tok0 * H + batch * 64]);
+        const float4* w4 = reinterpret_cast<const float4*>(&sm.w[st.info.qbuf][tok0 * H]);
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < NC; c += 4) {
             const float4 w = w4[c >> 2];
             const float2 r0 = make_float2(fmaxf(x[c], 0.f), fmaxf(x[c + 1], 0.f));
             const float2 r1 = make_float2(fmaxf(x[c + 2], 0.f), fmaxf(x[c + 3], 0.f));
@@ -345,115 +356,66 @@ struct Epilogue {
             a1 = __ffma2_rn(make_float2(w.z, w.w), r1, a1);
         }
         // ReLU(s x) = s * max(x, 0) for s >= 0 and s * (x - max(x, 0)) for s < 0;
-        // a warp that holds a negative scale also forms sum_h w * x.
-        float accx[kTPB];
+        // a warp that holds a negative scale also forms sum_h w * x, from a
+        // second pass over the TMEM columns (it kept the accumulator for this).
+        float accx[NT];
 #pragma unroll
-        for (int a = 0; a < kTPB; ++a)
+        for (int a = 0; a < NT; ++a)
             accx[a] = 0.f;
         if (st.negw) {
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                const float4 w = w4[c >> 2];
-                accx[c / H] = fmaf(w.x, x[c], accx[c / H]);
-                accx[c / H] = fmaf(w.y, x[c + 1], accx[c / H]);
-                accx[(c + 2) / H] = fmaf(w.z, x[c + 2], accx[(c + 2) / H]);
-                accx[(c + 2) / H] = fmaf(w.w, x[c + 3], accx[(c + 2) / H]);
+            for (int ch = 0; ch < NCH; ++ch) {
+                float xc[32];
+                tmem_ld32(taddr(st) + 32 * ch, xc);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int c = 32 * ch + k;
+                    accx[c / H] = fmaf(sm.w[st.info.qbuf][tok0 * H + c], xc[k], accx[c / H]);
+                }
             }
+            release(st);
         }
         const float ninf = __int_as_float(0xff800000u);
         const bool clean = (p.flags & kFlagClean) != 0;
         const bool compressed = (p.flags & kFlagCompressed) != 0;
         const long long j = (long long)st.info.t * kBlockKV + row();
+        const int r0 = st.info.b * p.tok + tok0;
 #pragma unroll
-        for (int a = 0; a < kTPB; ++a) {
-            const int lt = batch * kTPB + a;          // token within this group
-            if (lt < ntok) {
-                const int tk = tok0 + lt;
-                const int r = st.info.b * p.tok + tk;
-                if (r < p.rows) {
-                    float sum = 0.f;
-#pragma unroll
-                    for (int c = 0; c < kNP2; ++c)
-                        sum += acc2[a][c].x + acc2[a][c].y;
-                    const float v = (st.s >= 0.f) ? st.s * sum : st.s * (accx[a] - sum);
-                    const int2 rg = sm.range[st.info.qbuf][tk];
-                    const bool valid = j >= rg.x && j < rg.y;
-                    // one predicated store: the logit, -inf (clean) or nothing
-                    const long long col = compressed ? j - rg.x : j;
-                    const bool store = compressed ? (valid && col < p.ldo)
-                                                  : (j < p.width && (valid || clean));
-                    if (store)
-                        p.logits[(long long)r * p.ldo + col] = valid ? v : ninf;
+        for (int a = 0; a < NT; ++a) {
+            if (a < ntok && r0 + a < p.rows) {
+                float2 t2 = acc2[a][0];
+                if constexpr (kNP2 == 4) {
+                    t2 = __fadd2_rn(__fadd2_rn(acc2[a][0], acc2[a][1]),
+                                    __fadd2_rn(acc2[a][2], acc2[a][3]));
                 }
+                const float sum = t2.x + t2.y;
+                const float v = (st.s >= 0.f) ? st.s * sum : st.s * (accx[a] - sum);
+                const int2 rg = sm.range[st.info.qbuf][tok0 + a];
+                const bool valid = j >= rg.x && j < rg.y;
+                // one predicated store: the logit, -inf (clean) or nothing
+                const long long col = compressed ? j - rg.x : j;
+                const bool store = compressed ? (valid && col < p.ldo)
+                                              : (j < p.width && (valid || clean));
+                if (store)
+                    p.logits[(long long)(r0 + a) * p.ldo + col] = valid ? v : ninf;
             }
         }
     }
 
-    // NB batches of 64 columns per unit (NB = 1 or 2).  Buffer use alternates
-    // x0, x1 batch by batch, so the unit loop is unrolled by 2 when NB == 1.
-    template <int NB>
+    // NCH = number of 32-column chunks this group owns (compile time).
+    template <int NCH>
     __device__ __forceinline__ void run()
     {
-        if (n_units <= 0)
-            return;
-        float x0[64], x1[64];
-        Unit cur, nxt;
-        if (!begin(0, cur))
-            return;
-        issue(cur, 0, x0);
-        land(x0);
-        int u = 0;
-        while (true) {
-            // ---- x0 holds batch 0 of unit u
-            if (NB == 2) {
-                issue(cur, 1, x1);
-                reduce_store(cur, 0, x0);
-                land(x1);
-                release(cur);
-                const bool more = u + 1 < n_units;
-                if (more) {
-                    if (!begin(u + 1, nxt))
-                        return;
-                    issue(nxt, 0, x0);
-                }
-                reduce_store(cur, 1, x1);
-                finish(cur);
-                if (!more)
-                    return;
-                land(x0);
-                cur = nxt;
-                ++u;
-            } else {
-                release(cur);
-                bool more = u + 1 < n_units;
-                if (more) {
-                    if (!begin(u + 1, nxt))
-                        return;
-                    issue(nxt, 0, x1);
-                }
-                reduce_store(cur, 0, x0);
-                finish(cur);
-                if (!more)
-                    return;
-                land(x1);
-                cur = nxt;
-                ++u;
-                // ---- x1 holds batch 0 of unit u
-                release(cur);
-                more = u + 1 < n_units;
-                if (more) {
-                    if (!begin(u + 1, nxt))
-                        return;
-                    issue(nxt, 0, x0);
-                }
-                reduce_store(cur, 0, x1);
-                finish(cur);
-                if (!more)
-                    return;
-                land(x0);
-                cur = nxt;
-                ++u;
-            }
+        float x[128];
+        for (int u = 0; u < n_units; ++u) {
+            Unit st;
+            if (!begin(u, st))
+                return;
+            load_all<NCH>(st, x);
+            if (!st.negw)
+                release(st);
+            reduce_store<NCH>(st, x);   // releases the accumulator itself if negw
+            finish(st);
         }
     }
 
@@ -824,11 +786,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = (warp - kEpiWarp0) >> 2;          // warp group 0 / 1
         const int tok0 = g == 0 ? 0 : p.tok_split;
         const int ntok = g == 0 ? p.tok_split : p.tok - p.tok_split;
-        const int nb = (ntok * H + 63) >> 6;            // 64-column batches of this group
+        const int nch = (ntok * H + 31) >> 5;           // 32-column chunks of this group
         Epilogue<H, D> epi{sm, p, wctx, tmem_base, n_units, warp & 3, lane, tok0, ntok};
-        if (nb == 2)
+        if (nch >= 4)
+            epi.template run<4>();
+        else if (nch == 3)
+            epi.template run<3>();
+        else if (nch == 2)
             epi.template run<2>();
-        else if (nb == 1)
+        else if (nch == 1)
             epi.template run<1>();
         else
             epi.run_empty();
