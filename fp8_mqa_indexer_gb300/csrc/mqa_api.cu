@@ -478,7 +478,6 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
     p.k_end = k_end;
     p.width = S_kv;
     p.tok = tok;
-    p.tok_split = tok / 2;
     p.num_q_blocks = (S_q + tok - 1) / tok;
     p.rows = S_q;
     p.wait_limit = (long long)g_wait_limit.load();
@@ -513,16 +512,6 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
         return fail(MQA_ERR_UNSUPPORTED, "H must be 16, 32 or 64 (got %d)", H);
     if (next_n * H > kMaxN || (next_n * H) % 16 != 0)
         return fail(MQA_ERR_UNSUPPORTED, "next_n * H must be a multiple of 16 and <= 256");
-    // Tokens of epilogue warp group 0: about half, rounded up so that group 1
-    // starts on a 32-column boundary of the accumulator.
-    const int tok_quantum = H >= 32 ? 1 : 32 / H;
-    int tok_split = (next_n + 1) / 2;
-    tok_split = (tok_split + tok_quantum - 1) / tok_quantum * tok_quantum;
-    if (tok_split > next_n)
-        tok_split = next_n;
-    if (tok_split * H > 128 || (next_n - tok_split) * H > 128)
-        return fail(MQA_ERR_UNSUPPORTED, "next_n=%d does not split over the epilogue for H=%d",
-                    next_n, H);
     if (block_kv != 32 && block_kv != 64 && block_kv != 128)
         return fail(MQA_ERR_UNSUPPORTED, "block_kv must be 32, 64 or 128 (got %d)", block_kv);
     const long long width = (long long)max_blocks_per_seq * block_kv;
@@ -599,7 +588,6 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     p.max_blocks = max_blocks_per_seq;
     p.width = width;
     p.tok = next_n;
-    p.tok_split = tok_split;
     p.num_q_blocks = B;
     p.rows = B * next_n;
     p.wait_limit = (long long)g_wait_limit.load();

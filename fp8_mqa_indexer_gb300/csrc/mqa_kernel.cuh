@@ -41,9 +41,10 @@ namespace mqa {
 
 constexpr int kBlockKV = 128;      // keys per tile == MMA M == TMEM lanes
 constexpr int kMaxN = 256;         // TMEM columns per accumulator buffer
-constexpr int kThreads = 384;
-constexpr int kEpiWarp0 = 4;       // epilogue warps 4..11
-constexpr int kNumEpiWarps = 8;
+constexpr int kThreads = 640;
+constexpr int kEpiWarp0 = 4;       // epilogue warps 4..19: four warp groups
+constexpr int kNumEpiWarps = 16;
+constexpr int kEpiCols = 64;       // accumulator columns per epilogue warp group
 
 enum : unsigned { kFlagClean = 1u, kFlagCompressed = 2u };
 enum : int { kFirstOfBlock = 1, kLastOfBlock = 2 };
@@ -75,7 +76,6 @@ struct Params {
     // shared
     long long width;     // logical columns of an uncompressed row
     int tok;             // query tokens per work unit
-    int tok_split;       // tokens of epilogue warp group 0 (group 1 takes the rest)
     int num_q_blocks;    // dense: ceil(S_q / tok); paged: B
     int rows;            // output rows: S_q or B * next_n
     long long wait_limit;
@@ -272,8 +272,7 @@ struct Epilogue {
                 return false;
         }
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(&sm.empty[st.stage]));
+        mbar_arrive_one_per_warp(smem_u32(&sm.empty[st.stage]));
         st.buf = v & 1;
         if (!warp_wait(smem_u32(&sm.acc_full[st.buf]), (v >> 1) & 1, wctx))
             return false;
@@ -288,7 +287,7 @@ struct Epilogue {
     }
 
     template <int C>
-    static __device__ __forceinline__ float (&chunk(float (&x)[128]))[32]
+    static __device__ __forceinline__ float (&chunk(float (&x)[kEpiCols]))[32]
     {
         return *reinterpret_cast<float(*)[32]>(&x[32 * C]);
     }
@@ -296,45 +295,36 @@ struct Epilogue {
     // All NCH 32-column chunks of this group's columns of the unit, then one
     // wait: the accumulator can be handed back right after.
     template <int NCH>
-    __device__ __forceinline__ void load_all(const Unit& st, float (&x)[128])
+    __device__ __forceinline__ void load_all(const Unit& st, float (&x)[kEpiCols])
     {
+        static_assert(NCH >= 1 && NCH <= 2, "a warp group owns at most 64 columns");
         const uint32_t a = taddr(st);
         tmem_ld32_async(a, chunk<0>(x));
         if constexpr (NCH > 1)
             tmem_ld32_async(a + 32, chunk<1>(x));
-        if constexpr (NCH > 2)
-            tmem_ld32_async(a + 64, chunk<2>(x));
-        if constexpr (NCH > 3)
-            tmem_ld32_async(a + 96, chunk<3>(x));
         tmem_wait32(chunk<0>(x));
         if constexpr (NCH > 1)
             tmem_wait32(chunk<1>(x));
-        if constexpr (NCH > 2)
-            tmem_wait32(chunk<2>(x));
-        if constexpr (NCH > 3)
-            tmem_wait32(chunk<3>(x));
     }
 
     __device__ __forceinline__ void release(const Unit& st)
     {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(&sm.acc_empty[st.buf]));
+        mbar_arrive_one_per_warp(smem_u32(&sm.acc_empty[st.buf]));
     }
 
     __device__ __forceinline__ void finish(const Unit& st)
     {
         if (st.info.flags & kLastOfBlock) {
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&sm.q_empty[st.info.qbuf]));
+            mbar_arrive_one_per_warp(smem_u32(&sm.q_empty[st.info.qbuf]));
         }
     }
 
     // Reduce the NCH*32 loaded columns per token and store the logits.
     template <int NCH>
-    __device__ __forceinline__ void reduce_store(const Unit& st, const float (&x)[128])
+    __device__ __forceinline__ void reduce_store(const Unit& st, const float (&x)[kEpiCols])
     {
         constexpr int NC = NCH * 32;
         constexpr int NT = (NC + H - 1) / H;   // tokens covered by the loaded columns
@@ -406,7 +396,7 @@ struct Epilogue {
     template <int NCH>
     __device__ __forceinline__ void run()
     {
-        float x[128];
+        float x[kEpiCols];
         for (int u = 0; u < n_units; ++u) {
             Unit st;
             if (!begin(u, st))
@@ -442,13 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
-    // Register split after set-up (launch: 384 threads x 168 = 64512): the
-    // control warp group (producer, MMA, fill) gives registers to the two
-    // epilogue warp groups, whose double-buffered 2 x 64-column TMEM batches
-    // need most of them; 128 * ctl + 256 * epi == 64512.
-    constexpr int kRegsCtl = 56;
-    constexpr int kRegsEpi = 224;
-    static_assert(128 * kRegsCtl + 256 * kRegsEpi <= kThreads * 168, "register split exceeds launch");
+    // Register split after set-up (launch: 640 threads x 96 = 61440): the
+    // control warp group (producer, MMA, fill) gives registers to the four
+    // epilogue warp groups, which hold a 64-column TMEM slice each;
+    // 128 * ctl + 512 * epi <= 61440.
+    constexpr int kRegsCtl = 40;
+    constexpr int kRegsEpi = 104;
+    static_assert(128 * kRegsCtl + 512 * kRegsEpi <= kThreads * 96, "register split exceeds launch");
     static_assert(H >= 8 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two in [8,128]");
     static_assert(D == 64 || D == 128, "D must be 64 or 128");
 
@@ -783,16 +773,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ================================================= epilogue
         regs_inc<kRegsEpi>();
-        const int g = (warp - kEpiWarp0) >> 2;          // warp group 0 / 1
-        const int tok0 = g == 0 ? 0 : p.tok_split;
-        const int ntok = g == 0 ? p.tok_split : p.tok - p.tok_split;
+        // Warp group g owns accumulator columns [64 g, 64 g + 64): tokens
+        // [g * 64 / H, (g + 1) * 64 / H) of the unit's query block.
+        const int g = (warp - kEpiWarp0) >> 2;          // warp group 0..3
+        const int tpg = kEpiCols / H;                   // tokens per group
+        const int tok0 = g * tpg;
+        const int ntok = max(0, min(tpg, p.tok - tok0));
         const int nch = (ntok * H + 31) >> 5;           // 32-column chunks of this group
         Epilogue<H, D> epi{sm, p, wctx, tmem_base, n_units, warp & 3, lane, tok0, ntok};
-        if (nch >= 4)
-            epi.template run<4>();
-        else if (nch == 3)
-            epi.template run<3>();
-        else if (nch == 2)
+        if (nch >= 2)
             epi.template run<2>();
         else if (nch == 1)
             epi.template run<1>();
