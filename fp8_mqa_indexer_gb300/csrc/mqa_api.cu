@@ -403,8 +403,8 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
         return fail(MQA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", D);
     if (H != 8 && H != 32 && H != 64)
         return fail(MQA_ERR_UNSUPPORTED, "H must be 8, 32 or 64 (got %d)", H);
-    if ((long long)S_q * H >= INT_MAX)
-        return fail(MQA_ERR_INVALID_ARG, "S_q * H too large");
+    if ((long long)S_q * H >= INT_MAX || S_kv > INT_MAX - 256)
+        return fail(MQA_ERR_INVALID_ARG, "S_q * H or S_kv too large");
     if (!compressed && ldo < S_kv)
         return fail(MQA_ERR_INVALID_ARG, "ldo (%lld) < S_kv (%d)", (long long)ldo, S_kv);
     if (compressed && ldo < 1)
@@ -477,6 +477,7 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
     p.k_start = k_start;
     p.k_end = k_end;
     p.width = S_kv;
+    p.width_i = S_kv;
     p.tok = tok;
     p.num_q_blocks = (S_q + tok - 1) / tok;
     p.rows = S_q;
@@ -518,7 +519,7 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     if (ldo < width)
         return fail(MQA_ERR_INVALID_ARG, "ldo (%lld) < max_blocks_per_seq * block_kv (%lld)",
                     (long long)ldo, width);
-    if (width >= INT_MAX || (long long)num_blocks * block_kv >= INT_MAX ||
+    if (width > INT_MAX - 256 || (long long)num_blocks * block_kv >= INT_MAX ||
         (long long)B * next_n * H >= INT_MAX)
         return fail(MQA_ERR_INVALID_ARG, "size too large");
     if (B == 0)
@@ -587,6 +588,7 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     p.block_kv = block_kv;
     p.max_blocks = max_blocks_per_seq;
     p.width = width;
+    p.width_i = (int)width;
     p.tok = next_n;
     p.num_q_blocks = B;
     p.rows = B * next_n;

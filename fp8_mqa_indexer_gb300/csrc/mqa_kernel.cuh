@@ -75,6 +75,7 @@ struct Params {
     int max_blocks;
     // shared
     long long width;     // logical columns of an uncompressed row
+    int width_i;         // the same, as an int (below 2^31 - 256)
     int tok;             // query tokens per work unit
     int num_q_blocks;    // dense: ceil(S_q / tok); paged: B
     int rows;            // output rows: S_q or B * next_n
@@ -368,7 +369,8 @@ struct Epilogue {
         const float ninf = __int_as_float(0xff800000u);
         const bool clean = (p.flags & kFlagClean) != 0;
         const bool compressed = (p.flags & kFlagCompressed) != 0;
-        const long long j = (long long)st.info.t * kBlockKV + row();
+        // key index; the host keeps widths below 2^31 - 256 so this fits an int
+        const int j = st.info.t * kBlockKV + row();
         const int r0 = st.info.b * p.tok + tok0;
 #pragma unroll
         for (int a = 0; a < NT; ++a) {
@@ -383,9 +385,9 @@ struct Epilogue {
                 const int2 rg = sm.range[st.info.qbuf][tok0 + a];
                 const bool valid = j >= rg.x && j < rg.y;
                 // one predicated store: the logit, -inf (clean) or nothing
-                const long long col = compressed ? j - rg.x : j;
+                const int col = compressed ? j - rg.x : j;
                 const bool store = compressed ? (valid && col < p.ldo)
-                                              : (j < p.width && (valid || clean));
+                                              : (j < p.width_i && (valid || clean));
                 if (store)
                     p.logits[(long long)(r0 + a) * p.ldo + col] = valid ? v : ninf;
             }
