@@ -20,6 +20,7 @@ from typing import Optional
 
 __all__ = [
     "MQAError", "mqa_logits", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
+    "paged_mqa_logits_noalloc",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
     "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS",
 ]
@@ -66,6 +67,7 @@ def load_library() -> ctypes.CDLL:
             "mqa_logits": ([P, P, P, P, P, P, P, I, I, I, I, I64, U, P], I),
             "paged_mqa_logits_metadata": ([P, I, I, I, I, P, P], I),
             "paged_mqa_logits": ([P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I64, U, P], I),
+            "paged_mqa_logits_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I64, U, P], I),
             "mqa_get_num_sms": ([I], I),
             "mqa_device_status": ([P], I),
             "mqa_set_wait_limit": ([ULL], I),
@@ -235,6 +237,35 @@ def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
                                                _ptr(schedule_meta), _ptr(logits), B, next_n, H, D,
                                                block_kv, num_blocks, num_sms, ldo, flags,
                                                _stream_handle(stream)))
+    return logits
+
+
+def paged_mqa_logits_noalloc(q, kv_cache, kv_scales, weights, context_lens, block_table,
+                             logits, *, next_n: int, clean: bool = True,
+                             check_bounds: bool = False, stream=None):
+    """Paged decode MQA logits with the work schedule kept in the library's own
+    fixed device array (C ABI ``paged_mqa_logits_noalloc``): no schedule buffer
+    and no allocation.  ``logits`` must be given ([B*next_n, ldo] float32)."""
+    import torch
+    f8 = _fp8_types()
+    _dev(q, "q", f8)
+    _dev(kv_cache, "kv_cache", f8)
+    _dev(kv_scales, "kv_scales", (torch.float32,))
+    _dev(weights, "weights", (torch.float32,))
+    _dev(context_lens, "context_lens", (torch.int32,))
+    _dev(block_table, "block_table", (torch.int32,))
+    R, H, D = q.shape
+    B = context_lens.shape[0]
+    num_blocks, block_kv, _ = kv_cache.shape
+    if not (logits.is_cuda and logits.dtype == torch.float32 and logits.dim() == 2
+            and logits.stride(1) == 1 and logits.shape[0] == R):
+        raise ValueError("logits must be a CUDA float32 [B*next_n, ldo] matrix with unit column stride")
+    flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0)
+    with torch.cuda.device(q.device):
+        _check(load_library().paged_mqa_logits_noalloc(
+            _ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights), _ptr(context_lens),
+            _ptr(block_table), block_table.shape[1], _ptr(logits), B, next_n, H, D, block_kv,
+            num_blocks, logits.stride(0), flags, _stream_handle(stream)))
     return logits
 
 

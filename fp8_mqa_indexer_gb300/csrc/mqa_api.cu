@@ -604,4 +604,51 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     return MQA_OK;
 }
 
+// ------------------------------------------------ no-allocation paged call
+// The schedule lives in this fixed array instead of a caller buffer.  In host
+// code `g_noalloc_schedule` names a host-side stand-in, not a device address:
+// the device address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) int32_t g_noalloc_schedule[2 * (MQA_NOALLOC_MAX_SMS + 1)];
+
+namespace {
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[kMaxDevices];
+}  // namespace
+
+mqa_status paged_mqa_logits_noalloc(const void* q, const void* kv_cache, const float* kv_scales,
+                                    const float* weights, const int32_t* context_lens,
+                                    const int32_t* block_table, int max_blocks_per_seq,
+                                    float* logits, int B, int next_n, int H, int D, int block_kv,
+                                    int num_blocks, int64_t ldo, unsigned flags,
+                                    mqa_stream_t stream)
+{
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+    const int num_sms = g_num_sms[dev];
+    if (num_sms > MQA_NOALLOC_MAX_SMS)
+        return fail(MQA_ERR_UNSUPPORTED, "device has %d SMs; the fixed schedule holds at most %d",
+                    num_sms, MQA_NOALLOC_MAX_SMS);
+    int32_t* sched = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void* ptr = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_schedule);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaGetSymbolAddress(schedule)");
+            g_noalloc_ptr[dev] = static_cast<int32_t*>(ptr);
+        }
+        sched = g_noalloc_ptr[dev];
+    }
+    s = paged_mqa_logits_metadata(context_lens, B, next_n, block_kv, num_sms, sched, stream);
+    if (s != MQA_OK)
+        return s;
+    return paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
+                            max_blocks_per_seq, sched, logits, B, next_n, H, D, block_kv,
+                            num_blocks, num_sms, ldo, flags, stream);
+}
+
 }  // extern "C"

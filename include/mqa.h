@@ -143,6 +143,39 @@ MQA_API mqa_status paged_mqa_logits(const void *q, const void *kv_cache, const f
                             int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
                             unsigned flags, mqa_stream_t stream);
 
+/*
+ * Paged decode MQA logits without any caller-provided or library-allocated
+ * scratch (the pages have no counterpart to this call; it is an addition of
+ * this library).  Arguments are those of paged_mqa_logits minus
+ * schedule_meta and num_sms: the work schedule is written into a fixed array
+ * in the library's own device memory (a file-scope static device array of
+ * MQA_NOALLOC_MAX_SMS + 1 entries that every GPU loading the library holds
+ * until the process exits) and the paged kernel reads it from there.
+ *
+ * For callers that cannot allocate device memory: a C host program or plugin
+ * that has no handle to the framework's allocator owning the GPU, a decode loop
+ * that must not call cudaMalloc because it may implicitly synchronize the
+ * device in the middle of a step, or a service with a fixed, pre-planned
+ * device-memory budget.  The call itself allocates nothing and calls no
+ * allocating routine.
+ *
+ * - The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ * - Devices with more than MQA_NOALLOC_MAX_SMS SMs are rejected with
+ *   MQA_ERR_UNSUPPORTED.
+ * - Every call on a device shares the one array: calls whose work overlaps on
+ *   the GPU (different streams without ordering) race on it.  Each call
+ *   rewrites every entry it uses, so no state from an earlier call leaks in.
+ */
+#define MQA_NOALLOC_MAX_SMS 1024
+MQA_API mqa_status paged_mqa_logits_noalloc(const void *q, const void *kv_cache,
+                                            const float *kv_scales, const float *weights,
+                                            const int32_t *context_lens,
+                                            const int32_t *block_table, int max_blocks_per_seq,
+                                            float *logits, int B, int next_n, int H, int D,
+                                            int block_kv, int num_blocks, int64_t ldo,
+                                            unsigned flags, mqa_stream_t stream);
+
 /* Number of SMs of `device` (cached), or -1 on error. */
 MQA_API int mqa_get_num_sms(int device);
 
