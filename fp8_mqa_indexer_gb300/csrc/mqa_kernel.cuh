@@ -41,10 +41,21 @@ namespace mqa {
 
 constexpr int kBlockKV = 128;      // keys per tile == MMA M == TMEM lanes
 constexpr int kMaxN = 256;         // TMEM columns per accumulator buffer
-constexpr int kThreads = 640;
-constexpr int kEpiWarp0 = 4;       // epilogue warps 4..19: four warp groups
-constexpr int kNumEpiWarps = 16;
-constexpr int kEpiCols = 64;       // accumulator columns per epilogue warp group
+// Thread layout: warp group 0 holds the producer, MMA and fill warps; the
+// epilogue warp groups split the 256 accumulator columns.  kEpiCols picks the
+// split: 64 columns (four epilogue groups, 640 threads) or 128 (two groups,
+// 384 threads).  The register budget follows from the thread count.
+constexpr int kEpiCols = 64;                          // accumulator columns per epilogue group
+constexpr int kNumEpiWarps = 4 * (kMaxN / kEpiCols);
+constexpr int kEpiWarp0 = 4;                          // epilogue warps follow warp group 0
+constexpr int kThreads = 32 * (kEpiWarp0 + kNumEpiWarps);
+constexpr int kLaunchRegs = (65536 / kThreads) & ~7;  // registers per thread at launch
+constexpr int kRegsCtl = (kEpiCols == 64) ? 40 : 56;  // warp group 0 after the split
+constexpr int kRegsEpi = (kEpiCols == 64) ? 104 : 216;
+constexpr int kPiece = (kEpiCols == 64) ? 16 : 64;    // accumulator columns per TMEM load
+constexpr int kMaxTokW = kEpiCols / 8;                // tokens in one group's columns (H >= 8)
+static_assert(128 * kRegsCtl + 32 * kNumEpiWarps * kRegsEpi <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 
 enum : unsigned { kFlagClean = 1u, kFlagCompressed = 2u };
 enum : int { kFirstOfBlock = 1, kLastOfBlock = 2 };
@@ -54,6 +65,12 @@ struct UnitInfo {
     int t;        // key tile: keys [t*128, t*128+128)
     int qbuf;     // which query-block buffer holds block b
     int flags;    // kFirstOfBlock | kLastOfBlock (within this CTA's slice)
+};
+
+// Output row of one query token: where its logits go and which keys are valid.
+struct __align__(16) TokRow {
+    long long off;   // offset of the row in the logits, or -1 when the row does not exist
+    int lo, hi;      // valid keys [lo, hi)
 };
 
 struct Params {
@@ -111,6 +128,7 @@ struct __align__(1024) Smem {
     int start_t;
     int n_units;
     long long scan[kThreads / 32];
+    TokRow tokrow[kNumEpiWarps][kMaxTokW];   // per epilogue warp: its tokens' rows
 };
 
 // ----------------------------------------------------------------- ranges
@@ -220,92 +238,93 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 
 // Back-off of waiters off the critical path (ns between polls).
 constexpr unsigned kProducerSleepNs = 256;
-constexpr unsigned kMmaSleepNs = 32;
+constexpr unsigned kMmaSleepNs = 0;
 
 // --------------------------------------------------------------- epilogue
-// Epilogue of one warp group: per work unit it copies its columns of the TMEM
-// accumulator (keys on lanes, (token, head) on columns) into registers with one
-// wait, hands the accumulator back to the MMA warp at once, then reduces
-// sum_h w[h] * max(x, 0) per token with packed FFMA2, scales by s[j] and writes
-// the row-masked logits.  Weights come from shared memory as broadcast 16-byte
-// loads.
+// Epilogue of one warp: per work unit it reads its 32 keys x 128 columns of
+// the TMEM accumulator (keys on lanes, (token, head) on columns) in two halves
+// of 64 columns, reduces sum_h w[h] * ReLU(s x) per token and writes the
+// row-masked logits.  The 128 head weights of its columns stay in registers
+// for the whole query block; the output row and key range of each of its
+// tokens sit in shared memory, written once per block.  The accumulator goes
+// back to the MMA warp as soon as the second half is in registers.
+//
+// Arithmetic per element: with s >= 0 for every key of the warp, ReLU(s x) =
+// s * max(x, 0), so the warp accumulates w * max(x, 0) with packed FFMA2 and
+// scales once per token.  A warp that holds a negative scale uses
+// ReLU(y) = (y + |y|) / 2 instead: it accumulates A = sum w x and
+// B = sum w |x| and forms (s A + |s| B) / 2, which equals sum w ReLU(s x) for
+// either sign of s.
 template <int H, int D>
 struct Epilogue {
-    static_assert(H >= 8 && H <= 64, "a warp group's columns must hold whole tokens");
+    static_assert(H >= 8 && H <= kEpiCols, "a warp's columns must hold whole tokens");
     using C = Cfg<D>;
     static constexpr int S = C::kStages;
-    // independent pair-accumulators per token: keeps every FFMA2 chain short
-    static constexpr int kNP2 = (H >= 32) ? 4 : 1;
+    static constexpr int kTokW = kEpiCols / H;   // tokens in a warp's columns
+    static_assert(kTokW <= kMaxTokW, "token rows do not fit the shared table");
 
     struct Unit {
-        int stage;
         int buf;
         UnitInfo info;
         float s;
-        bool negw;
     };
 
     Smem<D>& sm;
     const Params& p;
     const WaitCtx& wctx;
-    uint32_t tmem_base;
+    uint32_t tmem_lane;   // TMEM address of this warp's lanes and first column
     int n_units;
-    int quad;
-    int lane;
-    int tok0;
-    int ntok;
-    int k_block = -1;
+    int row;              // key row of this thread within the tile (TMEM lane)
+    int col0;             // first accumulator column of this warp
+    int tok0;             // first token of those columns within the query block
+    int ntok;             // tokens of the block that fall in those columns
+    int slot;             // this warp's index among the epilogue warps
+    float2 w2[kEpiCols / 2];
 
-    __device__ __forceinline__ int row() const { return quad * 32 + lane; }
-
-    // Waits until unit v's inputs and accumulator are ready; hands the key-tile
-    // stage back to the producer (its scale has been read).
-    __device__ __forceinline__ bool begin(int v, Unit& st)
+    __device__ __forceinline__ void enter_block(const UnitInfo& info)
     {
-        st.stage = v % S;
-        if (!warp_wait(smem_u32(&sm.full[st.stage]), (v / S) & 1, wctx))
-            return false;
-        st.info = sm.info[st.stage];
-        st.s = sm.scale[st.stage][row()];
-        if (st.info.flags & kFirstOfBlock) {
-            ++k_block;
-            if (!warp_wait(smem_u32(&sm.q_full[st.info.qbuf]), (k_block >> 1) & 1, wctx))
-                return false;
+        const float4* w4 = reinterpret_cast<const float4*>(&sm.w[info.qbuf][col0]);
+#pragma unroll
+        for (int i = 0; i < kEpiCols / 4; ++i) {
+            const float4 v = w4[i];
+            w2[2 * i] = make_float2(v.x, v.y);
+            w2[2 * i + 1] = make_float2(v.z, v.w);
+        }
+        const int a = threadIdx.x & 31;
+        __syncwarp();
+        if (a < kTokW) {
+            TokRow t;
+            const int r = info.b * p.tok + tok0 + a;
+            const int2 rg = sm.range[info.qbuf][tok0 + a];
+            t.off = (a < ntok && r < p.rows) ? (long long)r * p.ldo : -1ll;
+            t.lo = rg.x;
+            t.hi = rg.y;
+            sm.tokrow[slot][a] = t;
         }
         __syncwarp();
-        mbar_arrive_one_per_warp(smem_u32(&sm.empty[st.stage]));
+    }
+
+    // Waits for unit v's inputs and accumulator; hands the key-tile stage back
+    // to the producer (its scale and work record have been read).
+    __device__ __forceinline__ bool begin(int stage, uint32_t phase, int v, int& k_block, Unit& st)
+    {
+        if (!warp_wait_fast(smem_u32(&sm.full[stage]), phase, wctx))
+            return false;
+        st.info = sm.info[stage];
+        st.s = sm.scale[stage][row];
+        if (st.info.flags & kFirstOfBlock) {
+            ++k_block;
+            if (!warp_wait_fast(smem_u32(&sm.q_full[st.info.qbuf]), (k_block >> 1) & 1, wctx))
+                return false;
+            enter_block(st.info);
+        }
+        __syncwarp();
+        mbar_arrive_one_per_warp(smem_u32(&sm.empty[stage]));
         st.buf = v & 1;
-        if (!warp_wait(smem_u32(&sm.acc_full[st.buf]), (v >> 1) & 1, wctx))
+        if (!warp_wait_fast(smem_u32(&sm.acc_full[st.buf]), (v >> 1) & 1, wctx))
             return false;
         tc_fence_after();
-        st.negw = __any_sync(0xffffffffu, st.s < 0.f);
         return true;
-    }
-
-    __device__ __forceinline__ uint32_t taddr(const Unit& st) const
-    {
-        return tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(st.buf * kMaxN + tok0 * H);
-    }
-
-    template <int C>
-    static __device__ __forceinline__ float (&chunk(float (&x)[kEpiCols]))[32]
-    {
-        return *reinterpret_cast<float(*)[32]>(&x[32 * C]);
-    }
-
-    // All NCH 32-column chunks of this group's columns of the unit, then one
-    // wait: the accumulator can be handed back right after.
-    template <int NCH>
-    __device__ __forceinline__ void load_all(const Unit& st, float (&x)[kEpiCols])
-    {
-        static_assert(NCH >= 1 && NCH <= 2, "a warp group owns at most 64 columns");
-        const uint32_t a = taddr(st);
-        tmem_ld32_async(a, chunk<0>(x));
-        if constexpr (NCH > 1)
-            tmem_ld32_async(a + 32, chunk<1>(x));
-        tmem_wait32(chunk<0>(x));
-        if constexpr (NCH > 1)
-            tmem_wait32(chunk<1>(x));
     }
 
     __device__ __forceinline__ void release(const Unit& st)
@@ -323,103 +342,121 @@ struct Epilogue {
         }
     }
 
-    // Reduce the NCH*32 loaded columns per token and store the logits.
-    template <int NCH>
-    __device__ __forceinline__ void reduce_store(const Unit& st, const float (&x)[kEpiCols])
+    // Mask and store one logit of a token row.
+    __device__ __forceinline__ void store(const Unit& st, const TokRow& t, float v)
     {
-        constexpr int NC = NCH * 32;
-        constexpr int NT = (NC + H - 1) / H;   // tokens covered by the loaded columns
-        float2 acc2[NT][kNP2];
-#pragma unroll
-        for (int a = 0; a < NT; ++a)
-#pragma unroll
-            for (int c = 0; c < kNP2; ++c)
-                acc2[a][c] = make_float2(0.f, 0.f);
-        const float4* w4 = reinterpret_cast<const float4*>(&sm.w[st.info.qbuf][tok0 * H]);
-#pragma unroll
-        for (int c = 0; c < NC; c += 4) {
-            const float4 w = w4[c >> 2];
-            const float2 r0 = make_float2(fmaxf(x[c], 0.f), fmaxf(x[c + 1], 0.f));
-            const float2 r1 = make_float2(fmaxf(x[c + 2], 0.f), fmaxf(x[c + 3], 0.f));
-            float2& a0 = acc2[c / H][(c >> 1) % kNP2];
-            a0 = __ffma2_rn(make_float2(w.x, w.y), r0, a0);
-            float2& a1 = acc2[(c + 2) / H][((c + 2) >> 1) % kNP2];
-            a1 = __ffma2_rn(make_float2(w.z, w.w), r1, a1);
-        }
-        // ReLU(s x) = s * max(x, 0) for s >= 0 and s * (x - max(x, 0)) for s < 0;
-        // a warp that holds a negative scale also forms sum_h w * x, from a
-        // second pass over the TMEM columns (it kept the accumulator for this).
-        float accx[NT];
-#pragma unroll
-        for (int a = 0; a < NT; ++a)
-            accx[a] = 0.f;
-        if (st.negw) {
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-                float xc[32];
-                tmem_ld32(taddr(st) + 32 * ch, xc);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int c = 32 * ch + k;
-                    accx[c / H] = fmaf(sm.w[st.info.qbuf][tok0 * H + c], xc[k], accx[c / H]);
-                }
-            }
-            release(st);
-        }
-        const float ninf = __int_as_float(0xff800000u);
-        const bool clean = (p.flags & kFlagClean) != 0;
-        const bool compressed = (p.flags & kFlagCompressed) != 0;
         // key index; the host keeps widths below 2^31 - 256 so this fits an int
-        const int j = st.info.t * kBlockKV + row();
-        const int r0 = st.info.b * p.tok + tok0;
+        const int j = st.info.t * kBlockKV + row;
+        const bool valid = j >= t.lo && j < t.hi;
+        const bool compressed = (p.flags & kFlagCompressed) != 0;
+        // one predicated store: the logit, -inf (clean) or nothing
+        const int col = compressed ? j - t.lo : j;
+        const bool ok = compressed ? (valid && col < p.ldo)
+                                   : (j < p.width_i && (valid || (p.flags & kFlagClean) != 0));
+        if (t.off >= 0 && ok)
+            p.logits[t.off + col] = valid ? v : __int_as_float(0xff800000u);
+    }
+
+    // Columns [c0, c0 + P) of the warp's slice, already in x.
+    template <bool POS, int P>
+    __device__ __forceinline__ void piece_math(const Unit& st, int c0, const float (&x)[P],
+                                               float2& a0, float2& a1, float2& b0)
+    {
 #pragma unroll
-        for (int a = 0; a < NT; ++a) {
-            if (a < ntok && r0 + a < p.rows) {
-                float2 t2 = acc2[a][0];
-                if constexpr (kNP2 == 4) {
-                    t2 = __fadd2_rn(__fadd2_rn(acc2[a][0], acc2[a][1]),
-                                    __fadd2_rn(acc2[a][2], acc2[a][3]));
+        for (int k = 0; k < P; k += 4) {
+            const int c = c0 + k;
+            const float2 wa = w2[c >> 1], wb = w2[(c >> 1) + 1];
+            if constexpr (POS) {
+                a0 = __ffma2_rn(wa, make_float2(fmaxf(x[k], 0.f), fmaxf(x[k + 1], 0.f)), a0);
+                a1 = __ffma2_rn(wb, make_float2(fmaxf(x[k + 2], 0.f), fmaxf(x[k + 3], 0.f)), a1);
+            } else {
+                a0 = __ffma2_rn(wa, make_float2(x[k], x[k + 1]), a0);
+                b0 = __ffma2_rn(wa, make_float2(fabsf(x[k]), fabsf(x[k + 1])), b0);
+                a0 = __ffma2_rn(wb, make_float2(x[k + 2], x[k + 3]), a0);
+                b0 = __ffma2_rn(wb, make_float2(fabsf(x[k + 2]), fabsf(x[k + 3])), b0);
+            }
+            if ((c + 4) % H == 0) {   // last columns of token c / H
+                float v;
+                if constexpr (POS) {
+                    const float2 t = __fadd2_rn(a0, a1);
+                    v = st.s * (t.x + t.y);
+                } else {
+                    v = 0.5f * fmaf(st.s, a0.x + a0.y, fabsf(st.s) * (b0.x + b0.y));
                 }
-                const float sum = t2.x + t2.y;
-                const float v = (st.s >= 0.f) ? st.s * sum : st.s * (accx[a] - sum);
-                const int2 rg = sm.range[st.info.qbuf][tok0 + a];
-                const bool valid = j >= rg.x && j < rg.y;
-                // one predicated store: the logit, -inf (clean) or nothing
-                const int col = compressed ? j - rg.x : j;
-                const bool store = compressed ? (valid && col < p.ldo)
-                                              : (j < p.width_i && (valid || clean));
-                if (store)
-                    p.logits[(long long)(r0 + a) * p.ldo + col] = valid ? v : ninf;
+                store(st, sm.tokrow[slot][c / H], v);
+                a0 = a1 = b0 = make_float2(0.f, 0.f);
             }
         }
     }
 
-    // NCH = number of 32-column chunks this group owns (compile time).
-    template <int NCH>
+    template <int P>
+    __device__ __forceinline__ void load(uint32_t taddr, float (&x)[P])
+    {
+        if constexpr (P == 64)
+            tmem_ld64_wait(taddr, x);
+        else if constexpr (P == 32)
+            tmem_ld32_wait(taddr, x);
+        else
+            tmem_ld16_wait(taddr, x);
+    }
+
+    // One unit over the first NC columns of the warp's slice (the columns that
+    // hold tokens of the block, rounded up to a power of two >= 16), read in
+    // pieces of kPiece columns.  POS: every scale of the warp is >= 0.
+    template <bool POS, int NC>
+    __device__ __forceinline__ void reduce(const Unit& st)
+    {
+        constexpr int P = NC < kPiece ? NC : kPiece;
+        const uint32_t taddr = tmem_lane + (uint32_t)(st.buf * kMaxN);
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0;
+#pragma unroll
+        for (int pc = 0; pc < NC / P; ++pc) {
+            float x[P];
+            load<P>(taddr + P * pc, x);
+            if (pc == NC / P - 1)
+                release(st);   // every column is in registers: the MMA may reuse the buffer
+            piece_math<POS, P>(st, P * pc, x, a0, a1, b0);
+        }
+    }
+
+    template <int NC>
     __device__ __forceinline__ void run()
     {
-        float x[kEpiCols];
+        int stage = 0;
+        uint32_t phase = 0;
+        int k_block = -1;
         for (int u = 0; u < n_units; ++u) {
             Unit st;
-            if (!begin(u, st))
+            if (!begin(stage, phase, u, k_block, st))
                 return;
-            load_all<NCH>(st, x);
-            if (!st.negw)
-                release(st);
-            reduce_store<NCH>(st, x);   // releases the accumulator itself if negw
+            if (__all_sync(0xffffffffu, st.s >= 0.f))
+                reduce<true, NC>(st);
+            else
+                reduce<false, NC>(st);
             finish(st);
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
     }
 
-    // A group with no columns in the unit still takes part in every hand-off.
+    // A warp with no columns in the unit still takes part in every hand-off.
     __device__ __forceinline__ void run_empty()
     {
+        int stage = 0;
+        uint32_t phase = 0;
+        int k_block = -1;
         for (int u = 0; u < n_units; ++u) {
-            Unit cur;
-            if (!begin(u, cur))
+            Unit st;
+            if (!begin(stage, phase, u, k_block, st))
                 return;
-            release(cur);
-            finish(cur);
+            release(st);
+            finish(st);
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
     }
 };
@@ -438,9 +475,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // control warp group (producer, MMA, fill) gives registers to the four
     // epilogue warp groups, which hold a 64-column TMEM slice each;
     // 128 * ctl + 512 * epi <= 61440.
-    constexpr int kRegsCtl = 40;
-    constexpr int kRegsEpi = 104;
-    static_assert(128 * kRegsCtl + 512 * kRegsEpi <= kThreads * 96, "register split exceeds launch");
     static_assert(H >= 8 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two in [8,128]");
     static_assert(D == 64 || D == 128, "D must be 64 or 128");
 
@@ -711,6 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         regs_dec<kRegsCtl>();
         if (lane == 0) {
             const uint32_t idesc = idesc_e4m3_f32(kBlockKV, (uint32_t)N);
+            const uint64_t desc_kv0 = smem_desc(smem_u32(sm.kv[0]), D);
+            const uint64_t desc_q0 = smem_desc(smem_u32(sm.q[0]), D);
             int k_block = -1;
             for (int u = 0; u < n_units; ++u) {
                 const int stage = u % S;
@@ -728,12 +764,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kMaxN);
-                const uint32_t a0 = smem_u32(sm.kv[stage]);
-                const uint32_t b0 = smem_u32(sm.q[info.qbuf]);
+                // descriptors advance by address / 16: one stage, one query
+                // buffer, 32 bytes of K per MMA
+                const uint64_t da = desc_kv0 + (uint64_t)(stage * (C::kKVTileBytes >> 4));
+                const uint64_t db = desc_q0 + (uint64_t)(info.qbuf * (C::kQTileBytes >> 4));
 #pragma unroll
                 for (int k = 0; k < D / 32; ++k)
-                    mma_f8f6f4(d_tmem, smem_desc(a0 + 32 * k, D), smem_desc(b0 + 32 * k, D), idesc,
-                               k > 0 ? 1u : 0u);
+                    mma_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
                 mma_commit(smem_u32(&sm.empty[stage]));
                 mma_commit(smem_u32(&sm.acc_full[buf]));
                 if (info.flags & kLastOfBlock)
@@ -775,18 +812,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ================================================= epilogue
         regs_inc<kRegsEpi>();
-        // Warp group g owns accumulator columns [64 g, 64 g + 64): tokens
-        // [g * 64 / H, (g + 1) * 64 / H) of the unit's query block.
-        const int g = (warp - kEpiWarp0) >> 2;          // warp group 0..3
+        // Warp group g owns accumulator columns [kEpiCols g, kEpiCols (g + 1)):
+        // tokens [g kEpiCols / H, (g + 1) kEpiCols / H) of the unit's query block.
+        const int g = (warp - kEpiWarp0) >> 2;
+        const int quad = warp & 3;                      // TMEM lanes 32 quad .. 32 quad + 31
         const int tpg = kEpiCols / H;                   // tokens per group
         const int tok0 = g * tpg;
         const int ntok = max(0, min(tpg, p.tok - tok0));
-        const int nch = (ntok * H + 31) >> 5;           // 32-column chunks of this group
-        Epilogue<H, D> epi{sm, p, wctx, tmem_base, n_units, warp & 3, lane, tok0, ntok};
-        if (nch >= 2)
-            epi.template run<2>();
-        else if (nch == 1)
-            epi.template run<1>();
+        Epilogue<H, D> epi{sm, p, wctx,
+                           tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * kEpiCols),
+                           n_units, quad * 32 + lane, g * kEpiCols, tok0, ntok, warp - kEpiWarp0};
+        const int nc = ntok * H;   // columns holding tokens, rounded up below
+        if (nc > 64)
+            epi.template run<(kEpiCols > 64 ? 128 : 64)>();
+        else if (nc > 32)
+            epi.template run<64>();
+        else if (nc > 16)
+            epi.template run<32>();
+        else if (nc > 0)
+            epi.template run<16>();
         else
             epi.run_empty();
         tc_fence_before();
