@@ -52,7 +52,7 @@ constexpr int kThreads = 32 * (kEpiWarp0 + kNumEpiWarps);
 constexpr int kLaunchRegs = (65536 / kThreads) & ~7;  // registers per thread at launch
 constexpr int kRegsCtl = (kEpiCols == 64) ? 40 : 56;  // warp group 0 after the split
 constexpr int kRegsEpi = (kEpiCols == 64) ? 104 : 216;
-constexpr int kPiece = (kEpiCols == 64) ? 16 : 64;    // accumulator columns per TMEM load
+constexpr int kPiece = (kEpiCols == 64) ? 16 : 32;    // accumulator columns per TMEM load
 constexpr int kMaxTokW = kEpiCols / 8;                // tokens in one group's columns (H >= 8)
 static_assert(128 * kRegsCtl + 32 * kNumEpiWarps * kRegsEpi <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
@@ -389,15 +389,14 @@ struct Epilogue {
         }
     }
 
+    // Load and wait as two statements: the compiler may schedule the previous
+    // piece's arithmetic between them, which hides the TMEM latency.
     template <int P>
     __device__ __forceinline__ void load(uint32_t taddr, float (&x)[P])
     {
-        if constexpr (P == 64)
-            tmem_ld64_wait(taddr, x);
-        else if constexpr (P == 32)
-            tmem_ld32_wait(taddr, x);
-        else
-            tmem_ld16_wait(taddr, x);
+        static_assert(P == 16 || P == 32, "TMEM pieces are 16 or 32 columns");
+        tmem_ld_async<P>(taddr, x);
+        tmem_wait<P>(x);
     }
 
     // One unit over the first NC columns of the warp's slice (the columns that
