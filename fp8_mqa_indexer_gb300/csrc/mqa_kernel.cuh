@@ -17,16 +17,17 @@
 //    accumulates x[key, (token, head)] in TMEM.
 //  * Epilogue threads each own one key (one TMEM lane) and reduce over heads in
 //    registers: acc = sum_h w[h] * max(x, 0), then multiply by s[j] once (exact
-//    rewrite of ReLU(s x) for s >= 0; warps that see a negative scale take a
-//    second path that keeps the literal ReLU(s x)).  For a fixed token the 128
+//    rewrite of ReLU(s x) for s >= 0; a warp that sees a negative scale sums
+//    w x and w |x| instead, since ReLU(y) = (y + |y|) / 2).  The head weights
+//    stay in registers for a whole query block.  For a fixed token the 128
 //    threads of a warp group write 128 consecutive floats: coalesced rows.
 //  * One persistent CTA per SM walks a contiguous slice of the (query block,
 //    key tile) work list: dense slices come from an in-kernel prefix sum over
 //    the query blocks; paged slices come from the schedule written by
 //    paged_mqa_logits_metadata.
-//  * Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+//  * Warp roles (640 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 //    owner, warps 2-3 write -inf into the columns no tile covers (clean mode),
-//    warps 4-11 are two epilogue warp groups splitting the N columns.
+//    warps 4-19 are four epilogue warp groups of 64 columns each.
 //  * Pipelines: a ring of key tiles (+ their scales and a small work record),
 //    two query-block buffers (+ weights and per-token ranges) and two TMEM
 //    accumulators of 256 columns; every hand-off is an mbarrier, every wait is
