@@ -69,9 +69,15 @@ struct UnitInfo {
 };
 
 // Output row of one query token: where its logits go and which keys are valid.
+// The logits of keys j in [slo, shi) go to logits[off + j]; keys in
+// [vlo, vhi) get their value, the rest of that window -inf (clean mode).  In
+// compressed mode off is shifted by the row's first key; a row that does not
+// exist has an empty window.
 struct __align__(16) TokRow {
-    long long off;   // offset of the row in the logits, or -1 when the row does not exist
-    int lo, hi;      // valid keys [lo, hi)
+    int slo, shi;    // keys stored
+    int vlo, vhi;    // keys with a value
+    long long off;   // offset of key 0 of the row in the logits
+    long long pad;
 };
 
 struct Params {
@@ -296,10 +302,23 @@ struct Epilogue {
         if (a < kTokW) {
             TokRow t;
             const int r = info.b * p.tok + tok0 + a;
-            const int2 rg = sm.range[info.qbuf][tok0 + a];
-            t.off = (a < ntok && r < p.rows) ? (long long)r * p.ldo : -1ll;
-            t.lo = rg.x;
-            t.hi = rg.y;
+            const int2 rg = sm.range[info.qbuf][tok0 + a];   // within [0, width)
+            t.slo = t.shi = t.vlo = t.vhi = 0;
+            t.off = 0;
+            t.pad = 0;
+            if (a < ntok && r < p.rows) {
+                t.off = (long long)r * p.ldo;
+                t.slo = t.vlo = rg.x;
+                t.shi = t.vhi = rg.y;
+                if (p.flags & kFlagCompressed) {   // column j - lo, below ldo
+                    t.off -= rg.x;
+                    if ((long long)rg.x + p.ldo < rg.y)
+                        t.shi = t.vhi = (int)(rg.x + p.ldo);
+                } else if (p.flags & kFlagClean) {   // -inf outside the range
+                    t.slo = 0;
+                    t.shi = p.width_i;
+                }
+            }
             sm.tokrow[slot][a] = t;
         }
         __syncwarp();
@@ -348,14 +367,9 @@ struct Epilogue {
     {
         // key index; the host keeps widths below 2^31 - 256 so this fits an int
         const int j = st.info.t * kBlockKV + row;
-        const bool valid = j >= t.lo && j < t.hi;
-        const bool compressed = (p.flags & kFlagCompressed) != 0;
         // one predicated store: the logit, -inf (clean) or nothing
-        const int col = compressed ? j - t.lo : j;
-        const bool ok = compressed ? (valid && col < p.ldo)
-                                   : (j < p.width_i && (valid || (p.flags & kFlagClean) != 0));
-        if (t.off >= 0 && ok)
-            p.logits[t.off + col] = valid ? v : __int_as_float(0xff800000u);
+        if (j >= t.slo && j < t.shi)
+            p.logits[t.off + j] = (j >= t.vlo && j < t.vhi) ? v : __int_as_float(0xff800000u);
     }
 
     // Columns [c0, c0 + P) of the warp's slice, already in x.
