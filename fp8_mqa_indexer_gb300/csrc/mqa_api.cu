@@ -474,6 +474,7 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
     p.flags = (clean ? kFlagClean : 0u) | (compressed ? kFlagCompressed : 0u);
     p.S_q = S_q;
     p.S_kv = S_kv;
+    p.kv_scale = kv_scale;
     p.k_start = k_start;
     p.k_end = k_end;
     p.width = S_kv;

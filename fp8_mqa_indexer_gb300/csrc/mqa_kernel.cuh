@@ -89,6 +89,7 @@ struct Params {
     int S_kv;
     const int* k_start;
     const int* k_end;
+    const float* kv_scale;   // dense: scanned once for negative scales
     // paged
     const int* context_lens;
     const int* block_table;
@@ -433,7 +434,8 @@ struct Epilogue {
         }
     }
 
-    template <int NC>
+    // MIXED: some key scale may be negative, so each unit votes on its signs.
+    template <int NC, bool MIXED>
     __device__ __forceinline__ void run()
     {
         int stage = 0;
@@ -443,7 +445,7 @@ struct Epilogue {
             Unit st;
             if (!begin(stage, phase, u, k_block, st))
                 return;
-            if (__all_sync(0xffffffffu, st.s >= 0.f))
+            if (!MIXED || __all_sync(0xffffffffu, st.s >= 0.f))
                 reduce<true, NC>(st);
             else
                 reduce<false, NC>(st);
@@ -611,7 +613,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm.start_t = t0;
         }
     }
-    __syncthreads();
+    // Any negative key scale?  Without one (the usual case: scales are
+    // quantisation factors) the epilogue runs the ReLU-by-FMNMX form only and
+    // skips the per-unit sign vote.  The paged pool is not scanned.
+    int any_neg = PAGED ? 1 : 0;
+    if (!PAGED) {
+        const int n4 = p.S_kv >> 2;
+        const float4* s4 = reinterpret_cast<const float4*>(p.kv_scale);
+        for (int k = tid; k < n4; k += kThreads) {
+            const float4 v = __ldg(s4 + k);
+            any_neg |= (v.x < 0.f) | (v.y < 0.f) | (v.z < 0.f) | (v.w < 0.f);
+        }
+        for (int k = (n4 << 2) + tid; k < p.S_kv; k += kThreads)
+            any_neg |= __ldg(p.kv_scale + k) < 0.f;
+    }
+    any_neg = __syncthreads_or(any_neg);
     tc_fence_after();
 
     const uint32_t tmem_base = sm.tmem_base;
@@ -837,16 +853,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * kEpiCols),
                            n_units, quad * 32 + lane, g * kEpiCols, tok0, ntok, warp - kEpiWarp0};
         const int nc = ntok * H;   // columns holding tokens, rounded up below
-        if (nc > 64)
-            epi.template run<(kEpiCols > 64 ? 128 : 64)>();
-        else if (nc > 32)
-            epi.template run<64>();
-        else if (nc > 16)
-            epi.template run<32>();
-        else if (nc > 0)
-            epi.template run<16>();
-        else
+        if (nc > 32) {
+            if (any_neg)
+                epi.template run<kEpiCols, true>();
+            else
+                epi.template run<kEpiCols, false>();
+        } else if (nc > 16) {
+            epi.template run<32, true>();
+        } else if (nc > 0) {
+            epi.template run<16, true>();
+        } else {
             epi.run_empty();
+        }
         tc_fence_before();
     }
 
