@@ -51,8 +51,8 @@ constexpr int kNumEpiWarps = 4 * (kMaxN / kEpiCols);
 constexpr int kEpiWarp0 = 4;                          // epilogue warps follow warp group 0
 constexpr int kThreads = 32 * (kEpiWarp0 + kNumEpiWarps);
 constexpr int kLaunchRegs = (65536 / kThreads) & ~7;  // registers per thread at launch
-constexpr int kRegsCtl = (kEpiCols == 64) ? 40 : 56;  // warp group 0 after the split
-constexpr int kRegsEpi = (kEpiCols == 64) ? 104 : 216;
+constexpr int kRegsCtl = (kEpiCols == 64) ? 32 : 56;  // warp group 0 after the split
+constexpr int kRegsEpi = (kEpiCols == 64) ? 112 : 216;
 constexpr int kPiece = (kEpiCols == 64) ? 16 : 32;    // accumulator columns per TMEM load
 constexpr int kMaxTokW = kEpiCols / 8;                // tokens in one group's columns (H >= 8)
 static_assert(128 * kRegsCtl + 32 * kNumEpiWarps * kRegsEpi <= kThreads * kLaunchRegs,
