@@ -130,7 +130,144 @@ def dist_env():
 
 def make_case(workload: str):
     from fp8_mqa_indexer_gb300 import workloads as wl
+    if workload in wl.PAGED_CONFIGS:
+        return wl.paged_config(workload)
     return wl.dense_config(workload)
+
+
+def is_paged(workload: str) -> bool:
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    return workload in wl.PAGED_CONFIGS
+
+
+def paged_oracle_sample(case, budget_s: float):
+    """Time the oracle on whole sequences (both of their rows) for ~budget_s."""
+    import oracle
+    oracle.build()
+    cores = max(1, len(os.sched_getaffinity(0)))
+    counts = case.valid_counts()
+    rows, flops = 0, 0.0
+    t0 = time.perf_counter()
+    b = 0
+    while b < case.B:
+        batch = list(range(b, min(case.B, b + cores)))
+        b += len(batch)
+
+        def one(seq):
+            r0 = seq * case.next_n
+            return oracle.paged_mqa_logits(case.q, case.kv_cache, case.kv_scales, case.weights,
+                                           case.context_lens, case.block_table,
+                                           next_n=case.next_n, ldo=case.ldo, clean=case.clean,
+                                           rows=(r0, r0 + case.next_n))
+        oracle.run_rows_parallel(one, batch, threads=cores)
+        rows += len(batch) * case.next_n
+        flops += float(sum(int(counts[r]) for s_ in batch
+                           for r in range(s_ * case.next_n, (s_ + 1) * case.next_n))) * 2 * case.H * case.D
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    wall = time.perf_counter() - t0
+    return {"tflops": flops / wall / 1e12, "cores": cores, "rows": rows, "wall_s": wall}
+
+
+def bench_paged(args, mqa, torch, dev, stream):
+    """Paged decode: schedule + logits per step; an HBM-bound path."""
+    case = make_case(args.workload)
+    valid = int(case.valid_counts().sum())
+    flops = valid * 2.0 * case.H * case.D
+    R = case.B * case.next_n
+    ctx = case.context_lens.to(torch.int64)
+    pages = ((ctx.clamp(min=0) + case.block_kv - 1) // case.block_kv)
+    # algorithmic bytes: every key of every context (E4M3 row + fp32 scale) once,
+    # the query rows, weights, block-table entries in use, and the whole output
+    alg_bytes = (int(ctx.clamp(min=0).sum()) * (case.D + 4) + case.q.numel() + case.weights.numel() * 4
+                 + int(pages.sum()) * 4 + case.B * 4 + R * case.ldo * 4)
+    q, kvc = case.q.to(dev), case.kv_cache.to(dev)
+    sc, w = case.kv_scales.to(dev), case.weights.to(dev)
+    cl, bt = case.context_lens.to(dev), case.block_table.to(dev)
+    out = torch.empty((R, case.ldo), dtype=torch.float32, device=dev)
+    meta = torch.empty((mqa.get_num_sms(dev) + 1, 2), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(q_, kvc_, sc_, w_, cl_, bt_):
+        mqa.paged_mqa_logits_metadata(cl_, next_n=case.next_n, block_kv=case.block_kv, out=meta)
+        mqa.paged_mqa_logits(q_, kvc_, sc_, w_, cl_, bt_, meta, out, next_n=case.next_n,
+                             clean=case.clean)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step(q, kvc, sc, w, cl, bt)
+    torch.cuda.synchronize()
+    assert mqa.device_status() == 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[0].strip() if vis else "0")
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step(q, kvc, sc, w, cl, bt)
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    assert mqa.device_status() == 0
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_per_step = sum(times_ms) / args.steps
+
+    host = {k: v.pin_memory() for k, v in dict(q=case.q, kvc=case.kv_cache, sc=case.kv_scales,
+                                                w=case.weights, cl=case.context_lens,
+                                                bt=case.block_table).items()}
+    host_out = torch.empty((R, case.ldo), dtype=torch.float32, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+
+    def e2e_step():
+        d = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+        step(d["q"], d["kvc"], d["sc"], d["w"], d["cl"], d["bt"])
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+
+    peaks, peaks_src = load_peaks()
+    achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": "MQA logits TFLOP/s (valid logits x 2*H*D)",
+        "value": flops / (ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": case.B, "next_n": case.next_n, "H": case.H,
+                   "D": case.D, "block_kv": case.block_kv, "num_blocks": case.num_blocks,
+                   "ldo": case.ldo, "valid_logits": valid, "clean": case.clean,
+                   "l2": "flushed (256 MiB write) before every timed step; the pool exceeds L2",
+                   "step": "paged_mqa_logits_metadata + paged_mqa_logits"},
+        "median_ms": statistics.median(times_ms),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes": alg_bytes, "peak_source": f"{peaks_src} HBM copy"},
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": host_out.numel() * 4,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        info = paged_oracle_sample(case, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": info["tflops"], "unit": "TFLOP/s", "cores": info["cores"],
+                                "kind": "oracle",
+                                "sample": f"{info['rows']} of {R} rows ({info['wall_s']:.1f} s of "
+                                          f"oracle time), throughput extrapolated"}
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def oracle_sample(case, budget_s: float, max_rows: int = 4096):
@@ -170,11 +307,15 @@ def run_reference(args, rank, world):
     flops_full = valid * 2.0 * case.H * case.D
     per_step = []
     info = None
+    paged = is_paged(args.workload)
     for _ in range(args.warmup):
-        oracle_sample(case, budget_s=0.5, max_rows=8)
+        if paged:
+            paged_oracle_sample(case, budget_s=0.5)
+        else:
+            oracle_sample(case, budget_s=0.5, max_rows=8)
     budget = args.ref_budget or max(1.0, min(6.0, 90.0 / max(1, args.steps)))
     for _ in range(args.steps):
-        info = oracle_sample(case, budget_s=budget)
+        info = paged_oracle_sample(case, budget_s=budget) if paged else oracle_sample(case, budget_s=budget)
         per_step.append(info["tflops"])
     value = statistics.median(per_step)
     ms_per_step = flops_full / (value * 1e12) * 1e3
@@ -184,10 +325,12 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (exact e4m3 decode)",
         "data": "synthetic",
-        "config": {"workload": args.workload, "S_q": case.S_q, "S_kv": case.S_kv, "H": case.H,
-                   "D": case.D, "valid_logits": valid, "clean": case.clean},
+        "config": ({"workload": args.workload, "B": case.B, "next_n": case.next_n, "H": case.H,
+                    "D": case.D, "valid_logits": valid, "clean": case.clean} if paged else
+                   {"workload": args.workload, "S_q": case.S_q, "S_kv": case.S_kv, "H": case.H,
+                    "D": case.D, "valid_logits": valid, "clean": case.clean}),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
-                         "sample": f"{info['rows']} of {case.S_q} rows per step, "
+                         "sample": f"{info['rows']} of {case.B * case.next_n if paged else case.S_q} rows per step, "
                                    f"extrapolated to the full workload ({info['wall_s']:.1f} s)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -230,6 +373,10 @@ def main():
     if pg:
         pg.barrier()
     mqa.load_library()
+    if is_paged(args.workload):
+        if world > 1:
+            raise SystemExit("the paged workload is measured on one GPU")
+        return bench_paged(args, mqa, torch, dev, torch.cuda.current_stream())
 
     case = make_case(args.workload)
     valid = int(case.valid_counts().sum())
