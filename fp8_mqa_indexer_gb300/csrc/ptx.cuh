@@ -113,15 +113,46 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     }
 }
 
-// The same wait taken by a whole warp, shaped for the hot path: one try_wait
-// and a vote when the phase is already complete, the polling loop (with its
-// abort and clock checks) only when it is not.  Every lane gets the same
-// answer.
+// The same wait taken by a whole warp, shaped for the hot path: the whole
+// loop is one PTX block whose branches are uniform (each try_wait answer is
+// voted across the warp), so the compiler adds no convergence bookkeeping
+// around it, and no shared load sits in the polling loop.  Polling stops when
+// the phase completes or the cycle budget is spent; a timeout records
+// kDevErrTimeout, raises the CTA's abort flag (which stops the waits of the
+// other roles) and returns false.  Every lane gets the same answer.
 __device__ __forceinline__ bool warp_wait_fast(uint32_t bar, uint32_t parity, const WaitCtx& w)
 {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+    uint32_t ok;
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        ".reg .u64 t0, t1;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "vote.sync.all.pred p, p, 0xffffffff;\n\t"
+        "@p bra.uni W_DONE;\n\t"
+        "mov.u64 t0, %%clock64;\n\t"
+        "W_LOOP:\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "vote.sync.all.pred p, p, 0xffffffff;\n\t"
+        "@p bra.uni W_DONE;\n\t"
+        "mov.u64 t1, %%clock64;\n\t"
+        "sub.s64 t1, t1, t0;\n\t"
+        "setp.lt.s64 p, t1, %3;\n\t"
+        "@p bra.uni W_LOOP;\n\t"
+        "mov.u32 %0, 0;\n\t"
+        "bra.uni W_END;\n\t"
+        "W_DONE:\n\t"
+        "mov.u32 %0, 1;\n\t"
+        "W_END:\n\t"
+        "}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "l"(w.limit)
+        : "memory");
+    if (ok)
         return true;
-    return __all_sync(0xffffffffu, wait_bounded(bar, parity, w));
+    *w.abort_flag = 1;
+    atomicOr(w.status, kDevErrTimeout);
+    return false;
 }
 
 // ---------------------------------------------------------------------- TMA
