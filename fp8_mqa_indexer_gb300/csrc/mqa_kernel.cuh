@@ -441,10 +441,14 @@ struct Epilogue {
         int stage = 0;
         uint32_t phase = 0;
         int k_block = -1;
-        for (int u = 0; u < n_units; ++u) {
+        // Eight units per trip: the accumulator buffer of each (and, with eight
+        // key-tile stages, the stage too) is then known at compile time, the
+        // loop's bookkeeping is shared, and the compiler can schedule one
+        // unit's tail against the next unit's hand-offs.
+        auto one = [&](int u) -> bool {
             Unit st;
             if (!begin(stage, phase, u, k_block, st))
-                return;
+                return false;
             if (!MIXED || __all_sync(0xffffffffu, st.s >= 0.f))
                 reduce<true, NC>(st);
             else
@@ -454,7 +458,17 @@ struct Epilogue {
                 stage = 0;
                 phase ^= 1u;
             }
+            return true;
+        };
+        int u = 0;
+        for (; u + 7 < n_units; u += 8) {
+            if (!one(u) || !one(u + 1) || !one(u + 2) || !one(u + 3) || !one(u + 4) ||
+                !one(u + 5) || !one(u + 6) || !one(u + 7))
+                return;
         }
+        for (; u < n_units; ++u)
+            if (!one(u))
+                return;
     }
 
     // A warp with no columns in the unit still takes part in every hand-off.
