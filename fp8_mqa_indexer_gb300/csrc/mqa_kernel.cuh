@@ -417,20 +417,29 @@ struct Epilogue {
 
     // One unit over the first NC columns of the warp's slice (the columns that
     // hold tokens of the block, rounded up to a power of two >= 16), read in
-    // pieces of kPiece columns.  POS: every scale of the warp is >= 0.
+    // pieces of kPiece columns, double-buffered: the next piece is in flight
+    // while the current one is reduced.  POS: every scale of the warp is >= 0.
     template <bool POS, int NC>
     __device__ __forceinline__ void reduce(const Unit& st)
     {
         constexpr int P = NC < kPiece ? NC : kPiece;
         const uint32_t taddr = tmem_lane + (uint32_t)(st.buf * kMaxN);
         float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0;
+        constexpr int NP = NC / P;
+        float xa[P], xb[P];
+        tmem_ld_async<P>(taddr, xa);
+        tmem_wait<P>(xa);
 #pragma unroll
-        for (int pc = 0; pc < NC / P; ++pc) {
-            float x[P];
-            load<P>(taddr + P * pc, x);
-            if (pc == NC / P - 1)
-                release(st);   // every column is in registers: the MMA may reuse the buffer
-            piece_math<POS, P>(st, P * pc, x, a0, a1, b0);
+        for (int pc = 0; pc < NP; ++pc) {
+            float(&cur)[P] = (pc & 1) ? xb : xa;
+            float(&nxt)[P] = (pc & 1) ? xa : xb;
+            if (pc + 1 < NP)
+                tmem_ld_async<P>(taddr + P * (pc + 1), nxt);
+            else
+                release(st);
+            piece_math<POS, P>(st, P * pc, cur, a0, a1, b0);
+            if (pc + 1 < NP)
+                tmem_wait<P>(nxt);
         }
     }
 
