@@ -57,8 +57,9 @@ def _load():
             lib.oracle_paged_mqa_logits.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                                     i32, i64, u32, i32, i32, P, P]
             lib.oracle_paged_mqa_logits_metadata.argtypes = [P, i32, i32, i32, i32, P]
+            lib.oracle_topk_indices.argtypes = [P, i64, P, P, i32, i32, u32, i32, i32, i32, P]
             for f in (lib.oracle_e4m3_table, lib.oracle_mqa_logits, lib.oracle_paged_mqa_logits,
-                      lib.oracle_paged_mqa_logits_metadata):
+                      lib.oracle_paged_mqa_logits_metadata, lib.oracle_topk_indices):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -162,6 +163,45 @@ def paged_mqa_logits_metadata(context_lens, *, next_n: int, block_kv: int, num_s
     if rc != 0:
         raise ValueError("oracle_paged_mqa_logits_metadata: invalid arguments")
     return meta
+
+
+def topk_indices(logits, k_start, k_end, *, topk: int, n_cols: Optional[int] = None,
+                 compressed: bool = False, rows: Optional[tuple] = None) -> np.ndarray:
+    """Top-k keys of rows [r0, r1) of a logits matrix ``[rows, ldo]`` (float32):
+    ``[r1 - r0, topk]`` int32, ascending keys then -1; see ``mqa_oracle.c``.
+
+    ``n_cols`` is the number of keys of an uncompressed row (default ``ldo``).
+    """
+    L = _np(logits, np.float32)
+    R, ldo = L.shape
+    ks, ke = _np(k_start, np.int32), _np(k_end, np.int32)
+    assert ks.shape == (R,) and ke.shape == (R,)
+    if n_cols is None:
+        n_cols = ldo
+    r0, r1 = rows if rows is not None else (0, R)
+    out = np.empty((r1 - r0, topk), np.int32)
+    rc = _load().oracle_topk_indices(_ptr(L), ldo, _ptr(ks), _ptr(ke), R, n_cols,
+                                     COMPRESSED if compressed else 0, topk, r0, r1, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_topk_indices: invalid arguments")
+    return out
+
+
+def paged_ranges(context_lens, next_n: int) -> tuple:
+    """Key ranges of the paged decode rows r = b * next_n + t: ``[0, ctx_b -
+    next_n + t + 1)`` (empty when negative), as int32 (start, end) arrays."""
+    cl = _np(context_lens, np.int64)
+    t = np.tile(np.arange(next_n, dtype=np.int64), cl.shape[0])
+    end = np.maximum(np.repeat(cl, next_n) - next_n + t + 1, 0)
+    return np.zeros(end.shape, np.int32), end.astype(np.int32)
+
+
+def paged_topk_indices(logits, context_lens, *, next_n: int, topk: int,
+                       width: Optional[int] = None, rows: Optional[tuple] = None) -> np.ndarray:
+    """Top-k keys of paged decode logits ``[B * next_n, ldo]``; a row has
+    ``width`` keys (default ``ldo``)."""
+    ks, ke = paged_ranges(context_lens, next_n)
+    return topk_indices(logits, ks, ke, topk=topk, n_cols=width, rows=rows)
 
 
 def _split(rows: Sequence[int], n: int) -> Iterable[list]:

@@ -317,3 +317,103 @@ int oracle_paged_mqa_logits_metadata(const int32_t *context_lens, int B, int nex
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Top-k key selection per query row: the step that consumes the logits.  The
+ * "FlashMLA" page (parameters of flash_mla_with_kvcache) fixes only its
+ * output contract: `indices` of shape (batch, seq_len_q, topk) naming the keys
+ * each query attends to, with invalid entries set to -1.  Readings this
+ * oracle takes, since the pages leave the rest open:
+ *   - the candidates of row i are the keys of its range [lo, hi), normalised as
+ *     for the logits (intersected with [0, n_cols); in the compressed layout key
+ *     j sits at column j - lo and the range stops at lo + ldo);
+ *   - "top" means the largest logits under the IEEE-754 totalOrder of the fp32
+ *     value (-NaN < -inf < ... < -0 < +0 < ... < +inf < +NaN), and among equal
+ *     values (the same bit pattern) the smaller key index comes first;
+ *   - the first min(topk, hi - lo) keys of that order are written in
+ *     ascending key order, followed by -1 up to topk.
+ * ------------------------------------------------------------------------- */
+
+/* Rank of an fp32 bit pattern in totalOrder: non-negative values by their
+ * magnitude bits, negative values below every non-negative one and reversed. */
+static int64_t total_order_rank(float v)
+{
+    union {
+        float f;
+        uint32_t u;
+    } b;
+    b.f = v;
+    int64_t mag = (int64_t)(b.u & 0x7fffffffu);
+    return (b.u >> 31) ? -mag - 1 : mag;
+}
+
+typedef struct {
+    int64_t rank;
+    int32_t key;
+} ranked_key;
+
+/* Larger rank first; equal ranks by smaller key. */
+static int by_rank_then_key(const void *pa, const void *pb)
+{
+    const ranked_key *a = pa, *b = pb;
+    if (a->rank != b->rank)
+        return a->rank > b->rank ? -1 : 1;
+    return (a->key > b->key) - (a->key < b->key);
+}
+
+/*
+ * Top-k keys of rows [row_begin, row_end).
+ *   logits  [rows, ldo] fp32 (row i starts at logits + i * ldo)
+ *   k_start, k_end [rows] int32 key ranges; n_cols = keys per uncompressed row
+ *   flags   ORACLE_COMPRESSED: key j of row i is at column j - lo, and the
+ *           range is cut at lo + ldo
+ *   out     points at row row_begin of an [.., topk] int32 matrix
+ * Returns 0, or -1 on invalid arguments.
+ */
+int oracle_topk_indices(const float *logits, int64_t ldo, const int32_t *k_start,
+                        const int32_t *k_end, int rows, int n_cols, unsigned flags, int topk,
+                        int row_begin, int row_end, int32_t *out)
+{
+    int compressed = (flags & ORACLE_COMPRESSED) != 0;
+    if (rows < 0 || n_cols < 0 || topk <= 0 || ldo < 0 || row_begin < 0 || row_end > rows ||
+        row_begin > row_end || (!compressed && ldo < n_cols))
+        return -1;
+    ranked_key *cand = malloc(sizeof(ranked_key) * (size_t)(n_cols > 0 ? n_cols : 1));
+    unsigned char *chosen = malloc((size_t)(n_cols > 0 ? n_cols : 1));
+    if (!cand || !chosen) {
+        free(cand);
+        free(chosen);
+        return -2;
+    }
+    for (int i = row_begin; i < row_end; ++i) {
+        int lo = k_start[i] < 0 ? 0 : (k_start[i] > n_cols ? n_cols : k_start[i]);
+        int hi = k_end[i] > n_cols ? n_cols : k_end[i];
+        if (hi < lo)
+            hi = lo;
+        if (compressed && (int64_t)(hi - lo) > ldo)
+            hi = (int)(lo + ldo);
+        const float *row = logits + (size_t)i * (size_t)ldo;
+        int n = hi - lo;
+        for (int c = 0; c < n; ++c) {
+            int j = lo + c;
+            cand[c].rank = total_order_rank(row[compressed ? c : j]);
+            cand[c].key = j;
+        }
+        qsort(cand, (size_t)n, sizeof(ranked_key), by_rank_then_key);
+        int take = n < topk ? n : topk;
+        for (int c = 0; c < n; ++c)
+            chosen[c] = 0;
+        for (int c = 0; c < take; ++c)
+            chosen[cand[c].key - lo] = 1;
+        int32_t *o = out + (size_t)(i - row_begin) * (size_t)topk;
+        int pos = 0;
+        for (int c = 0; c < n; ++c)
+            if (chosen[c])
+                o[pos++] = lo + c;
+        while (pos < topk)
+            o[pos++] = -1;
+    }
+    free(cand);
+    free(chosen);
+    return 0;
+}
