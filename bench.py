@@ -11,6 +11,9 @@ synchronize around the timed loop, the max over ranks.  Prints one JSON line.
 
 --impl reference times the CPU oracle (the plain double-precision reference in
 oracle/) on a bounded row sample of the same workload on this host's cores.
+Other workloads: the 2048 x 4096 and 8192 x 65536 dense calls, the paged decode
+call, and the top-k key selection over 2048 x 32768 logits rows
+(topk_2k_32k_k2048, reported in rows/s against the HBM roofline).
 Under torchrun each rank runs the whole workload on its own GPU (the rows are
 independent; no collective is on the data path) and rank 0 reports the
 aggregate.
@@ -130,6 +133,8 @@ def dist_env():
 
 def make_case(workload: str):
     from fp8_mqa_indexer_gb300 import workloads as wl
+    if workload in wl.TOPK_CONFIGS:
+        return wl.topk_config(workload)
     if workload in wl.PAGED_CONFIGS:
         return wl.paged_config(workload)
     return wl.dense_config(workload)
@@ -138,6 +143,122 @@ def make_case(workload: str):
 def is_paged(workload: str) -> bool:
     from fp8_mqa_indexer_gb300 import workloads as wl
     return workload in wl.PAGED_CONFIGS
+
+
+def is_topk(workload: str) -> bool:
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    return workload in wl.TOPK_CONFIGS
+
+
+def topk_oracle_sample(case, budget_s: float):
+    """Time the oracle's top-k on evenly spread rows until ~budget_s of wall time."""
+    import oracle
+    import numpy as np
+    oracle.build()
+    cores = max(1, len(os.sched_getaffinity(0)))
+    L = case.logits.numpy()
+    ks, ke = case.k_start.numpy(), case.k_end.numpy()
+    order = list(range(0, case.rows, max(1, case.rows // 256)))
+    order += [r for r in range(case.rows) if r not in set(order)]
+    done, t0, k = 0, time.perf_counter(), 0
+    while k < len(order):
+        batch = order[k:k + cores]
+        k += len(batch)
+        oracle.run_rows_parallel(
+            lambda r: oracle.topk_indices(L, ks, ke, topk=case.topk, n_cols=case.n_cols,
+                                          rows=(r, r + 1)), batch, threads=cores)
+        done += len(batch)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    wall = time.perf_counter() - t0
+    return {"rows_per_s": done / wall, "cores": cores, "rows": done, "wall_s": wall}
+
+
+def bench_topk(args, mqa, torch, dev, stream):
+    """Top-k key selection over a logits matrix; an HBM-bound path."""
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    case = wl.topk_config(args.workload)
+    R = case.rows
+    valid = int(case.valid_counts().sum())
+    # algorithmic bytes: every in-range logit read once, the index matrix and the ranges
+    alg_bytes = valid * 4 + R * case.topk * 4 + R * 8
+    L = case.logits.to(dev)
+    ks, ke = case.k_start.to(dev), case.k_end.to(dev)
+    out = torch.empty((R, case.topk), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(L_, ks_, ke_):
+        mqa.mqa_topk_indices(L_, ks_, ke_, case.topk, out, S_kv=case.n_cols)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step(L, ks, ke)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[0].strip() if vis else "0")
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step(L, ks, ke)
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_per_step = sum(times_ms) / args.steps
+
+    host = {k: v.pin_memory() for k, v in dict(L=case.logits, ks=case.k_start, ke=case.k_end).items()}
+    host_out = torch.empty((R, case.topk), dtype=torch.int32, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+
+    def e2e_step():
+        d = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+        step(d["L"], d["ks"], d["ke"])
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+
+    peaks, peaks_src = load_peaks()
+    achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": "top-k key selection rows/s",
+        "value": R / (ms_per_step * 1e-3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 -> i32", "data": "synthetic",
+        "config": {"workload": args.workload, "rows": R, "n_cols": case.n_cols, "topk": case.topk,
+                   "in_range_logits": valid,
+                   "l2": "flushed (256 MiB write) before every timed step; the logits exceed L2",
+                   "step": "mqa_topk_indices"},
+        "median_ms": statistics.median(times_ms),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes": alg_bytes, "peak_source": f"{peaks_src} HBM copy"},
+        "e2e": {"value": R / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": host_out.numel() * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        info = topk_oracle_sample(case, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": info["rows_per_s"], "unit": "rows/s", "cores": info["cores"],
+                                "kind": "oracle",
+                                "sample": f"{info['rows']} of {R} rows ({info['wall_s']:.1f} s of "
+                                          f"oracle time), throughput extrapolated"}
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def paged_oracle_sample(case, budget_s: float):
@@ -302,6 +423,8 @@ def oracle_sample(case, budget_s: float, max_rows: int = 4096):
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
+    if is_topk(args.workload):
+        return run_reference_topk(args)
     case = make_case(args.workload)
     valid = int(case.valid_counts().sum())
     flops_full = valid * 2.0 * case.H * case.D
@@ -333,6 +456,33 @@ def run_reference(args, rank, world):
                          "sample": f"{info['rows']} of {case.B * case.next_n if paged else case.S_q} rows per step, "
                                    f"extrapolated to the full workload ({info['wall_s']:.1f} s)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_topk(args):
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    case = wl.topk_config(args.workload)
+    for _ in range(args.warmup):
+        topk_oracle_sample(case, budget_s=0.3)
+    budget = args.ref_budget or max(1.0, min(6.0, 90.0 / max(1, args.steps)))
+    per_step, info = [], None
+    for _ in range(args.steps):
+        info = topk_oracle_sample(case, budget_s=budget)
+        per_step.append(info["rows_per_s"])
+    value = statistics.median(per_step)
+    line = {
+        "impl": "reference", "metric": "top-k key selection rows/s", "value": value,
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": case.rows / value * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 -> i32", "data": "synthetic",
+        "config": {"workload": args.workload, "rows": case.rows, "n_cols": case.n_cols,
+                   "topk": case.topk},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": info["cores"], "kind": "oracle",
+                         "sample": f"{info['rows']} of {case.rows} rows per step, extrapolated to "
+                                   f"the full workload ({info['wall_s']:.1f} s)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -373,6 +523,10 @@ def main():
     if pg:
         pg.barrier()
     mqa.load_library()
+    if is_topk(args.workload):
+        if world > 1:
+            raise SystemExit("the top-k workload is measured on one GPU")
+        return bench_topk(args, mqa, torch, dev, torch.cuda.current_stream())
     if is_paged(args.workload):
         if world > 1:
             raise SystemExit("the paged workload is measured on one GPU")

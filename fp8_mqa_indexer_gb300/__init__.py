@@ -10,6 +10,7 @@ CPU fallback: if the library is missing or no GPU is present the calls raise.
     meta = paged_mqa_logits_metadata(context_lens, next_n=2, block_kv=64)  # paged
     logits = paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens,
                               block_table, meta)
+    idx = mqa_topk_indices(logits, k_start, k_end, topk=2048)      # top-k keys
 """
 from __future__ import annotations
 
@@ -20,7 +21,7 @@ from typing import Optional
 
 __all__ = [
     "MQAError", "mqa_logits", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
-    "paged_mqa_logits_noalloc",
+    "paged_mqa_logits_noalloc", "mqa_topk_indices", "paged_mqa_topk_indices",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
     "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS",
 ]
@@ -68,6 +69,8 @@ def load_library() -> ctypes.CDLL:
             "paged_mqa_logits_metadata": ([P, I, I, I, I, P, P], I),
             "paged_mqa_logits": ([P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I64, U, P], I),
             "paged_mqa_logits_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I64, U, P], I),
+            "mqa_topk_indices": ([P, P, P, P, I, I, I64, I, U, P], I),
+            "paged_mqa_topk_indices": ([P, P, P, I, I, I, I64, I, P], I),
             "mqa_get_num_sms": ([I], I),
             "mqa_device_status": ([P], I),
             "mqa_set_wait_limit": ([ULL], I),
@@ -267,6 +270,73 @@ def paged_mqa_logits_noalloc(q, kv_cache, kv_scales, weights, context_lens, bloc
             _ptr(block_table), block_table.shape[1], _ptr(logits), B, next_n, H, D, block_kv,
             num_blocks, logits.stride(0), flags, _stream_handle(stream)))
     return logits
+
+
+def _logits_matrix(logits, rows: int) -> None:
+    import torch
+    if not (isinstance(logits, torch.Tensor) and logits.is_cuda and logits.dtype == torch.float32
+            and logits.dim() == 2 and logits.stride(1) == 1 and logits.shape[0] == rows):
+        raise ValueError("logits must be a CUDA float32 [rows, ldo] matrix with unit column stride")
+
+
+def _indices_out(indices, rows: int, topk: int, device):
+    import torch
+    if indices is None:
+        return torch.empty((rows, topk), dtype=torch.int32, device=device)
+    if not (indices.is_cuda and indices.dtype == torch.int32 and indices.is_contiguous()
+            and tuple(indices.shape) == (rows, topk)):
+        raise ValueError("indices must be a contiguous CUDA int32 [rows, topk] tensor")
+    return indices
+
+
+def mqa_topk_indices(logits, k_start, k_end, topk: int, indices=None, *, S_kv: Optional[int] = None,
+                     compressed: bool = False, stream=None):
+    """Top-k keys per row of dense logits (C ABI ``mqa_topk_indices``).
+
+    ``logits`` [S_q, ldo] float32 (the output of ``mqa_logits``), ``k_start`` /
+    ``k_end`` [S_q] int32 (the ranges given to it).  Returns int32 [S_q, topk]:
+    the keys with the largest logits in ascending key order, then -1.
+    ``S_kv`` (keys of an uncompressed row) defaults to ``ldo``; compressed
+    logits need it.
+    """
+    import torch
+    _dev(k_start, "k_start", (torch.int32,))
+    _dev(k_end, "k_end", (torch.int32,))
+    S_q = k_start.shape[0]
+    if k_end.shape != (S_q,):
+        raise ValueError("k_start and k_end must have the same length")
+    _logits_matrix(logits, S_q)
+    ldo = logits.stride(0)
+    if S_kv is None:
+        if compressed:
+            raise ValueError("compressed logits need S_kv (the keys of an uncompressed row)")
+        S_kv = logits.shape[1]
+    indices = _indices_out(indices, S_q, topk, logits.device)
+    flags = MQA_COMPRESSED if compressed else 0
+    with torch.cuda.device(logits.device):
+        _check(load_library().mqa_topk_indices(_ptr(logits), _ptr(k_start), _ptr(k_end), _ptr(indices),
+                                               S_q, S_kv, ldo, topk, flags, _stream_handle(stream)))
+    return indices
+
+
+def paged_mqa_topk_indices(logits, context_lens, topk: int, indices=None, *, next_n: int,
+                           width: Optional[int] = None, stream=None):
+    """Top-k keys per row of paged decode logits (C ABI
+    ``paged_mqa_topk_indices``): row b * next_n + t selects among keys
+    [0, context_lens[b] - next_n + t + 1).  ``width`` (keys per row) defaults
+    to the logits' column count."""
+    import torch
+    _dev(context_lens, "context_lens", (torch.int32,))
+    B = context_lens.shape[0]
+    _logits_matrix(logits, B * next_n)
+    if width is None:
+        width = logits.shape[1]
+    indices = _indices_out(indices, B * next_n, topk, logits.device)
+    with torch.cuda.device(logits.device):
+        _check(load_library().paged_mqa_topk_indices(_ptr(logits), _ptr(context_lens), _ptr(indices),
+                                                     B, next_n, width, logits.stride(0), topk,
+                                                     _stream_handle(stream)))
+    return indices
 
 
 def device_status(stream=None) -> int:

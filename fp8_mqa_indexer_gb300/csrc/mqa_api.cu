@@ -1,6 +1,7 @@
 // mqa_api.cu -- the C ABI declared in include/mqa.h: argument validation, TMA
 // tensor-map encoding, the paged work-schedule kernel, the optional on-device
-// bounds check, the device status word, and kernel launches.
+// bounds check, the device status word, and kernel launches (the logits
+// kernels and the top-k selection).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -13,6 +14,7 @@
 
 #include "mqa.h"
 #include "launch.h"
+#include "topk.h"
 
 using namespace mqa;
 
@@ -650,6 +652,85 @@ mqa_status paged_mqa_logits_noalloc(const void* q, const void* kv_cache, const f
     return paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
                             max_blocks_per_seq, sched, logits, B, next_n, H, D, block_kv,
                             num_blocks, num_sms, ldo, flags, stream);
+}
+
+// ------------------------------------------------------- top-k selection
+namespace {
+mqa_status launch_topk_checked(TopkParams& p, cudaStream_t stream)
+{
+    if (p.rows == 0)
+        return MQA_OK;
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+    const int cap = kTopkCtasPerSm * g_num_sms[dev];
+    cudaError_t e = launch_topk(p, p.rows < cap ? p.rows : cap, stream);
+    return e == cudaSuccess ? MQA_OK : cuda_fail(e, "top-k kernel launch");
+}
+}  // namespace
+
+mqa_status mqa_topk_indices(const float* logits, const int32_t* k_start, const int32_t* k_end,
+                            int32_t* indices, int S_q, int S_kv, int64_t ldo, int topk,
+                            unsigned flags, mqa_stream_t stream)
+{
+    if (flags & ~(unsigned)(MQA_CLEAN | MQA_COMPRESSED))
+        return fail(MQA_ERR_INVALID_ARG, "unknown or unsupported flag bits 0x%x", flags);
+    const bool compressed = (flags & MQA_COMPRESSED) != 0;
+    if (S_q < 0 || S_kv < 0 || topk < 1)
+        return fail(MQA_ERR_INVALID_ARG, "need S_q >= 0, S_kv >= 0, topk >= 1");
+    if (!compressed && ldo < S_kv)
+        return fail(MQA_ERR_INVALID_ARG, "ldo (%lld) < S_kv (%d)", (long long)ldo, S_kv);
+    if (compressed && ldo < 1)
+        return fail(MQA_ERR_INVALID_ARG, "compressed logits need ldo >= 1");
+    if (S_q == 0)
+        return MQA_OK;
+    if (!logits || !k_start || !k_end || !indices)
+        return fail(MQA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(logits, 4) || !aligned(k_start, 4) || !aligned(k_end, 4) || !aligned(indices, 4))
+        return fail(MQA_ERR_INVALID_ARG, "logits, k_start, k_end, indices must be 4-byte aligned");
+    TopkParams p;
+    memset(&p, 0, sizeof(p));
+    p.logits = logits;
+    p.ldo = ldo;
+    p.rows = S_q;
+    p.n_cols = S_kv;
+    p.k_start = k_start;
+    p.k_end = k_end;
+    p.compressed = compressed ? 1 : 0;
+    p.topk = topk;
+    p.indices = indices;
+    return launch_topk_checked(p, (cudaStream_t)stream);
+}
+
+mqa_status paged_mqa_topk_indices(const float* logits, const int32_t* context_lens,
+                                  int32_t* indices, int B, int next_n, int width, int64_t ldo,
+                                  int topk, mqa_stream_t stream)
+{
+    if (B < 0 || next_n < 1 || width < 0 || topk < 1)
+        return fail(MQA_ERR_INVALID_ARG, "need B >= 0, next_n >= 1, width >= 0, topk >= 1");
+    if (ldo < width)
+        return fail(MQA_ERR_INVALID_ARG, "ldo (%lld) < width (%d)", (long long)ldo, width);
+    if ((long long)B * next_n >= INT_MAX)
+        return fail(MQA_ERR_INVALID_ARG, "B * next_n too large");
+    if (B == 0)
+        return MQA_OK;
+    if (!logits || !context_lens || !indices)
+        return fail(MQA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(logits, 4) || !aligned(context_lens, 4) || !aligned(indices, 4))
+        return fail(MQA_ERR_INVALID_ARG, "logits, context_lens, indices must be 4-byte aligned");
+    TopkParams p;
+    memset(&p, 0, sizeof(p));
+    p.logits = logits;
+    p.ldo = ldo;
+    p.rows = B * next_n;
+    p.n_cols = width;
+    p.context_lens = context_lens;
+    p.next_n = next_n;
+    p.topk = topk;
+    p.indices = indices;
+    return launch_topk_checked(p, (cudaStream_t)stream);
 }
 
 }  // extern "C"

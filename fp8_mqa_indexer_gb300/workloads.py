@@ -231,3 +231,71 @@ PAGED_CONFIGS = {
 
 def paged_config(name: str) -> PagedCase:
     return paged_case(name=name, **PAGED_CONFIGS[name])
+
+
+@dataclass
+class TopkCase:
+    """Input of the top-k key selection: a logits matrix and its row ranges."""
+    name: str
+    logits: torch.Tensor    # [rows, ldo] float32
+    k_start: torch.Tensor   # [rows] int32
+    k_end: torch.Tensor     # [rows] int32
+    n_cols: int             # keys of an uncompressed row
+    topk: int
+    compressed: bool = False
+
+    @property
+    def rows(self):
+        return self.logits.shape[0]
+
+    @property
+    def ldo(self):
+        return self.logits.shape[1]
+
+    def valid_counts(self) -> torch.Tensor:
+        lo = self.k_start.to(torch.int64).clamp(0, self.n_cols)
+        hi = self.k_end.to(torch.int64).clamp(max=self.n_cols)
+        n = (hi - lo).clamp(min=0)
+        return n.clamp(max=self.ldo) if self.compressed else n
+
+
+def topk_case(rows: int, n_cols: int, topk: int, *, seed: int, ranges: str = "causal_tail",
+              levels: int = 0, ldo: Optional[int] = None, name: str = "topk",
+              k_start=None, k_end=None) -> TopkCase:
+    """Logits-shaped rows for the top-k selection: N(0,1) fp32 values (rounded
+    to multiples of 1/levels when ``levels`` > 0, which makes exact ties common)
+    and -inf outside each row's range, as clean logits have.  ``ranges`` as in
+    ``dense_case`` with S_q = rows and S_kv = n_cols."""
+    g = _gen(seed)
+    L = torch.empty((rows, ldo or n_cols), dtype=torch.float32)
+    chunk = max(1, (1 << 24) // max(1, L.shape[1]))
+    for r in range(0, rows, chunk):
+        x = torch.randn((min(chunk, rows - r), L.shape[1]), generator=g)
+        if levels:
+            x = torch.round(x * levels) / levels
+        L[r:r + x.shape[0]] = x
+    i = torch.arange(rows, dtype=torch.int32)
+    if ranges == "causal_tail":
+        ks, ke = torch.zeros_like(i), n_cols - rows + i
+    elif ranges == "full":
+        ks, ke = torch.zeros_like(i), torch.full_like(i, n_cols)
+    elif ranges == "custom":
+        ks = torch.as_tensor(k_start, dtype=torch.int32)
+        ke = torch.as_tensor(k_end, dtype=torch.int32)
+    else:
+        raise ValueError(ranges)
+    cols = torch.arange(L.shape[1], dtype=torch.int64)[None, :]
+    outside = (cols < ks.to(torch.int64)[:, None]) | (cols >= ke.to(torch.int64)[:, None])
+    L[outside] = float("-inf")
+    return TopkCase(name, L, ks.contiguous(), ke.contiguous(), n_cols, topk)
+
+
+# The selection over rows shaped like the 2048 x 32768 dense workload's logits,
+# k = 2048 (the pages leave k to the caller).
+TOPK_CONFIGS = {
+    "topk_2k_32k_k2048": dict(rows=2048, n_cols=32768, topk=2048, ranges="causal_tail", seed=1005),
+}
+
+
+def topk_config(name: str) -> TopkCase:
+    return topk_case(name=name, **TOPK_CONFIGS[name])

@@ -176,6 +176,46 @@ MQA_API mqa_status paged_mqa_logits_noalloc(const void *q, const void *kv_cache,
                                             int block_kv, int num_blocks, int64_t ldo,
                                             unsigned flags, mqa_stream_t stream);
 
+/*
+ * Top-k keys per query row of dense MQA logits: the `indices` that the
+ * sparse-attention call on the "FlashMLA" page consumes (parameters of
+ * flash_mla_with_kvcache: shape (batch, seq_len_q, topk), invalid entries set
+ * to -1).  The pages fix only that contract; this library reads it as:
+ *
+ *   row i of `indices` holds the min(topk, len_i) keys j of the row's range
+ *   with the largest logits[i, j], in ascending key order, then -1 up to topk.
+ *   "Largest" follows the IEEE-754 totalOrder of the fp32 value (-NaN < -inf
+ *   < ... < -0 < +0 < ... < +inf < +NaN); among equal values the smaller key
+ *   is taken, so the result is unique.
+ *
+ *   logits   [S_q, ldo] fp32, 4-byte aligned: the output of mqa_logits
+ *   k_start, k_end [S_q] int32: the ranges given to mqa_logits, intersected
+ *            with [0, S_kv) in the same way (start >= end: no keys)
+ *   indices  [S_q, topk] int32 output, 4-byte aligned
+ *   S_kv     keys of an uncompressed row, ldo >= S_kv.  With MQA_COMPRESSED
+ *            key j of row i is read at column j - k_start[i], and a range
+ *            longer than ldo is cut at k_start[i] + ldo.
+ *   topk >= 1; flags: MQA_COMPRESSED (MQA_CLEAN is accepted and has no
+ *   effect; MQA_CHECK_BOUNDS is rejected).
+ * The logits are only read; positions outside the ranges are never read.
+ */
+MQA_API mqa_status mqa_topk_indices(const float *logits, const int32_t *k_start,
+                                    const int32_t *k_end, int32_t *indices, int S_q, int S_kv,
+                                    int64_t ldo, int topk, unsigned flags, mqa_stream_t stream);
+
+/*
+ * Top-k keys per row of paged decode logits (the output of paged_mqa_logits):
+ * row r = b * next_n + t selects among keys [0, context_lens[b] - next_n + t +
+ * 1) intersected with [0, width), with the rules of mqa_topk_indices.
+ *
+ *   logits       [B * next_n, ldo] fp32, 4-byte aligned; width <= ldo keys a row
+ *   context_lens [B] int32
+ *   indices      [B * next_n, topk] int32 output, 4-byte aligned
+ */
+MQA_API mqa_status paged_mqa_topk_indices(const float *logits, const int32_t *context_lens,
+                                          int32_t *indices, int B, int next_n, int width,
+                                          int64_t ldo, int topk, mqa_stream_t stream);
+
 /* Number of SMs of `device` (cached), or -1 on error. */
 MQA_API int mqa_get_num_sms(int device);
 

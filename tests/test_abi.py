@@ -116,3 +116,43 @@ def test_valid_call_without_gpu_fails_cleanly(lib):
     # passes validation, then the first CUDA runtime call fails: MQA_ERR_CUDA
     assert call_dense(lib) == 3
     assert lib.mqa_get_num_sms(0) == -1
+
+
+def call_topk(lib, **kw):
+    a = dict(logits=F, k_start=F, k_end=F, indices=F, S_q=4, S_kv=256, ldo=256, topk=16, flags=0)
+    a.update(kw)
+    return lib.mqa_topk_indices(a["logits"], a["k_start"], a["k_end"], a["indices"], a["S_q"],
+                                a["S_kv"], a["ldo"], a["topk"], a["flags"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(topk=0), 1), (dict(S_q=-1), 1), (dict(S_kv=-1), 1), (dict(ldo=255), 1),
+    (dict(flags=2, ldo=0), 1), (dict(flags=4), 1), (dict(flags=8), 1), (dict(logits=None), 1),
+    (dict(indices=None), 1), (dict(k_end=None), 1), (dict(logits=F + 2), 1), (dict(indices=F + 1), 1),
+])
+def test_topk_rejects_invalid_arguments(lib, kw, status):
+    assert call_topk(lib, **kw) == status
+    assert lib.mqa_last_error_message().decode()
+
+
+def test_topk_zero_rows_is_a_no_op(lib):
+    assert call_topk(lib, S_q=0, logits=None, indices=None) == 0
+
+
+def call_paged_topk(lib, **kw):
+    a = dict(logits=F, ctx=F, indices=F, B=2, next_n=2, width=1024, ldo=1024, topk=16)
+    a.update(kw)
+    return lib.paged_mqa_topk_indices(a["logits"], a["ctx"], a["indices"], a["B"], a["next_n"],
+                                      a["width"], a["ldo"], a["topk"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(topk=0), 1), (dict(B=-1), 1), (dict(next_n=0), 1), (dict(width=-1), 1),
+    (dict(ldo=1000), 1), (dict(ctx=None), 1), (dict(logits=F + 2), 1),
+])
+def test_paged_topk_rejects_invalid_arguments(lib, kw, status):
+    assert call_paged_topk(lib, **kw) == status
+
+
+def test_paged_topk_zero_batch_is_a_no_op(lib):
+    assert call_paged_topk(lib, B=0, logits=None) == 0
