@@ -37,12 +37,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_PER_BF16 = 2.0   # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 KERNEL_SOURCES = ["fp8_mqa_indexer_gb300/csrc/mqa_kernel.cuh", "fp8_mqa_indexer_gb300/csrc/ptx.cuh",
                   "fp8_mqa_indexer_gb300/csrc/launch.h"]
+TOPK_SOURCES = ["fp8_mqa_indexer_gb300/csrc/mqa_topk.cu", "fp8_mqa_indexer_gb300/csrc/topk.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -56,13 +57,13 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, sources=KERNEL_SOURCES):
     """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         rec = json.load(f).get(workload)
-    if not rec or rec.get("kernel_hash") != kernel_hash():
+    if not rec or rec.get("kernel_hash") != kernel_hash(sources):
         return None
     return rec.get("bytes_per_launch")
 
@@ -244,7 +245,8 @@ def bench_topk(args, mqa, torch, dev, stream):
                    "step": "mqa_topk_indices"},
         "median_ms": statistics.median(times_ms),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic(args.workload, TOPK_SOURCES),
                      "algorithmic_bytes": alg_bytes, "peak_source": f"{peaks_src} HBM copy"},
         "e2e": {"value": R / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": host_out.numel() * 4, "ms_per_step": e2e_ms},
@@ -256,7 +258,8 @@ def bench_topk(args, mqa, torch, dev, stream):
         line["cpu_baseline"] = {"value": info["rows_per_s"], "unit": "rows/s", "cores": info["cores"],
                                 "kind": "oracle",
                                 "sample": f"{info['rows']} of {R} rows ({info['wall_s']:.1f} s of "
-                                          f"oracle time), throughput extrapolated"}
+                                          f"oracle time)" + (", throughput extrapolated"
+                                                             if info["rows"] < R else "")}
     print(json.dumps(line), flush=True)
     return 0
 

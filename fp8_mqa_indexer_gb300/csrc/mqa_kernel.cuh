@@ -249,13 +249,13 @@ constexpr unsigned kProducerSleepNs = 256;
 constexpr unsigned kMmaSleepNs = 0;
 
 // --------------------------------------------------------------- epilogue
-// Epilogue of one warp: per work unit it reads its 32 keys x 128 columns of
-// the TMEM accumulator (keys on lanes, (token, head) on columns) in two halves
-// of 64 columns, reduces sum_h w[h] * ReLU(s x) per token and writes the
-// row-masked logits.  The 128 head weights of its columns stay in registers
+// Epilogue of one warp: per work unit it reads its 32 keys x 64 columns of
+// the TMEM accumulator (keys on lanes, (token, head) on columns) in pieces of
+// 16 columns, reduces sum_h w[h] * ReLU(s x) per token and writes the
+// row-masked logits.  The 64 head weights of its columns stay in registers
 // for the whole query block; the output row and key range of each of its
 // tokens sit in shared memory, written once per block.  The accumulator goes
-// back to the MMA warp as soon as the second half is in registers.
+// back to the MMA warp as soon as the last piece is in registers.
 //
 // Arithmetic per element: with s >= 0 for every key of the warp, ReLU(s x) =
 // s * max(x, 0), so the warp accumulates w * max(x, 0) with packed FFMA2 and

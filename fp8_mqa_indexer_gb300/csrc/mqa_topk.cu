@@ -7,14 +7,23 @@
 // -1).  Larger means later in the IEEE-754 totalOrder of the fp32 value;
 // among equal values the smaller key is taken, so the result is unique.
 //
-// A persistent grid (two CTAs per SM) walks the rows, one row per CTA at a
-// time.  Each logit maps to a 32-bit key whose unsigned order is totalOrder,
-// and a radix select over three digits (bits 31..20, 19..8, 7..0) finds the
-// k-th largest key T:
+// A persistent grid (four CTAs per SM) walks the rows, one row per CTA at a
+// time.  A block-wide step covers four tiles of 4 x 256 elements; a thread
+// loads four consecutive elements of each tile (coalesced 16-byte loads, four
+// in flight per thread).  Each logit maps to a 32-bit key whose unsigned
+// order is totalOrder, and a radix select over three digits (bits 31..20,
+// 19..8, 7..0) finds the k-th largest key T:
+//   0. (rows with k <= 2048 and at least max(8192, 4 k) keys) a sample of
+//      1/16 of the row sets a threshold t0 that about 1.4 k keys clear; one
+//      ordered pass compacts every key >= t0 into shared memory and, when
+//      that list holds between k and its capacity of keys, steps 3 and 4 (and
+//      the digit-1 histogram) run on the list alone: the row is read from HBM
+//      once.  Otherwise:
 //   1. histogram of digit 1 over the row (the row's read from HBM) gives the
 //      bin holding the k-th largest key;
 //   2. every element in or above that bin is compacted, in key order, into
-//      shared memory (a second read of the row, normally from L2);
+//      shared memory (a second read of the row, from L2: the first read marks
+//      the row's lines evict-last, the second evict-first);
 //   3. histograms of digits 2 and 3 over the compacted elements of the bin
 //      give T, the count of keys above T, and r = the number of keys equal to
 //      T that are taken (the r smallest such keys);
@@ -30,16 +39,20 @@ namespace {
 
 constexpr int kNT = kTopkThreads;
 constexpr int kNW = kNT / 32;
-constexpr int kTile = 4 * kNT;   // elements per block-wide step (four per thread)
-constexpr int kBins12 = 4096;    // digits 1 and 2
-constexpr int kBins8 = 256;      // digit 3
-constexpr int kCap = 8192;       // compacted elements held in shared memory
+constexpr int kPer = 16;            // elements per thread per step: 4 tiles x 4
+constexpr int kTile = 4 * kNT;      // elements per tile
+constexpr int kStep = kPer * kNT;   // elements per block-wide step (4 tiles)
+constexpr int kBins12 = 4096;       // digits 1 and 2
+constexpr int kBins8 = 256;         // digit 3
+constexpr int kCap = 4096;          // compacted elements held in shared memory
+static_assert(kTile < (1 << 16), "per-tile counts are packed in 16-bit fields");
 
 struct TopkSmem {
-    unsigned hist[kBins12];
-    unsigned cand_key[kCap];
-    int cand_idx[kCap];
+    alignas(16) unsigned hist[kBins12];
+    alignas(16) unsigned cand_key[kCap];
+    alignas(16) int cand_idx[kCap];
     unsigned warp_sum[2][kNW];
+    unsigned long long warp_sum64[2][2][kNW];
     unsigned sel_bin, sel_above, sel_count;
 };
 
@@ -49,6 +62,35 @@ __device__ __forceinline__ unsigned order_key(float v)
 {
     const unsigned u = __float_as_uint(v);
     return u ^ ((unsigned)((int)u >> 31) | 0x80000000u);
+}
+
+// L2 eviction policies for the two reads of a row.
+__device__ __forceinline__ unsigned long long policy_evict_last()
+{
+    unsigned long long p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ unsigned long long policy_evict_first()
+{
+    unsigned long long p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ float4 load4(const float* ptr, unsigned long long pol)
+{
+    float4 v;
+    asm("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(ptr), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ float4 load4(const float* ptr)
+{
+    return __ldg(reinterpret_cast<const float4*>(ptr));
 }
 
 // Exclusive prefix sum of v over the block in thread order; `total` gets the
@@ -78,27 +120,89 @@ __device__ __forceinline__ unsigned block_exclusive_sum(unsigned v, unsigned* ws
     return before + x - v;
 }
 
+// Exclusive prefix sums, in thread order, of two packed vectors of four 16-bit
+// counts (one field per tile of a step); tot_* get the block-wide sums.  One
+// __syncthreads, double-buffered like block_exclusive_sum.
+__device__ __forceinline__ void block_exclusive_sum64x2(unsigned long long a, unsigned long long b,
+                                                        unsigned long long (*ws)[kNW],
+                                                        unsigned long long& pre_a,
+                                                        unsigned long long& pre_b,
+                                                        unsigned long long& tot_a,
+                                                        unsigned long long& tot_b)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long x = a, y = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long xs = __shfl_up_sync(0xffffffffu, x, o);
+        const unsigned long long ys = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) {
+            x += xs;
+            y += ys;
+        }
+    }
+    if (lane == 31) {
+        ws[0][warp] = x;
+        ws[1][warp] = y;
+    }
+    __syncthreads();
+    unsigned long long ba = 0, bb = 0, ta = 0, tb = 0;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) {
+        const unsigned long long sa = ws[0][w], sb = ws[1][w];
+        ba += w < warp ? sa : 0ull;
+        bb += w < warp ? sb : 0ull;
+        ta += sa;
+        tb += sb;
+    }
+    pre_a = ba + x - a;
+    pre_b = bb + y - b;
+    tot_a = ta;
+    tot_b = tb;
+}
+
+// Start, in index order, of each tile's run of a thread: the elements of all
+// earlier tiles of the step plus those of earlier threads in this tile.
+__device__ __forceinline__ void tile_offsets(unsigned long long pre, unsigned long long tot,
+                                             unsigned (&off)[4])
+{
+    unsigned before = 0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        off[g] = before + (unsigned)((pre >> (16 * g)) & 0xffffu);
+        before += (unsigned)((tot >> (16 * g)) & 0xffffu);
+    }
+}
+
 // The bin of hist[0, NBINS) that holds the need-th largest element (1 <= need
-// <= the histogram's total): sel_bin, sel_above (elements in higher bins) and
-// sel_count (elements in the bin).  Ends with the selection visible to all.
+// <= the histogram's total): its index, the elements in higher bins and the
+// elements in the bin.  Ends with the selection visible to all threads.
 template <int NBINS>
 __device__ __forceinline__ void select_bin(TopkSmem& sm, unsigned need, int& buf, unsigned& bin,
                                            unsigned& above, unsigned& count)
 {
-    constexpr int kPer = NBINS >= kNT ? NBINS / kNT : 1;
-    const int b0 = threadIdx.x * kPer;
-    unsigned h[kPer], s = 0;
+    constexpr int kB = NBINS >= kNT ? NBINS / kNT : 1;   // bins per thread
+    static_assert(kB == 1 || kB % 4 == 0, "bins are read four at a time");
+    const int b0 = threadIdx.x * kB;
+    unsigned h[kB], s = 0;
+    if constexpr (kB == 1) {
+        h[0] = b0 < NBINS ? sm.hist[b0] : 0u;
+    } else {
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-        h[q] = b0 + q < NBINS ? sm.hist[b0 + q] : 0u;
-        s += h[q];
+        for (int q = 0; q < kB; q += 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(&sm.hist[b0 + q]);
+            h[q] = v.x, h[q + 1] = v.y, h[q + 2] = v.z, h[q + 3] = v.w;
+        }
     }
+#pragma unroll
+    for (int q = 0; q < kB; ++q)
+        s += h[q];
     unsigned total;
     const unsigned before = block_exclusive_sum(s, sm.warp_sum[buf], total);
     buf ^= 1;
     unsigned acc = total - before - s;   // elements in the bins of higher threads
 #pragma unroll
-    for (int q = kPer - 1; q >= 0; --q) {
+    for (int q = kB - 1; q >= 0; --q) {
         if (acc < need && acc + h[q] >= need) {
             sm.sel_bin = (unsigned)(b0 + q);
             sm.sel_above = acc;
@@ -120,109 +224,107 @@ struct RowView {
     int key_of_col0;       // key index = column + key_of_col0
 };
 
-// f(key[4], idx[4], ok[4]) for each thread's four consecutive columns of
-// every block-wide step over the range; all threads take the same number of
-// steps, so f may synchronize the block.  Whole aligned groups load as one
-// float4, the ragged ends element by element.
-template <class F>
-__device__ __forceinline__ void for_row(const RowView& r, F&& f)
-{
-    for (long long base = r.c_start; base < r.c_hi; base += kTile) {
-        const long long c = base + 4 * threadIdx.x;
-        float v[4];
-        bool ok[4];
-        if (c >= r.c_lo && c + 4 <= r.c_hi) {
-            const float4 x = __ldg(reinterpret_cast<const float4*>(r.ptr + c));
-            v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
-            ok[0] = ok[1] = ok[2] = ok[3] = true;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                ok[e] = c + e >= r.c_lo && c + e < r.c_hi;
-                v[e] = ok[e] ? __ldg(r.ptr + c + e) : 0.f;
-            }
-        }
-        unsigned key[4];
-        int idx[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            key[e] = order_key(v[e]);
-            idx[e] = (int)(c + e) + r.key_of_col0;
-        }
-        f(key, idx, ok);
-    }
-}
+// Element e = 4 g + j of a thread's step is element j of its run in tile g.
+struct RowIdx {            // key of element e in the row
+    int key0;              // key of the thread's first element in tile 0
+    __device__ int operator()(int e) const { return key0 + (e >> 2) * kTile + (e & 3); }
+};
 
-// Digit-1 histogram with four block-wide steps per trip, so that each thread
-// has four 16-byte loads in flight.
-__device__ __forceinline__ void hist_digit1(TopkSmem& sm, const RowView& r)
+struct CandIdx {           // key of element e in the compacted list
+    const int* p;          // the thread's first entry in tile 0
+    __device__ int operator()(int e) const { return p[(e >> 2) * kTile + (e & 3)]; }
+};
+
+// f(key[16], okmask, idx) for every block-wide step over the range: element
+// 4 g + j of thread t is column base + g * kTile + 4 t + j.  All threads take
+// the same number of steps, so f may synchronize the block.  Whole aligned
+// runs load as float4 with L2 policy `pol`, the ragged ends element by element.
+template <bool HINT, class F>
+__device__ __forceinline__ void for_row(const RowView& r, unsigned long long pol, F&& f)
 {
-    for (long long base = r.c_start; base < r.c_hi; base += 4 * kTile) {
-        float v[4][4];
-        bool ok[4][4];
+    for (long long base = r.c_start; base < r.c_hi; base += kStep) {
+        const long long c0 = base + 4 * threadIdx.x;
+        float v[kPer];
+        if (base >= r.c_lo && base + kStep <= r.c_hi) {   // the whole step is in range
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 x = HINT ? load4(r.ptr + c0 + g * kTile, pol) : load4(r.ptr + c0 + g * kTile);
+                v[4 * g] = x.x, v[4 * g + 1] = x.y, v[4 * g + 2] = x.z, v[4 * g + 3] = x.w;
+            }
+            unsigned key[kPer];
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                key[e] = order_key(v[e]);
+            f(key, (1u << kPer) - 1u, RowIdx{(int)c0 + r.key_of_col0});
+            continue;
+        }
+        unsigned okm = 0;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            const long long c = base + g * kTile + 4 * threadIdx.x;
+            const long long c = c0 + g * kTile;
             if (c >= r.c_lo && c + 4 <= r.c_hi) {
-                const float4 x = __ldg(reinterpret_cast<const float4*>(r.ptr + c));
-                v[g][0] = x.x, v[g][1] = x.y, v[g][2] = x.z, v[g][3] = x.w;
-                ok[g][0] = ok[g][1] = ok[g][2] = ok[g][3] = true;
+                const float4 x = HINT ? load4(r.ptr + c, pol) : load4(r.ptr + c);
+                v[4 * g] = x.x, v[4 * g + 1] = x.y, v[4 * g + 2] = x.z, v[4 * g + 3] = x.w;
+                okm |= 0xfu << (4 * g);
             } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    ok[g][e] = c + e >= r.c_lo && c + e < r.c_hi;
-                    v[g][e] = ok[g][e] ? __ldg(r.ptr + c + e) : 0.f;
+                for (int j = 0; j < 4; ++j) {
+                    const bool ok = c + j >= r.c_lo && c + j < r.c_hi;
+                    v[4 * g + j] = ok ? __ldg(r.ptr + c + j) : 0.f;
+                    okm |= (unsigned)ok << (4 * g + j);
                 }
             }
         }
+        unsigned key[kPer];
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (ok[g][e])
-                    atomicAdd(&sm.hist[order_key(v[g][e]) >> 20], 1u);
+        for (int e = 0; e < kPer; ++e)
+            key[e] = order_key(v[e]);
+        f(key, okm, RowIdx{(int)c0 + r.key_of_col0});
     }
 }
 
-// f(key[4], idx[4], ok[4]) over the first m compacted elements, four per
-// thread per block-wide step, in key order.
+// The same over the first m compacted elements, in key order (entry
+// base + g * kTile + 4 t + j).
 template <class F>
 __device__ __forceinline__ void for_cand(const TopkSmem& sm, unsigned m, F&& f)
 {
-    for (unsigned base = 0; base < m; base += kTile) {
-        unsigned key[4];
-        int idx[4];
-        bool ok[4];
+    for (unsigned base = 0; base < m; base += kStep) {
+        const unsigned k0 = base + 4 * threadIdx.x;
+        unsigned key[kPer], okm = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const unsigned k = base + 4 * threadIdx.x + e;
-            ok[e] = k < m;
-            key[e] = ok[e] ? sm.cand_key[k] : 0u;
-            idx[e] = ok[e] ? sm.cand_idx[k] : 0;
+        for (int g = 0; g < 4; ++g) {
+            const unsigned k = k0 + g * kTile;
+            const uint4 v = k < (unsigned)kCap ? *reinterpret_cast<const uint4*>(&sm.cand_key[k])
+                                               : make_uint4(0u, 0u, 0u, 0u);
+            key[4 * g] = v.x, key[4 * g + 1] = v.y, key[4 * g + 2] = v.z, key[4 * g + 3] = v.w;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                okm |= (unsigned)(k + j < m) << (4 * g + j);
         }
-        f(key, idx, ok);
+        f(key, okm, CandIdx{sm.cand_idx + (k0 < (unsigned)kCap ? k0 : 0u)});
     }
 }
 
 template <int NBINS>
 __device__ __forceinline__ void clear_hist(TopkSmem& sm)
 {
-    for (int b = threadIdx.x; b < NBINS; b += kNT)
-        sm.hist[b] = 0u;
+    uint4* h4 = reinterpret_cast<uint4*>(sm.hist);
+    for (int b = threadIdx.x; b < NBINS / 4; b += kNT)
+        h4[b] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 }
 
-// Digits 2 and 3 over `each` (a for_row or for_cand walk), then the ordered
-// write of the selection.  b1 / above1 come from digit 1.
+// Digits 2 and 3 over `each` (a row or list walk), then the ordered write of
+// the selection.  b1 / above1 come from digit 1.
 template <class Walk>
 __device__ __forceinline__ void finish_row(TopkSmem& sm, Walk&& each, unsigned b1, unsigned above1,
                                            unsigned k, int* out, int& buf)
 {
     clear_hist<kBins12>(sm);
-    each([&](const unsigned(&key)[4], const int(&)[4], const bool(&ok)[4]) {
+    each([&](const unsigned(&key)[kPer], unsigned okm, auto) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (ok[e] && (key[e] >> 20) == b1)
+        for (int e = 0; e < kPer; ++e)
+            if (((okm >> e) & 1u) && (key[e] >> 20) == b1)
                 atomicAdd(&sm.hist[(key[e] >> 8) & 0xfffu], 1u);
     });
     __syncthreads();
@@ -230,10 +332,10 @@ __device__ __forceinline__ void finish_row(TopkSmem& sm, Walk&& each, unsigned b
     select_bin<kBins12>(sm, k - above1, buf, b2, above2, cnt);
     const unsigned prefix = (b1 << 12) | b2;
     clear_hist<kBins8>(sm);
-    each([&](const unsigned(&key)[4], const int(&)[4], const bool(&ok)[4]) {
+    each([&](const unsigned(&key)[kPer], unsigned okm, auto) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (ok[e] && (key[e] >> 8) == prefix)
+        for (int e = 0; e < kPer; ++e)
+            if (((okm >> e) & 1u) && (key[e] >> 8) == prefix)
                 atomicAdd(&sm.hist[key[e] & 0xffu], 1u);
     });
     __syncthreads();
@@ -242,36 +344,176 @@ __device__ __forceinline__ void finish_row(TopkSmem& sm, Walk&& each, unsigned b
     const unsigned T = (prefix << 8) | b3;
     const unsigned r = k - above1 - above2 - above3;   // keys equal to T that are taken
     unsigned gt_run = 0, eq_run = 0;
-    each([&](const unsigned(&key)[4], const int(&idx)[4], const bool(&ok)[4]) {
-        unsigned g = 0, q = 0;
+    each([&](const unsigned(&key)[kPer], unsigned okm, auto idx) {
+        unsigned gm = 0, qm = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            g += ok[e] && key[e] > T;
-            q += ok[e] && key[e] == T;
+        for (int e = 0; e < kPer; ++e) {
+            const bool ok = (okm >> e) & 1u;
+            gm |= (unsigned)(ok && key[e] > T) << e;
+            qm |= (unsigned)(ok && key[e] == T) << e;
         }
-        // a step holds at most kTile < 2^16 elements: both counts fit 16 bits
-        unsigned tot;
-        const unsigned off = block_exclusive_sum(g | (q << 16), sm.warp_sum[buf], tot);
-        buf ^= 1;
-        unsigned gb = gt_run + (off & 0xffffu), eb = eq_run + (off >> 16);
+        unsigned long long ga = 0, qa = 0;   // per-tile counts, 16 bits each
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (!ok[e])
-                continue;
-            if (key[e] > T) {
-                const unsigned pos = gb + min(eb, r);
-                if (pos < k)
-                    out[pos] = idx[e];
-                ++gb;
-            } else if (key[e] == T) {
-                if (eb < r && gb + eb < k)
-                    out[gb + eb] = idx[e];
-                ++eb;
+        for (int g = 0; g < 4; ++g) {
+            ga |= (unsigned long long)__popc((gm >> (4 * g)) & 0xfu) << (16 * g);
+            qa |= (unsigned long long)__popc((qm >> (4 * g)) & 0xfu) << (16 * g);
+        }
+        unsigned long long gpre, qpre, gtot, qtot;
+        block_exclusive_sum64x2(ga, qa, sm.warp_sum64[buf], gpre, qpre, gtot, qtot);
+        buf ^= 1;
+        unsigned goff[4], qoff[4];
+        tile_offsets(gpre, gtot, goff);
+        tile_offsets(qpre, qtot, qoff);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            unsigned gb = gt_run + goff[g], eb = eq_run + qoff[g];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = 4 * g + j;
+                if ((gm >> e) & 1u) {
+                    const unsigned pos = gb + min(eb, r);
+                    if (pos < k)
+                        out[pos] = idx(e);
+                    ++gb;
+                } else if ((qm >> e) & 1u) {
+                    if (eb < r && gb + eb < k)
+                        out[gb + eb] = idx(e);
+                    ++eb;
+                }
             }
         }
-        gt_run += tot & 0xffffu;
-        eq_run += tot >> 16;
+        unsigned gsum = 0, qsum = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            gsum += (unsigned)((gtot >> (16 * g)) & 0xffffu);
+            qsum += (unsigned)((qtot >> (16 * g)) & 0xffffu);
+        }
+        gt_run += gsum;
+        eq_run += qsum;
     });
+}
+
+// Ordered compaction of the row's elements with key >= thr into the shared
+// list (the first kCap of them, in key order); returns how many there are.
+template <bool HINT>
+__device__ __forceinline__ unsigned compact_row(TopkSmem& sm, const RowView& r,
+                                                unsigned long long pol, unsigned thr, int& buf)
+{
+    unsigned run = 0;
+    for_row<HINT>(r, pol, [&](const unsigned(&key)[kPer], unsigned okm, RowIdx idx) {
+        unsigned fm = 0;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            fm |= (unsigned)(((okm >> e) & 1u) && key[e] >= thr) << e;
+        unsigned long long fa = 0;   // per-tile counts, 16 bits each
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            fa |= (unsigned long long)__popc((fm >> (4 * g)) & 0xfu) << (16 * g);
+        unsigned long long pre, unused_pre, tot, unused_tot;
+        block_exclusive_sum64x2(fa, 0ull, sm.warp_sum64[buf], pre, unused_pre, tot, unused_tot);
+        buf ^= 1;
+        unsigned off[4];
+        tile_offsets(pre, tot, off);
+        if (fm) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                unsigned pos = run + off[g];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int e = 4 * g + j;
+                    if ((fm >> e) & 1u) {
+                        if (pos < (unsigned)kCap) {
+                            sm.cand_key[pos] = key[e];
+                            sm.cand_idx[pos] = idx(e);
+                        }
+                        ++pos;
+                    }
+                }
+            }
+        }
+        unsigned sum = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            sum += (unsigned)((tot >> (16 * g)) & 0xffffu);
+        run += sum;
+    });
+    __syncthreads();
+    return run;
+}
+
+// Threshold key t0 from a sample of the row (one aligned float4 in every
+// `stride` elements, 1/16 of the keys for rows up to 65536): the lower edge of
+// the 24-bit key prefix holding the sample's need-th largest key, with need
+// scaled so that about 1.4 k keys of the whole row lie at or above t0.  The
+// sample only steers the work: whatever t0 is, the caller checks the count
+// it yields and falls back to the full selection.  Returns false when the
+// sample is too small.  Uses the shared list as scratch.
+__device__ __forceinline__ bool sample_threshold(TopkSmem& sm, const RowView& r, unsigned n,
+                                                 unsigned k, int& buf, unsigned& t0)
+{
+    const long long span = r.c_hi - r.c_start;
+    long long stride = 64;
+    while ((span + stride - 1) / stride > kCap / 4)
+        stride *= 2;
+    const int nf4 = (int)((span + stride - 1) / stride);
+    clear_hist<kBins12>(sm);
+    unsigned valid = 0;
+    for (int f = threadIdx.x; f < nf4; f += kNT) {
+        const long long c = r.c_start + f * stride;
+        uint4 kk = make_uint4(0u, 0u, 0u, 0u);   // key 0: not a sample
+        if (c >= r.c_lo && c + 4 <= r.c_hi) {
+            const float4 x = load4(r.ptr + c);
+            kk = make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
+            atomicAdd(&sm.hist[kk.x >> 20], 1u);
+            atomicAdd(&sm.hist[kk.y >> 20], 1u);
+            atomicAdd(&sm.hist[kk.z >> 20], 1u);
+            atomicAdd(&sm.hist[kk.w >> 20], 1u);
+            valid += 4;
+        }
+        *reinterpret_cast<uint4*>(&sm.cand_key[4 * f]) = kk;
+    }
+    unsigned total;
+    block_exclusive_sum(valid, sm.warp_sum[buf], total);   // also orders the atomics
+    buf ^= 1;
+    if (total < 256)
+        return false;
+    unsigned long long want = (14ull * k * total + 10ull * n - 1) / (10ull * n);
+    const unsigned need = want < 1 ? 1u : (want > total ? total : (unsigned)want);
+    unsigned b1, above1, cnt1;
+    select_bin<kBins12>(sm, need, buf, b1, above1, cnt1);
+    clear_hist<kBins12>(sm);
+    for (int f = threadIdx.x; f < nf4; f += kNT) {
+        const uint4 kk = *reinterpret_cast<const uint4*>(&sm.cand_key[4 * f]);
+        const unsigned kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (kv[j] != 0u && (kv[j] >> 20) == b1)
+                atomicAdd(&sm.hist[(kv[j] >> 8) & 0xfffu], 1u);
+    }
+    __syncthreads();
+    unsigned b2, above2, cnt2;
+    select_bin<kBins12>(sm, need - above1, buf, b2, above2, cnt2);
+    t0 = (b1 << 20) | (b2 << 8);
+    return true;
+}
+
+// Exact selection from the first m list entries (in key order), which hold
+// every key of the row that can be among its k largest (k <= m <= kCap).
+__device__ __forceinline__ void select_from_list(TopkSmem& sm, unsigned m, unsigned k, int* out,
+                                                 int& buf)
+{
+    clear_hist<kBins12>(sm);
+    for_cand(sm, m, [&](const unsigned(&key)[kPer], unsigned okm, auto) {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            if ((okm >> e) & 1u)
+                atomicAdd(&sm.hist[key[e] >> 20], 1u);
+    });
+    __syncthreads();
+    unsigned b1, above1, n1;
+    select_bin<kBins12>(sm, k, buf, b1, above1, n1);
+    finish_row(
+        sm, [&](auto&& f) { for_cand(sm, m, f); }, b1, above1, k, out, buf);
 }
 
 __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
@@ -280,6 +522,7 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
     TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
     int buf = 0;
     const unsigned k = (unsigned)p.topk;
+    const unsigned long long keep = policy_evict_last(), drop = policy_evict_first();
     for (int i = blockIdx.x; i < p.rows; i += gridDim.x) {
         // ---- the row's key range, intersected with [0, n_cols)
         long long lo, hi;
@@ -310,44 +553,40 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
             r.c_hi = r.c_lo + (long long)n;
             r.key_of_col0 = p.compressed ? (int)lo : 0;
             r.c_start = r.c_lo - (long long)((reinterpret_cast<unsigned long long>(r.ptr + r.c_lo) >> 2) & 3);
-            // ---- digit 1 over the row
-            clear_hist<kBins12>(sm);
-            hist_digit1(sm, r);
-            __syncthreads();
-            unsigned b1, above1, n1;
-            select_bin<kBins12>(sm, k, buf, b1, above1, n1);
-            const unsigned m = above1 + n1;   // elements in bin b1 or above
-            if (m <= (unsigned)kCap) {
-                // ---- compact those elements, in key order, into shared memory
-                unsigned run = 0;
-                for_row(r, [&](const unsigned(&key)[4], const int(&idx)[4], const bool(&ok)[4]) {
-                    bool f[4];
-                    unsigned cnt = 0;
+            bool done = false;
+            // ---- common case: a sampled threshold, one pass over the row
+            unsigned t0;
+            if (2u * k <= (unsigned)kCap && n >= 8192u && n >= 4u * k &&
+                sample_threshold(sm, r, n, k, buf, t0)) {
+                const unsigned m = compact_row<false>(sm, r, 0ull, t0, buf);
+                if (m >= k && m <= (unsigned)kCap) {
+                    select_from_list(sm, m, k, out, buf);
+                    done = true;
+                }
+            }
+            if (!done) {
+                // ---- full selection: digit 1 over the row
+                clear_hist<kBins12>(sm);
+                for_row<true>(r, keep, [&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        f[e] = ok[e] && (key[e] >> 20) >= b1;
-                        cnt += f[e];
-                    }
-                    unsigned tot;
-                    unsigned pos = run + block_exclusive_sum(cnt, sm.warp_sum[buf], tot);
-                    buf ^= 1;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (f[e] && pos < (unsigned)kCap) {
-                            sm.cand_key[pos] = key[e];
-                            sm.cand_idx[pos] = idx[e];
-                        }
-                        pos += f[e];
-                    }
-                    run += tot;
+                    for (int e = 0; e < kPer; ++e)
+                        if ((okm >> e) & 1u)
+                            atomicAdd(&sm.hist[key[e] >> 20], 1u);
                 });
                 __syncthreads();
-                const unsigned mm = run < (unsigned)kCap ? run : (unsigned)kCap;
-                finish_row(
-                    sm, [&](auto&& f) { for_cand(sm, mm, f); }, b1, above1, k, out, buf);
-            } else {
-                finish_row(
-                    sm, [&](auto&& f) { for_row(r, f); }, b1, above1, k, out, buf);
+                unsigned b1, above1, n1;
+                select_bin<kBins12>(sm, k, buf, b1, above1, n1);
+                const unsigned m = above1 + n1;   // elements in bin b1 or above
+                if (m <= (unsigned)kCap) {
+                    // ---- compact those elements, in key order, into shared memory
+                    const unsigned mm = compact_row<true>(sm, r, drop, b1 << 20, buf);
+                    finish_row(
+                        sm, [&](auto&& f) { for_cand(sm, mm < (unsigned)kCap ? mm : (unsigned)kCap, f); },
+                        b1, above1, k, out, buf);
+                } else {
+                    finish_row(
+                        sm, [&](auto&& f) { for_row<true>(r, drop, f); }, b1, above1, k, out, buf);
+                }
             }
         }
         for (unsigned c = taken + threadIdx.x; c < k; c += kNT)

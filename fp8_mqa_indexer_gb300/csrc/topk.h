@@ -18,8 +18,8 @@ struct TopkParams {
     int* indices;             // [rows, topk] int32 output
 };
 
-constexpr int kTopkThreads = 512;
-constexpr int kTopkCtasPerSm = 2;
+constexpr int kTopkThreads = 256;
+constexpr int kTopkCtasPerSm = 4;
 
 cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t stream);
 
