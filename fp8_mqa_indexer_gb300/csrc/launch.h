@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "mqa_kernel.cuh"
 
 namespace mqa {
@@ -27,16 +29,38 @@ cudaError_t launch_instance(const LaunchArgs& a)
 {
     auto kern = mqa_logits_kernel<H, D, PAGED>;
     const size_t smem = sizeof(Smem<D>) + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+    // The shared-memory limit is a per-device attribute of the function: set it
+    // once on each device (one bit per device; setting it twice is harmless).
+    static std::atomic<unsigned long long> attr_set{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (!(attr_set.load() & bit) || !bit) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
-        attr_set = true;
+        attr_set.fetch_or(bit);
     }
-    kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_kv, a.tm_scale, a.tm_w, a.p);
-    return cudaGetLastError();
+    if constexpr (PAGED) {
+        // a dependent of the preceding kernel (the work schedule): see
+        // grid_dependency_wait in the kernel
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = a.stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_kv, a.tm_scale, a.tm_w, a.p);
+    } else {
+        kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_kv, a.tm_scale, a.tm_w, a.p);
+        return cudaGetLastError();
+    }
 }
 
 }  // namespace mqa

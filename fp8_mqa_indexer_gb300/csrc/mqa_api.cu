@@ -157,6 +157,9 @@ __global__ void __launch_bounds__(kMetaThreads)
                           unsigned* status)
 {
     __shared__ long long warp_tot[kMetaThreads / 32];
+    // the paged logits kernel that follows may start its set-up now; it waits
+    // for this kernel's completion before reading the schedule
+    launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int chunk = (B + kMetaThreads - 1) / kMetaThreads;
     const int c0 = min(tid * chunk, B), c1 = min(c0 + chunk, B);

@@ -558,6 +558,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(&sm.tmem_base), 512);
         tmem_relinquish();
     }
+    // Paged calls are launched as dependents of the schedule kernel: the set-up
+    // above (shared memory and TMEM only) overlaps it; every global access
+    // below comes after it has finished.
+    if constexpr (PAGED)
+        grid_dependency_wait();
 
     // Work slice of this CTA: start (block, tile) and number of units.
     if (!PAGED) {

@@ -32,6 +32,8 @@
 // If the bin and everything above it do not fit shared memory (many equal or
 // nearly equal logits), steps 3 and 4 read the row from global memory.
 // Rows with at most topk keys take every key without reading the logits.
+#include <atomic>
+
 #include "topk.h"
 
 namespace mqa {
@@ -599,13 +601,18 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
 cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t stream)
 {
     const size_t smem = sizeof(TopkSmem);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+    // per-device function attribute: set once on each device (see launch.h)
+    static std::atomic<unsigned long long> attr_set{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (!(attr_set.load() & bit) || !bit) {
+        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
-        attr_set = true;
+        attr_set.fetch_or(bit);
     }
     topk_kernel<<<grid, kNT, smem, stream>>>(p);
     return cudaGetLastError();

@@ -192,3 +192,19 @@ def test_paged_logits_then_topk(dev):
                                          topk=topk)
         assert np.array_equal(idx.cpu().numpy(), want), topk
     assert mqa.device_status() == 0
+
+
+def test_row_split_matches_whole(dev):
+    """Row slabs selected by separate calls (views into the same logits, as
+    one rank per GPU would run them) give the whole call's rows bit for bit."""
+    from fp8_mqa_indexer_gb300 import sharding
+    case = wl.topk_case(301, 20000, 2048, seed=780, ranges="causal_tail", levels=2)
+    Ld, ks, ke = case.logits.to(dev), case.k_start.to(dev), case.k_end.to(dev)
+    whole = mqa.mqa_topk_indices(Ld, ks, ke, case.topk, S_kv=case.n_cols)
+    parts = []
+    for rank in range(3):
+        v, _ = sharding.topk_row_shard(Ld, ks, ke, rank, 3)
+        parts.append(mqa.mqa_topk_indices(v["logits"], v["k_start"], v["k_end"], case.topk,
+                                          S_kv=case.n_cols))
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(parts), whole)

@@ -1,6 +1,7 @@
 """Multi-rank path on CPU: two gloo ranks each score their row slab (views of
-the inputs, same keys) with the oracle; the gathered slabs must equal the
-unsharded result bit for bit, and the split must cover every row once."""
+the inputs, same keys) with the oracle, and each selects the top-k keys of its
+slab of logits rows; the gathered slabs must equal the unsharded results bit
+for bit, and the split must cover every row once."""
 import os
 import socket
 
@@ -54,6 +55,38 @@ def test_two_rank_row_sharding_is_bitwise(tmp_path):
     oracle.build()
     out = tmp_path / "result.txt"
     mp.start_processes(_worker, args=(2, _free_port(), str(out)), nprocs=2, start_method="spawn")
+    assert out.read_text() == "ok"
+
+
+def _topk_worker(rank, world, port, result_path):
+    import oracle
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    case = wl.topk_case(41, 900, 50, seed=902, ranges="causal_tail", levels=3)
+    views, (r0, r1) = sharding.topk_row_shard(case.logits, case.k_start, case.k_end, rank, world)
+    slab = oracle.topk_indices(views["logits"], views["k_start"], views["k_end"], topk=case.topk,
+                               n_cols=case.n_cols)
+    slabs = [None] * world
+    dist.all_gather_object(slabs, (r0, r1, slab))
+    if rank == 0:
+        full = oracle.topk_indices(case.logits, case.k_start, case.k_end, topk=case.topk,
+                                   n_cols=case.n_cols)
+        rows = sorted(slabs, key=lambda s: s[0])
+        got = np.concatenate([s[2] for s in rows])
+        ok = np.array_equal(got, full) and rows[0][0] == 0 and rows[-1][1] == case.rows
+        with open(result_path, "w") as f:
+            f.write("ok" if ok else "mismatch")
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_topk_sharding_is_bitwise(tmp_path):
+    import oracle
+    oracle.build()
+    out = tmp_path / "result.txt"
+    mp.start_processes(_topk_worker, args=(2, _free_port(), str(out)), nprocs=2, start_method="spawn")
     assert out.read_text() == "ok"
 
 
