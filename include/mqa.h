@@ -55,7 +55,7 @@ typedef struct CUstream_st *mqa_stream_t;
 typedef enum {
     MQA_OK = 0,
     MQA_ERR_INVALID_ARG = 1, /* bad pointer, size, stride or alignment */
-    MQA_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for */
+    MQA_ERR_UNSUPPORTED = 2, /* valid request this library has no kernel for */
     MQA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
     MQA_ERR_TIMEOUT = 4,     /* a kernel wait ran out (reported by mqa_device_status) */
     MQA_ERR_BAD_INPUT = 5    /* MQA_CHECK_BOUNDS found an out-of-range input value */
