@@ -299,3 +299,70 @@ TOPK_CONFIGS = {
 
 def topk_config(name: str) -> TopkCase:
     return topk_case(name=name, **TOPK_CONFIGS[name])
+
+
+@dataclass
+class MxDenseCase:
+    """Dense MX (block-scaled) input: E4M3 or packed E2M1 elements with four
+    UE8M0 block scales per 128-element row, packed in an int32."""
+    name: str
+    q: torch.Tensor          # [S_q, H, 128] uint8 (E4M3) or [S_q, H, 64] uint8 (E2M1 pairs)
+    q_sf: torch.Tensor       # [S_q, H] int32
+    kv: torch.Tensor         # [S_kv, 128] or [S_kv, 64] uint8
+    kv_sf: torch.Tensor      # [S_kv] int32
+    weights: torch.Tensor    # [S_q, H] float32
+    k_start: torch.Tensor    # [S_q] int32
+    k_end: torch.Tensor      # [S_q] int32
+    fp4: bool
+    ldo: int
+
+    @property
+    def S_q(self):
+        return self.q.shape[0]
+
+    @property
+    def H(self):
+        return self.q.shape[1]
+
+    @property
+    def S_kv(self):
+        return self.kv.shape[0]
+
+
+def packed_scales(shape, lo: int, hi: int, g: torch.Generator) -> torch.Tensor:
+    """int32 tensor whose four bytes are independent UE8M0 codes in [lo, hi]."""
+    b = torch.randint(lo, hi + 1, tuple(shape) + (4,), generator=g, dtype=torch.int64)
+    v = b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24)
+    return torch.where(v >= 1 << 31, v - (1 << 32), v).to(torch.int32)
+
+
+def e2m1_pairs(shape, g: torch.Generator) -> torch.Tensor:
+    """Bytes of two uniformly drawn E2M1 codes each (``shape`` in bytes)."""
+    lo = torch.randint(0, 16, shape, generator=g, dtype=torch.int64)
+    hi = torch.randint(0, 16, shape, generator=g, dtype=torch.int64)
+    return (lo | (hi << 4)).to(torch.uint8)
+
+
+def mx_dense_case(S_q: int, S_kv: int, H: int, *, seed: int, fp4: bool = False,
+                  ranges: str = "causal_tail", sf_lo: int = 124, sf_hi: int = 130,
+                  name: str = "mx_dense") -> MxDenseCase:
+    """MX dense case, D = 128: E4M3 elements from N(0,1) (or uniform E2M1
+    codes), block scales drawn uniformly from [sf_lo, sf_hi] (127 is one), the
+    dense ranges of ``dense_case``."""
+    g = _gen(seed)
+    D = 128
+    if fp4:
+        q, kv = e2m1_pairs((S_q, H, D // 2), g), e2m1_pairs((S_kv, D // 2), g)
+    else:
+        q, kv = e4m3_normal((S_q, H, D), g), e4m3_normal((S_kv, D), g)
+    q_sf = packed_scales((S_q, H), sf_lo, sf_hi, g)
+    kv_sf = packed_scales((S_kv,), sf_lo, sf_hi, g)
+    weights = torch.randn((S_q, H), generator=g)
+    i = torch.arange(S_q, dtype=torch.int32)
+    if ranges == "causal_tail":
+        ks, ke = torch.zeros_like(i), S_kv - S_q + i
+    elif ranges == "full":
+        ks, ke = torch.zeros_like(i), torch.full_like(i, S_kv)
+    else:
+        raise ValueError(ranges)
+    return MxDenseCase(name, q, q_sf, kv, kv_sf, weights, ks.contiguous(), ke.contiguous(), fp4, S_kv)

@@ -58,8 +58,12 @@ def _load():
                                                     i32, i64, u32, i32, i32, P, P]
             lib.oracle_paged_mqa_logits_metadata.argtypes = [P, i32, i32, i32, i32, P]
             lib.oracle_topk_indices.argtypes = [P, i64, P, P, i32, i32, u32, i32, i32, i32, P]
+            lib.oracle_e2m1_table.argtypes = [P]
+            lib.oracle_mx_mqa_logits.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i64,
+                                                 u32, i32, i32, P, P]
             for f in (lib.oracle_e4m3_table, lib.oracle_mqa_logits, lib.oracle_paged_mqa_logits,
-                      lib.oracle_paged_mqa_logits_metadata, lib.oracle_topk_indices):
+                      lib.oracle_paged_mqa_logits_metadata, lib.oracle_topk_indices,
+                      lib.oracle_e2m1_table, lib.oracle_mx_mqa_logits):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -163,6 +167,45 @@ def paged_mqa_logits_metadata(context_lens, *, next_n: int, block_kv: int, num_s
     if rc != 0:
         raise ValueError("oracle_paged_mqa_logits_metadata: invalid arguments")
     return meta
+
+
+def e2m1_table() -> np.ndarray:
+    """Value of each of the 16 E2M1 codes, decoded in double."""
+    out = np.empty(16, np.float64)
+    _load().oracle_e2m1_table(_ptr(out))
+    return out
+
+
+def mx_mqa_logits(q, q_sf, kv, kv_sf, weights, k_start, k_end, *, fp4: bool = False,
+                  ldo: Optional[int] = None, clean: bool = True, compressed: bool = False,
+                  rows: Optional[tuple] = None, out: Optional[np.ndarray] = None,
+                  with_tol: bool = False):
+    """MX (block-scaled) dense logits for rows [r0, r1); see ``mqa_oracle.c``.
+
+    q: [S_q, H, 128] E4M3 bytes, or [S_q, H, 64] packed E2M1 bytes when ``fp4``;
+    q_sf: [S_q, H] int32/uint32 (four UE8M0 bytes); kv: [S_kv, 128] or [S_kv, 64];
+    kv_sf: [S_kv]; weights [S_q, H] f32; k_start/k_end [S_q] int32.
+    """
+    qn, kvn = _np(q, np.uint8), _np(kv, np.uint8)
+    S_q, H, qb = qn.shape
+    S_kv = kvn.shape[0]
+    D = 2 * qb if fp4 else qb
+    if ldo is None:
+        ldo = S_kv
+    r0, r1 = rows if rows is not None else (0, S_q)
+    if out is None:
+        out = np.full((r1 - r0, ldo), np.nan, np.float32)
+    tol = np.zeros((r1 - r0, ldo), np.float64) if with_tol else None
+    qs = np.ascontiguousarray(_np(q_sf, np.int64).astype(np.uint32))
+    ks_ = np.ascontiguousarray(_np(kv_sf, np.int64).astype(np.uint32))
+    w = _np(weights, np.float32)
+    ks, ke = _np(k_start, np.int32), _np(k_end, np.int32)
+    rc = _load().oracle_mx_mqa_logits(_ptr(qn), _ptr(qs), _ptr(kvn), _ptr(ks_), _ptr(w), _ptr(ks),
+                                      _ptr(ke), S_q, S_kv, H, D, 1 if fp4 else 0, ldo,
+                                      _flags(clean, compressed), r0, r1, _ptr(out), _ptr(tol))
+    if rc != 0:
+        raise ValueError("oracle_mx_mqa_logits: invalid arguments")
+    return (out, tol) if with_tol else out
 
 
 def topk_indices(logits, k_start, k_end, *, topk: int, n_cols: Optional[int] = None,

@@ -417,3 +417,126 @@ int oracle_topk_indices(const float *logits, int64_t ldo, const int32_t *k_start
     free(chosen);
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * MX variant of the dense logits ("[PR #435] Improve SM100 MX MQA logits
+ * clean-output performance", sections "Performance" and "Standalone
+ * performance reproducer"): q and kv carry microscaling block scales instead
+ * of a per-key fp32 scale.  The reproducer fixes the shapes: q [S_q, H, D]
+ * elements with one int32 per (row, head) holding four UE8M0 scale bytes for
+ * D = 128, kv [S_kv, D] with one int32 per key, and 0x7f7f7f7f meaning every
+ * scale is one.  Readings this oracle takes where the pages are silent:
+ *   - a block is 32 consecutive elements of D, and byte b of the int32 (bits
+ *     8b .. 8b+7) scales block b;
+ *   - a UE8M0 byte e scales by 2^(e - 127) (e = 255 is not a number);
+ *   - MXFP8 elements are E4M3 as above; MXFP4 elements are E2M1 (1 sign, 2
+ *     exponent bits with bias 1, 1 mantissa bit), two per byte, element 2c in
+ *     the low nibble of byte c;
+ *   - the score is the same ReLU, weight and head sum with the block-scaled dot
+ *     product in place of s[j] * <q, kv>:
+ *       x = sum_b 2^(eq_b - 127) * 2^(ek_b - 127) * sum_{d in block b} q[d] kv[d].
+ * Each block's sum is exact (E4M3 or E2M1 products are integers after scaling
+ * by 2^18, 32 of them stay below 2^43), the blocks combine in double.
+ * ------------------------------------------------------------------------- */
+
+/* E2M1: value = (-1)^s * (m * 0.5) when the exponent field is 0, else
+ * (-1)^s * 2^(e - 1) * (1 + m / 2). */
+static double e2m1_decode(unsigned code)
+{
+    int sign = (code >> 3) & 1;
+    int expo = (code >> 1) & 3;
+    int mant = code & 1;
+    double mag = expo == 0 ? 0.5 * mant : ldexp(1.0 + 0.5 * mant, expo - 1);
+    return sign ? -mag : mag;
+}
+
+int oracle_e2m1_table(double *out16)
+{
+    for (unsigned c = 0; c < 16; ++c)
+        out16[c] = e2m1_decode(c);
+    return 0;
+}
+
+/* Element d of a row of D elements: E4M3 byte d, or nibble d of the packed
+ * E2M1 bytes (low nibble first). */
+static double mx_element(const uint8_t *row, int d, int fp4)
+{
+    if (!fp4)
+        return table()[row[d]];
+    uint8_t byte = row[d / 2];
+    return e2m1_decode((d & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 0xF));
+}
+
+/* Block-scaled dot product of a query row and a key row (D elements each). */
+static double mx_dot(const uint8_t *qrow, uint32_t qsf, const uint8_t *krow, uint32_t ksf, int D,
+                     int fp4)
+{
+    double x = 0.0;
+    for (int b = 0; b < D / 32; ++b) {
+        int64_t acc = 0; /* block sum, in units of 2^-18 */
+        for (int d = 32 * b; d < 32 * b + 32; ++d)
+            acc += (int64_t)llround(ldexp(mx_element(qrow, d, fp4), 9)) *
+                   (int64_t)llround(ldexp(mx_element(krow, d, fp4), 9));
+        int eq = (int)((qsf >> (8 * b)) & 0xFF), ek = (int)((ksf >> (8 * b)) & 0xFF);
+        if (eq == 255 || ek == 255)
+            return NAN;
+        x += ldexp((double)acc, eq + ek - 254 - 18);
+    }
+    return x;
+}
+
+/*
+ * MX dense logits for rows [row_begin, row_end); layout and flags as
+ * oracle_mqa_logits.
+ *   q     [S_q, H, D] E4M3 bytes, or [S_q, H, D/2] packed E2M1 when fp4
+ *   q_sf  [S_q, H] uint32, four UE8M0 block scales each
+ *   kv    [S_kv, D] E4M3 bytes, or [S_kv, D/2] packed E2M1 when fp4
+ *   kv_sf [S_kv] uint32
+ * D must be 128 (four blocks).  tol receives 1e-3 * sum_h |w x| + 1e-5.
+ */
+int oracle_mx_mqa_logits(const uint8_t *q, const uint32_t *q_sf, const uint8_t *kv,
+                         const uint32_t *kv_sf, const float *weights, const int32_t *k_start,
+                         const int32_t *k_end, int S_q, int S_kv, int H, int D, int fp4,
+                         int64_t ldo, unsigned flags, int row_begin, int row_end, float *logits,
+                         double *tol)
+{
+    int clean = (flags & ORACLE_CLEAN) != 0;
+    int compressed = (flags & ORACLE_COMPRESSED) != 0;
+    if (S_q < 0 || S_kv < 0 || H <= 0 || D != 128 || row_begin < 0 || row_end > S_q ||
+        row_begin > row_end || (!compressed && ldo < S_kv) || (compressed && ldo < 0))
+        return -1;
+    const size_t row_bytes = (size_t)(fp4 ? D / 2 : D);
+    for (int i = row_begin; i < row_end; ++i) {
+        float *out = logits + (size_t)(i - row_begin) * (size_t)ldo;
+        double *tout = tol ? tol + (size_t)(i - row_begin) * (size_t)ldo : NULL;
+        int lo = k_start[i] < 0 ? 0 : k_start[i];
+        int hi = k_end[i] > S_kv ? S_kv : k_end[i];
+        if (hi < lo)
+            hi = lo;
+        if (compressed && (int64_t)(hi - lo) > ldo)
+            return -1;
+        int64_t width = compressed ? ldo : S_kv;
+        for (int64_t c = 0; c < width; ++c) {
+            int j = compressed ? (int)(lo + c) : (int)c;
+            int valid = compressed ? (c < hi - lo) : (j >= lo && j < hi);
+            if (valid) {
+                double sum = 0.0, asum = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    double x = mx_dot(q + ((size_t)i * H + h) * row_bytes, q_sf[(size_t)i * H + h],
+                                      kv + (size_t)j * row_bytes, kv_sf[j], D, fp4);
+                    double w = (double)weights[(size_t)i * H + h];
+                    sum += w * (x > 0.0 ? x : 0.0);
+                    asum += fabs(w * x);
+                }
+                out[c] = (float)sum;
+                if (tout)
+                    tout[c] = 1e-3 * asum + 1e-5;
+            } else if (clean) {
+                out[c] = -INFINITY;
+                if (tout)
+                    tout[c] = 0.0;
+            }
+        }
+    }
+    return 0;
+}
