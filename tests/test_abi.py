@@ -156,3 +156,11 @@ def test_paged_topk_rejects_invalid_arguments(lib, kw, status):
 
 def test_paged_topk_zero_batch_is_a_no_op(lib):
     assert call_paged_topk(lib, B=0, logits=None) == 0
+
+
+def test_valid_topk_call_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU suite")
+    assert call_topk(lib) == 3
+    assert call_paged_topk(lib) == 3
