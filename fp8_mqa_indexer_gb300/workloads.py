@@ -15,7 +15,11 @@ The shapes and distributions follow the workloads the pages describe:
     8192/65536, each row using [0, KV - Q + row));
   * paged decode as in the article's "Implementing Paged MQA Logits Computation
     for Decoding" with next_n and 64-token blocks as in "[PR #314] fix: SM90
-    paged MQA logits IMA on next_n=4".
+    paged MQA logits IMA on next_n=4";
+  * logits-shaped rows for the top-k key selection (N(0,1) values, -inf
+    outside each row's range), sized like the 2048 x 32768 dense output;
+  * MX inputs (E4M3 or packed E2M1 elements, UE8M0 block scales packed four
+    to an int32) with the shapes of the PR #435 reproducer.
 The datasets behind those numbers are not public inputs; these synthetic
 tensors stand in for them.
 """
