@@ -164,3 +164,20 @@ def test_valid_topk_call_without_gpu_fails_cleanly(lib):
         pytest.skip("a GPU is present; covered by the GPU suite")
     assert call_topk(lib) == 3
     assert call_paged_topk(lib) == 3
+
+
+def test_binding_signatures_match_the_header():
+    """Every declared call has a ctypes signature in the binding with the same
+    number of parameters (a drift between the two would shift arguments)."""
+    import inspect
+    text = open(HEADER).read()
+    decls = {}
+    for m in re.finditer(r"MQA_API\s+[\w\s\*]+?\b(\w+)\s*\(([^)]*)\)", text):
+        params = [p for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        decls[m.group(1)] = len(params)
+    src = inspect.getsource(mqa.load_library)
+    sig = dict(re.findall(r'"(\w+)": \(\[([^\]]*)\]', src))
+    for name, n in decls.items():
+        assert name in sig, f"{name} has no ctypes signature in the binding"
+        got = len([a for a in sig[name].split(",") if a.strip()])
+        assert got == n, f"{name}: header has {n} parameters, binding {got}"
