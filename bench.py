@@ -125,6 +125,104 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def percentiles(times_ms):
+    xs = sorted(times_ms)
+
+    def q(f):
+        k = (len(xs) - 1) * f
+        lo, hi = int(k), min(int(k) + 1, len(xs) - 1)
+        return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+    return {"median_ms": q(0.5), "p10_ms": q(0.1), "p90_ms": q(0.9)}
+
+
+# Dense E4M3 tensor-core work per SM and SM clock: one 128 x 256 x 128 MMA
+# unit (8.4 MFLOP) issues every 512 cycles when nothing else limits it (an
+# MMA-only issue loop on this GPU); used for the fraction at the kernel's own
+# clock.
+FP8_FLOP_PER_SM_CLK = 16384
+
+
+def measure_fp8_peak(torch, dev, seconds: float = 4.0, n: int = 8192):
+    """Dense FP8 (E4M3 x E4M3, fp32 accumulate) GEMM rate of this GPU through
+    cuBLAS (torch._scaled_mm, bf16 out) at n^3: best of 10 (burst) and back to
+    back for `seconds` (sustained), with the SM clocks sampled meanwhile."""
+    g = torch.Generator(device=dev).manual_seed(7)
+    a = torch.randn((n, n), device=dev, generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn((n, n), device=dev, generator=g).to(torch.float8_e4m3fn).t()
+    one = torch.ones((), device=dev, dtype=torch.float32)
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    flop = 2.0 * n ** 3
+    for _ in range(3):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[0].strip() if vis else str(dev.index or 0))
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    iters = 0
+    t0 = time.perf_counter()
+    e0.record()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(20):
+            mm()
+        iters += 20
+        torch.cuda.synchronize()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    sustained = flop * iters / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    del a, b
+    return {"burst_tflops": flop / (best * 1e-3) / 1e12, "sustained_tflops": sustained,
+            "sustained_sm_mhz": clocks.get("sm_mhz"), "sustained_reasons": clocks.get("reasons"),
+            "how": f"torch._scaled_mm e4m3 x e4m3 -> bf16, {n}^3 (2*n^3 FLOP): best of 10 (burst) "
+                   f"and back to back for {seconds:.0f} s (sustained)"}
+
+
+def graph_timing(torch, call, out, calls: int = 5, samples: int = 40):
+    """Timing in the manner of the PR #435 reproducer: one CUDA graph holding
+    `calls` calls, each writing its own output buffer, replayed `samples`
+    times; per-call time of every replay (CUDA events) -> median, p10, p90."""
+    outs = [out] + [torch.empty_like(out) for _ in range(calls - 1)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for o in outs:
+            call(o)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for o in outs:
+            call(o)
+    graph.replay()
+    torch.cuda.synchronize()
+    per_call = []
+    for _ in range(samples):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        per_call.append(e0.elapsed_time(e1) / calls)
+    del graph, outs
+    r = percentiles(per_call)
+    r.update({"calls_per_graph": calls, "samples": samples,
+              "note": "no L2 flush between calls; each call writes its own output buffer"})
+    return r
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -138,6 +236,9 @@ def make_case(workload: str):
         return wl.topk_config(workload)
     if workload in wl.PAGED_CONFIGS:
         return wl.paged_config(workload)
+    if workload not in wl.DENSE_CONFIGS:
+        raise SystemExit(f"unknown workload {workload!r}; known: "
+                         f"{sorted(wl.DENSE_CONFIGS) + sorted(wl.PAGED_CONFIGS) + sorted(wl.TOPK_CONFIGS)}")
     return wl.dense_config(workload)
 
 
@@ -243,7 +344,7 @@ def bench_topk(args, mqa, torch, dev, stream):
                    "in_range_logits": valid,
                    "l2": "flushed (256 MiB write) before every timed step; the logits exceed L2",
                    "step": "mqa_topk_indices"},
-        "median_ms": statistics.median(times_ms),
+        **percentiles(times_ms),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": recorded_traffic(args.workload, TOPK_SOURCES),
@@ -361,6 +462,15 @@ def bench_paged(args, mqa, torch, dev, stream):
     torch.cuda.synchronize()
     e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
 
+    graph = None
+    if not args.no_graph:
+        def call(o):
+            mqa.paged_mqa_logits_metadata(cl, next_n=case.next_n, block_kv=case.block_kv, out=meta)
+            mqa.paged_mqa_logits(q, kvc, sc, w, cl, bt, meta, o, next_n=case.next_n, clean=case.clean)
+        graph = graph_timing(torch, call, out)
+        graph["gbs_at_median"] = alg_bytes / (graph["median_ms"] * 1e-3) / 1e9
+    assert mqa.device_status() == 0
+
     peaks, peaks_src = load_peaks()
     achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
     line = {
@@ -374,9 +484,11 @@ def bench_paged(args, mqa, torch, dev, stream):
                    "ldo": case.ldo, "valid_logits": valid, "clean": case.clean,
                    "l2": "flushed (256 MiB write) before every timed step; the pool exceeds L2",
                    "step": "paged_mqa_logits_metadata + paged_mqa_logits"},
-        "median_ms": statistics.median(times_ms),
+        **percentiles(times_ms),
+        "graph_timing": graph,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic(args.workload),
                      "algorithmic_bytes": alg_bytes, "peak_source": f"{peaks_src} HBM copy"},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": host_out.numel() * 4,
@@ -491,6 +603,72 @@ def run_reference_topk(args):
     return 0
 
 
+def case_bytes(case) -> int:
+    """Algorithmic bytes of a dense call: output, q, kv, scales, weights and
+    ranges, each once."""
+    return (case.S_q * case.ldo * 4 + case.q.numel() + case.kv.numel() + case.kv_scale.numel() * 4
+            + case.weights.numel() * 4 + case.S_q * 8)
+
+
+def e2e_dense_pipelined(args, mqa, torch, dev, case, out, n_chunks: int = 8):
+    """Per step: copy the inputs from pinned host memory, compute, copy the
+    logits back, with the rows cut into chunks so that the two copy directions
+    and the kernel overlap.  Returns (ms per step, h2d bytes, d2h bytes, chunks)."""
+    host = {k: v.pin_memory() for k, v in dict(q=case.q, kv=case.kv, s=case.kv_scale, w=case.weights,
+                                                ks=case.k_start, ke=case.k_end).items()}
+    host_out = torch.empty((case.S_q, case.ldo), dtype=torch.float32, pin_memory=True)
+    dv = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    tok = max(1, 256 // case.H)
+    per = -(-case.S_q // n_chunks)
+    per = -(-per // tok) * tok
+    bounds = [(a, min(case.S_q, a + per)) for a in range(0, case.S_q, per)]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def step():
+        start = torch.cuda.Event()
+        start.record(comp)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        with torch.cuda.stream(s_in):
+            for k in ("kv", "s"):
+                dv[k].copy_(host[k], non_blocking=True)
+            ev_in = []
+            for a, b in bounds:
+                for k in ("q", "w", "ks", "ke"):
+                    dv[k][a:b].copy_(host[k][a:b], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_in)
+                ev_in.append(e)
+        ev_out = []
+        for (a, b), e in zip(bounds, ev_in):
+            comp.wait_event(e)
+            mqa.mqa_logits(dv["q"][a:b], dv["kv"], dv["s"], dv["w"][a:b], dv["ks"][a:b],
+                           dv["ke"][a:b], out[a:b], clean=case.clean, compressed=case.compressed,
+                           ldo=case.ldo, stream=comp)
+            e2 = torch.cuda.Event()
+            e2.record(comp)
+            ev_out.append(e2)
+        with torch.cuda.stream(s_out):
+            for (a, b), e in zip(bounds, ev_out):
+                s_out.wait_event(e)
+                host_out[a:b].copy_(out[a:b], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        comp.wait_event(done)
+
+    step()
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(comp)
+    for _ in range(args.e2e_steps):
+        step()
+    eb.record(comp)
+    torch.cuda.synchronize()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    return ea.elapsed_time(eb) / args.e2e_steps, h2d, host_out.numel() * 4, len(bounds)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -503,6 +681,10 @@ def main():
                     help="oracle seconds per reference step (default: about 90 s in all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph timing (5 calls per graph, 40 replays)")
+    ap.add_argument("--no-fp8-peak", action="store_true",
+                    help="skip the live cuBLAS FP8 peak measurement (use bf16 x 2)")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -582,36 +764,22 @@ def main():
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = flops * world / (ms_per_step * 1e-3) / 1e12
-    median_ms = statistics.median(times_ms)
 
-    # end to end through the public call: pinned host inputs in, logits out
-    host = {k: v.pin_memory() for k, v in dict(q=case.q, kv=case.kv, s=case.kv_scale, w=case.weights,
-                                                ks=case.k_start, ke=case.k_end).items()}
-    host_out = torch.empty((case.S_q, case.ldo), dtype=torch.float32, pin_memory=True)
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = host_out.numel() * 4
-
-    def e2e_step():
-        dq = host["q"].to(dev, non_blocking=True)
-        dkv = host["kv"].to(dev, non_blocking=True)
-        ds = host["s"].to(dev, non_blocking=True)
-        dw = host["w"].to(dev, non_blocking=True)
-        dks = host["ks"].to(dev, non_blocking=True)
-        dke = host["ke"].to(dev, non_blocking=True)
-        mqa.mqa_logits(dq, dkv, ds, dw, dks, dke, out, clean=case.clean,
-                       compressed=case.compressed, ldo=case.ldo)
-        host_out.copy_(out, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ea.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    eb.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+    # End to end through the public call, from pinned host buffers: the rows
+    # are cut into chunks whose host->device copies, mqa_logits calls and
+    # device->host copies of the logits run on three streams, so that copies in
+    # both directions overlap the kernel (the keys and their scales go first;
+    # every chunk's call needs them).
+    e2e_ms, h2d, d2h, n_chunks = e2e_dense_pipelined(args, mqa, torch, dev, case, out)
     e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    graph = None
+    if not args.no_graph:
+        graph = graph_timing(torch, lambda o: mqa.mqa_logits(q, kv, s, w, ks, ke, o, clean=case.clean,
+                                                             compressed=case.compressed,
+                                                             ldo=case.ldo), out)
+        graph["tflops_at_median"] = flops / (graph["median_ms"] * 1e-3) / 1e12
+    assert mqa.device_status() == 0
 
     if rank != 0:
         if pg:
@@ -619,9 +787,14 @@ def main():
         return 0
 
     peaks, peaks_src = load_peaks()
-    peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    nominal_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    fp8 = None if args.no_fp8_peak else measure_fp8_peak(torch, dev)
+    peak = fp8["burst_tflops"] if fp8 else nominal_peak
     achieved = flops / (ms_per_step * 1e-3) / 1e12
     traffic = recorded_traffic(args.workload)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    at_clock = (FP8_FLOP_PER_SM_CLK * n_sm * clocks["sm_mhz"] * 1e6 / 1e12
+                if clocks.get("sm_mhz") else None)
     line = {
         "metric": "MQA logits TFLOP/s (valid logits x 2*H*D)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -634,12 +807,23 @@ def main():
                    "l2": "flushed (256 MiB write) before every timed step",
                    "parallelism": f"replicas x{world} (independent rows, no collective)"},
         "valid_logits_per_s": valid * world / (ms_per_step * 1e-3),
-        "median_ms": median_ms,
+        **percentiles(times_ms),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peaks_src} bf16 burst x {FP8_PER_BF16} (nominal fp8:bf16)"},
+                     "algorithmic_bytes": case_bytes(case),
+                     "peak_source": ("measured fp8 (cuBLAS e4m3 GEMM burst on this GPU)" if fp8 else
+                                     f"{peaks_src} bf16 burst x {FP8_PER_BF16} (nominal fp8:bf16)"),
+                     "peak_bf16x2": nominal_peak, "frac_bf16x2": achieved / nominal_peak,
+                     "peak_at_kernel_clock": at_clock,
+                     "frac_at_kernel_clock": achieved / at_clock if at_clock else None,
+                     "at_clock_basis": f"{FP8_FLOP_PER_SM_CLK} FLOP per SM per cycle x {n_sm} SMs x "
+                                       "median SM clock of the timed region"},
+        "fp8_peak": fp8,
+        "graph_timing": graph,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "how": f"pinned host buffers, {n_chunks} row chunks, copies in both directions "
+                       "overlapping the calls on three streams"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }

@@ -193,6 +193,60 @@ def paged_mqa_logits_metadata(context_lens, *, next_n: int, block_kv: int,
     return out
 
 
+def _paged_inputs(q, kv_cache, kv_scales, weights, context_lens, block_table, next_n):
+    """Type and shape checks shared by the two paged calls; returns
+    (R, H, D, B, next_n, num_blocks, block_kv, max_blocks)."""
+    import torch
+    f8 = _fp8_types()
+    _dev(q, "q", f8)
+    _dev(kv_cache, "kv_cache", f8)
+    _dev(kv_scales, "kv_scales", (torch.float32,))
+    _dev(weights, "weights", (torch.float32,))
+    _dev(context_lens, "context_lens", (torch.int32,))
+    _dev(block_table, "block_table", (torch.int32,))
+    return paged_shapes(tuple(q.shape), tuple(kv_cache.shape), tuple(kv_scales.shape),
+                        tuple(weights.shape), tuple(context_lens.shape), tuple(block_table.shape),
+                        next_n)
+
+
+def paged_shapes(q, kv_cache, kv_scales, weights, context_lens, block_table, next_n=None):
+    """Shape rules of a paged call, on shape tuples alone (no tensors, no GPU).
+
+    Returns (R, H, D, B, next_n, num_blocks, block_kv, max_blocks) or raises
+    ValueError: q [B*next_n, H, D], kv_cache [num_blocks, block_kv, D],
+    kv_scales [num_blocks, block_kv], weights [B*next_n, H], context_lens [B],
+    block_table [B, max_blocks].  next_n is inferred from q and context_lens
+    when not given.
+    """
+    if len(q) != 3 or len(kv_cache) != 3 or len(block_table) != 2 or len(context_lens) != 1:
+        raise ValueError("q and kv_cache must be 3-D, block_table 2-D, context_lens 1-D")
+    R, H, D = q
+    B = context_lens[0]
+    if next_n is None:
+        if B == 0 or R % B:
+            raise ValueError("cannot infer next_n from q and context_lens")
+        next_n = R // B
+    num_blocks, block_kv, D2 = kv_cache
+    if D2 != D or R != B * next_n or tuple(weights) != (R, H) or \
+            tuple(kv_scales) != (num_blocks, block_kv):
+        raise ValueError("shape mismatch between paged inputs (q rows must be B * next_n)")
+    if block_table[0] != B:
+        raise ValueError("block_table must have one row per sequence")
+    return R, H, D, B, next_n, num_blocks, block_kv, block_table[1]
+
+
+def _paged_logits_out(logits, R, width, device):
+    import torch
+    if logits is None:
+        return torch.empty((R, width), dtype=torch.float32, device=device)
+    if not (isinstance(logits, torch.Tensor) and logits.is_cuda and logits.dtype == torch.float32
+            and logits.dim() == 2 and logits.stride(1) == 1 and logits.shape[0] == R
+            and logits.shape[1] >= width):
+        raise ValueError("logits must be a CUDA float32 [B*next_n, >= max_blocks_per_seq*block_kv] "
+                         "matrix with unit column stride")
+    return logits
+
+
 def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table, schedule_meta,
                      logits=None, *, next_n: Optional[int] = None, clean: bool = True,
                      check_bounds: bool = False, stream=None):
@@ -205,69 +259,41 @@ def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
     ldo >= max_blocks_per_seq * block_kv.
     """
     import torch
-    f8 = _fp8_types()
-    _dev(q, "q", f8)
-    _dev(kv_cache, "kv_cache", f8)
-    _dev(kv_scales, "kv_scales", (torch.float32,))
-    _dev(weights, "weights", (torch.float32,))
-    _dev(context_lens, "context_lens", (torch.int32,))
-    _dev(block_table, "block_table", (torch.int32,))
+    R, H, D, B, next_n, num_blocks, block_kv, max_blocks = _paged_inputs(
+        q, kv_cache, kv_scales, weights, context_lens, block_table, next_n)
     _dev(schedule_meta, "schedule_meta", (torch.int32,))
-    R, H, D = q.shape
-    B = context_lens.shape[0]
-    if next_n is None:
-        if B == 0 or R % B:
-            raise ValueError("cannot infer next_n from q and context_lens")
-        next_n = R // B
-    num_blocks, block_kv, D2 = kv_cache.shape
-    max_blocks = block_table.shape[1]
-    if D2 != D or R != B * next_n or weights.shape != (R, H) or kv_scales.shape != (num_blocks, block_kv):
-        raise ValueError("shape mismatch between paged inputs")
-    if block_table.shape[0] != B:
-        raise ValueError("block_table must have one row per sequence")
+    if schedule_meta.dim() != 2 or schedule_meta.shape[1] != 2:
+        raise ValueError("schedule_meta must be an int32 [num_sms + 1, 2] tensor")
     num_sms = schedule_meta.shape[0] - 1
-    width = max_blocks * block_kv
-    if logits is None:
-        logits = torch.empty((R, width), dtype=torch.float32, device=q.device)
-    elif not (logits.dtype == torch.float32 and logits.dim() == 2 and logits.stride(1) == 1
-              and logits.shape[0] == R):
-        raise ValueError("logits must be a float32 [B*next_n, ldo] matrix with unit column stride")
-    ldo = logits.stride(0)
+    logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0)
     with torch.cuda.device(q.device):
         _check(load_library().paged_mqa_logits(_ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights),
                                                _ptr(context_lens), _ptr(block_table), max_blocks,
                                                _ptr(schedule_meta), _ptr(logits), B, next_n, H, D,
-                                               block_kv, num_blocks, num_sms, ldo, flags,
+                                               block_kv, num_blocks, num_sms, logits.stride(0), flags,
                                                _stream_handle(stream)))
     return logits
 
 
 def paged_mqa_logits_noalloc(q, kv_cache, kv_scales, weights, context_lens, block_table,
-                             logits, *, next_n: int, clean: bool = True,
+                             logits, *, next_n: Optional[int] = None, clean: bool = True,
                              check_bounds: bool = False, stream=None):
     """Paged decode MQA logits with the work schedule kept in the library's own
     fixed device array (C ABI ``paged_mqa_logits_noalloc``): no schedule buffer
-    and no allocation.  ``logits`` must be given ([B*next_n, ldo] float32)."""
+    and no allocation.  ``logits`` must be given ([B*next_n, ldo] float32);
+    the inputs are checked exactly as for ``paged_mqa_logits``."""
     import torch
-    f8 = _fp8_types()
-    _dev(q, "q", f8)
-    _dev(kv_cache, "kv_cache", f8)
-    _dev(kv_scales, "kv_scales", (torch.float32,))
-    _dev(weights, "weights", (torch.float32,))
-    _dev(context_lens, "context_lens", (torch.int32,))
-    _dev(block_table, "block_table", (torch.int32,))
-    R, H, D = q.shape
-    B = context_lens.shape[0]
-    num_blocks, block_kv, _ = kv_cache.shape
-    if not (logits.is_cuda and logits.dtype == torch.float32 and logits.dim() == 2
-            and logits.stride(1) == 1 and logits.shape[0] == R):
-        raise ValueError("logits must be a CUDA float32 [B*next_n, ldo] matrix with unit column stride")
+    R, H, D, B, next_n, num_blocks, block_kv, max_blocks = _paged_inputs(
+        q, kv_cache, kv_scales, weights, context_lens, block_table, next_n)
+    if logits is None:
+        raise ValueError("paged_mqa_logits_noalloc needs a caller-provided logits buffer")
+    logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0)
     with torch.cuda.device(q.device):
         _check(load_library().paged_mqa_logits_noalloc(
             _ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights), _ptr(context_lens),
-            _ptr(block_table), block_table.shape[1], _ptr(logits), B, next_n, H, D, block_kv,
+            _ptr(block_table), max_blocks, _ptr(logits), B, next_n, H, D, block_kv,
             num_blocks, logits.stride(0), flags, _stream_handle(stream)))
     return logits
 

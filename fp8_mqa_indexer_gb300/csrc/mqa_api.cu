@@ -382,6 +382,8 @@ mqa_status paged_mqa_logits_metadata(const int32_t* context_lens, int B, int nex
         return fail(MQA_ERR_UNSUPPORTED, "block_kv must be 32, 64 or 128 (got %d)", block_kv);
     if (!schedule_meta || (B > 0 && !context_lens))
         return fail(MQA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(schedule_meta, 4) || (B > 0 && !aligned(context_lens, 4)))
+        return fail(MQA_ERR_INVALID_ARG, "context_lens and schedule_meta must be 4-byte aligned");
     int dev;
     unsigned* st;
     mqa_status s = device_state(&dev, &st);
@@ -499,14 +501,24 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
     return MQA_OK;
 }
 
-mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv_scales,
-                            const float* weights, const int32_t* context_lens,
-                            const int32_t* block_table, int max_blocks_per_seq,
-                            const int32_t* schedule_meta, float* logits, int B, int next_n, int H,
-                            int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
-                            unsigned flags, mqa_stream_t stream_)
+namespace {
+// Host-side checks of a paged call, shared by paged_mqa_logits and
+// paged_mqa_logits_noalloc (which runs them before it writes its schedule).
+// Sets *nothing_to_do for B == 0.
+mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_scales,
+                          const float* weights, const int32_t* context_lens,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* schedule_meta, const float* logits, int B, int next_n,
+                          int H, int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
+                          unsigned flags, bool own_schedule, bool* nothing_to_do)
 {
-    cudaStream_t stream = (cudaStream_t)stream_;
+    // own_schedule: the call keeps the schedule itself (no schedule_meta or
+    // num_sms from the caller to check)
+    if (own_schedule) {
+        schedule_meta = context_lens;
+        num_sms = 1;
+    }
+    *nothing_to_do = false;
     if (flags & ~(unsigned)(MQA_CLEAN | MQA_CHECK_BOUNDS))
         return fail((flags & MQA_COMPRESSED) ? MQA_ERR_UNSUPPORTED : MQA_ERR_INVALID_ARG,
                     "paged logits take only MQA_CLEAN and MQA_CHECK_BOUNDS (flags 0x%x)", flags);
@@ -528,8 +540,10 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     if (width > INT_MAX - 256 || (long long)num_blocks * block_kv >= INT_MAX ||
         (long long)B * next_n * H >= INT_MAX)
         return fail(MQA_ERR_INVALID_ARG, "size too large");
-    if (B == 0)
+    if (B == 0) {
+        *nothing_to_do = true;
         return MQA_OK;
+    }
     if (!q || !kv_cache || !kv_scales || !weights || !context_lens || !block_table ||
         !schedule_meta || !logits)
         return fail(MQA_ERR_INVALID_ARG, "null pointer");
@@ -539,6 +553,25 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     if (!aligned(logits, 4) || !aligned(context_lens, 4) || !aligned(block_table, 4) ||
         !aligned(schedule_meta, 4))
         return fail(MQA_ERR_INVALID_ARG, "int and float arrays must be 4-byte aligned");
+    return MQA_OK;
+}
+}  // namespace
+
+mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv_scales,
+                            const float* weights, const int32_t* context_lens,
+                            const int32_t* block_table, int max_blocks_per_seq,
+                            const int32_t* schedule_meta, float* logits, int B, int next_n, int H,
+                            int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
+                            unsigned flags, mqa_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    bool nothing = false;
+    mqa_status v0 = validate_paged(q, kv_cache, kv_scales, weights, context_lens, block_table,
+                                   max_blocks_per_seq, schedule_meta, logits, B, next_n, H, D,
+                                   block_kv, num_blocks, num_sms, ldo, flags, false, &nothing);
+    if (v0 != MQA_OK || nothing)
+        return v0;
+    const long long width = (long long)max_blocks_per_seq * block_kv;
 
     int dev;
     unsigned* st;
@@ -628,9 +661,17 @@ mqa_status paged_mqa_logits_noalloc(const void* q, const void* kv_cache, const f
                                     int num_blocks, int64_t ldo, unsigned flags,
                                     mqa_stream_t stream)
 {
+    // every host-side check runs before the first CUDA call and before the
+    // shared schedule array is touched
+    bool nothing = false;
+    mqa_status s = validate_paged(q, kv_cache, kv_scales, weights, context_lens, block_table,
+                                  max_blocks_per_seq, nullptr, logits, B, next_n, H, D, block_kv,
+                                  num_blocks, 0, ldo, flags, true, &nothing);
+    if (s != MQA_OK || nothing)
+        return s;
     int dev;
     unsigned* st;
-    mqa_status s = device_state(&dev, &st);
+    s = device_state(&dev, &st);
     if (s != MQA_OK)
         return s;
     const int num_sms = g_num_sms[dev];

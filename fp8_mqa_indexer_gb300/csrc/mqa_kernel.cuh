@@ -790,12 +790,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 first = true;
             }
         }
-        // Drain: every copy this warp issued must have landed before exit.
+        // Drain: every copy this warp issued must have landed before exit,
+        // also when some role gave up (wait_drain ignores the abort flag).
         if (lane == 0) {
             for (int u = max(0, n_issued - S); u < n_issued; ++u)
-                wait_bounded(smem_u32(&sm.full[u % S]), (u / S) & 1, wctx);
+                wait_drain(smem_u32(&sm.full[u % S]), (u / S) & 1, wctx);
             for (int k = max(0, q_issued - 2); k < q_issued; ++k)
-                wait_bounded(smem_u32(&sm.q_full[k & 1]), (k >> 1) & 1, wctx);
+                wait_drain(smem_u32(&sm.q_full[k & 1]), (k >> 1) & 1, wctx);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -834,9 +835,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (info.flags & kLastOfBlock)
                     mma_commit(smem_u32(&sm.q_empty[info.qbuf]));
             }
-            // every MMA issued above has completed once this barrier flips
+            // every MMA issued above has completed once this barrier flips;
+            // waited for even after an abort, before TMEM is freed
             mma_commit(smem_u32(&sm.mma_done));
-            wait_bounded(smem_u32(&sm.mma_done), 0, wctx);
+            wait_drain(smem_u32(&sm.mma_done), 0, wctx);
         }
         __syncwarp();
     } else if (warp < kEpiWarp0) {

@@ -129,13 +129,45 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     }
 }
 
+// Cycle budget of a drain wait: at least 2^30 cycles (about half a second),
+// whatever budget the pipeline waits were given.
+__device__ __forceinline__ long long drain_limit(const WaitCtx& w)
+{
+    return w.limit > (1ll << 30) ? w.limit : (1ll << 30);
+}
+
+// Wait for an asynchronous operation this thread issued itself (a TMA copy, a
+// tcgen05 MMA) to complete, before the CTA frees the shared memory or TMEM it
+// targets.  Its completion depends on no other role of the CTA, so the abort
+// flag is ignored: after another role has given up, the operations already in
+// flight must still land.  Bounded by drain_limit(); running out records
+// kDevErrTimeout.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const WaitCtx& w)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    const long long limit = drain_limit(w);
+    for (unsigned n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((n & 15) == 0 && clock64() - t0 > limit) {
+            *w.abort_flag = 1;
+            atomicOr(w.status, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+
 // The same wait taken by a whole warp, shaped for the hot path: the whole
 // loop is one PTX block whose branches are uniform (each try_wait answer is
 // voted across the warp), so the compiler adds no convergence bookkeeping
-// around it, and no shared load sits in the polling loop.  Polling stops when
-// the phase completes or the cycle budget is spent; a timeout records
-// kDevErrTimeout, raises the CTA's abort flag (which stops the waits of the
-// other roles) and returns false.  Every lane gets the same answer.
+// around it.  Polling stops when the phase completes, when the cycle budget is
+// spent, or when another role of the CTA has raised the abort flag (read every
+// eighth poll, so a shared load sits in the loop only while it waits).  A
+// timeout records kDevErrTimeout and raises the abort flag, which stops the
+// waits of the other roles; both failures return false.  Every lane gets the
+// same answer.
 __device__ __forceinline__ bool warp_wait_fast(uint32_t bar, uint32_t parity, const WaitCtx& w)
 {
     uint32_t ok;
@@ -143,18 +175,31 @@ __device__ __forceinline__ bool warp_wait_fast(uint32_t bar, uint32_t parity, co
         "{\n\t"
         ".reg .pred p;\n\t"
         ".reg .u64 t0, t1;\n\t"
+        ".reg .u32 n, f;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "vote.sync.all.pred p, p, 0xffffffff;\n\t"
         "@p bra.uni W_DONE;\n\t"
         "mov.u64 t0, %%clock64;\n\t"
+        "mov.u32 n, 0;\n\t"
         "W_LOOP:\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "vote.sync.all.pred p, p, 0xffffffff;\n\t"
         "@p bra.uni W_DONE;\n\t"
         "mov.u64 t1, %%clock64;\n\t"
         "sub.s64 t1, t1, t0;\n\t"
-        "setp.lt.s64 p, t1, %3;\n\t"
+        "setp.ge.s64 p, t1, %3;\n\t"
+        "@p bra.uni W_TIMEOUT;\n\t"
+        "add.u32 n, n, 1;\n\t"
+        "and.b32 f, n, 7;\n\t"
+        "setp.ne.u32 p, f, 0;\n\t"
         "@p bra.uni W_LOOP;\n\t"
+        "ld.volatile.shared.u32 f, [%4];\n\t"
+        "setp.ne.u32 p, f, 0;\n\t"
+        "vote.sync.any.pred p, p, 0xffffffff;\n\t"
+        "@!p bra.uni W_LOOP;\n\t"
+        "mov.u32 %0, 2;\n\t"
+        "bra.uni W_END;\n\t"
+        "W_TIMEOUT:\n\t"
         "mov.u32 %0, 0;\n\t"
         "bra.uni W_END;\n\t"
         "W_DONE:\n\t"
@@ -162,12 +207,14 @@ __device__ __forceinline__ bool warp_wait_fast(uint32_t bar, uint32_t parity, co
         "W_END:\n\t"
         "}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "l"(w.limit)
+        : "r"(bar), "r"(parity), "l"(w.limit), "r"(smem_u32((const void*)w.abort_flag))
         : "memory");
-    if (ok)
+    if (ok == 1)
         return true;
-    *w.abort_flag = 1;
-    atomicOr(w.status, kDevErrTimeout);
+    if (ok == 0) {
+        *w.abort_flag = 1;
+        atomicOr(w.status, kDevErrTimeout);
+    }
     return false;
 }
 

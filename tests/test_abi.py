@@ -181,3 +181,37 @@ def test_binding_signatures_match_the_header():
         assert name in sig, f"{name} has no ctypes signature in the binding"
         got = len([a for a in sig[name].split(",") if a.strip()])
         assert got == n, f"{name}: header has {n} parameters, binding {got}"
+
+
+def call_noalloc(lib, **kw):
+    a = dict(q=F, kv_cache=F, kv_scales=F, weights=F, context_lens=F, block_table=F, max_blocks=16,
+             logits=F, B=2, next_n=2, H=64, D=128, block_kv=64, num_blocks=40, ldo=1024, flags=1,
+             stream=None)
+    a.update(kw)
+    return lib.paged_mqa_logits_noalloc(a["q"], a["kv_cache"], a["kv_scales"], a["weights"],
+                                        a["context_lens"], a["block_table"], a["max_blocks"],
+                                        a["logits"], a["B"], a["next_n"], a["H"], a["D"],
+                                        a["block_kv"], a["num_blocks"], a["ldo"], a["flags"],
+                                        a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=2), 2), (dict(flags=8), 1), (dict(D=32), 2), (dict(H=8), 2),
+    (dict(block_kv=16), 2), (dict(ldo=1000), 1), (dict(next_n=0), 1), (dict(B=-1), 1),
+    (dict(context_lens=None), 1), (dict(context_lens=F + 2), 1), (dict(logits=None), 1),
+    (dict(kv_cache=F + 1), 1), (dict(block_table=F + 2), 1),
+])
+def test_noalloc_rejects_invalid_arguments_before_any_cuda_call(lib, kw, status):
+    # the same host checks as paged_mqa_logits, run before the device is touched
+    # (on this GPU-less host a CUDA call would return MQA_ERR_CUDA instead)
+    assert call_noalloc(lib, **kw) == status
+    assert lib.mqa_last_error_message().decode()
+
+
+def test_noalloc_zero_batch_is_a_no_op(lib):
+    assert call_noalloc(lib, B=0) == 0
+
+
+def test_metadata_rejects_misaligned_pointers(lib):
+    assert lib.paged_mqa_logits_metadata(F + 2, 3, 2, 64, 8, F, None) == 1
+    assert lib.paged_mqa_logits_metadata(F, 3, 2, 64, 8, F + 1, None) == 1

@@ -53,3 +53,15 @@ def test_noalloc_matches_regular_call_twice_in_a_row():
         fin = np.isfinite(b)
         assert np.isfinite(a[fin]).all()
         assert (np.abs(a[fin].astype(np.float64) - b[fin]) <= tol[fin]).all()
+
+    # The property the call exists for: once warmed up (kernels loaded, the
+    # array's address looked up), a call allocates no device memory, neither
+    # through torch's allocator nor through the driver.
+    torch.cuda.synchronize()
+    allocs0 = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+    free0 = torch.cuda.mem_get_info()[0]
+    mqa.paged_mqa_logits_noalloc(q, kvc, kvs, w, cl, bt, out, next_n=2)
+    torch.cuda.synchronize()
+    assert mqa.device_status() == 0
+    assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == allocs0
+    assert torch.cuda.mem_get_info()[0] == free0
