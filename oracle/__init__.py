@@ -57,12 +57,14 @@ def _load():
             lib.oracle_paged_mqa_logits.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                                     i32, i64, u32, i32, i32, P, P]
             lib.oracle_paged_mqa_logits_metadata.argtypes = [P, i32, i32, i32, i32, P]
+            lib.oracle_mqa_logits_metadata.argtypes = [P, P, i32, i32, i32, i32, P]
             lib.oracle_topk_indices.argtypes = [P, i64, P, P, i32, i32, u32, i32, i32, i32, P]
             lib.oracle_e2m1_table.argtypes = [P]
             lib.oracle_mx_mqa_logits.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i64,
                                                  u32, i32, i32, P, P]
             for f in (lib.oracle_e4m3_table, lib.oracle_mqa_logits, lib.oracle_paged_mqa_logits,
-                      lib.oracle_paged_mqa_logits_metadata, lib.oracle_topk_indices,
+                      lib.oracle_paged_mqa_logits_metadata, lib.oracle_mqa_logits_metadata,
+                      lib.oracle_topk_indices,
                       lib.oracle_e2m1_table, lib.oracle_mx_mqa_logits):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -166,6 +168,21 @@ def paged_mqa_logits_metadata(context_lens, *, next_n: int, block_kv: int, num_s
                                                   num_sms, _ptr(meta))
     if rc != 0:
         raise ValueError("oracle_paged_mqa_logits_metadata: invalid arguments")
+    return meta
+
+
+def mqa_logits_metadata(k_start, k_end, *, S_kv: int, H: int, num_sms: int) -> np.ndarray:
+    """[num_sms + 1, 2] int32 dense schedule: (query block, absolute 128-key
+    tile) where each SM starts; (num_blocks, 0) at the end."""
+    ks = _np(k_start, np.int32)
+    ke = _np(k_end, np.int32)
+    if ks.shape != ke.shape:
+        raise ValueError("k_start and k_end differ in length")
+    meta = np.zeros((num_sms + 1, 2), np.int32)
+    rc = _load().oracle_mqa_logits_metadata(_ptr(ks), _ptr(ke), ks.shape[0], S_kv, H, num_sms,
+                                            _ptr(meta))
+    if rc != 0:
+        raise ValueError("oracle_mqa_logits_metadata: invalid arguments")
     return meta
 
 

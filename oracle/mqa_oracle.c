@@ -319,6 +319,83 @@ int oracle_paged_mqa_logits_metadata(const int32_t *context_lens, int B, int nex
 }
 
 /* ---------------------------------------------------------------------------
+ * Dense work schedule, the counterpart of the paged one for mqa_logits ("[PR
+ * #435] ...", section "Standalone performance reproducer", which builds
+ * get_mqa_logits_metadata(starts, ends, ...) once and passes it as
+ * schedule_meta; section "Validation", scheduled-path equality).  The pages fix
+ * neither its layout nor its unit; this library's reading, with the same
+ * num_sms + 1 shape as the paged schedule:
+ *   - a query block is tok = 256 / H consecutive query rows (block b holds rows
+ *     [b * tok, min(S_q, (b + 1) * tok)));
+ *   - the keys of a row are its range intersected with [0, S_kv) (start >= end:
+ *     no keys); block b spans the 128-key tiles from the first key of any of
+ *     its rows to the last: tiles [min lo / 128, ceil(max hi / 128)), none if
+ *     every row is empty;
+ *   - a unit is one block against one tile of its span; units are numbered
+ *     block by block, tile by tile, U in total;
+ *   - SM k starts at unit floor(k * U / num_sms); entry k is that unit's
+ *     (block, tile) with the tile's absolute index; the end entry, and any
+ *     start at U, is (num_blocks, 0).
+ * Returns 0, or -1 on invalid arguments.
+ * ------------------------------------------------------------------------- */
+static void dense_block_span(const int32_t *k_start, const int32_t *k_end, int S_q, int S_kv,
+                             int tok, int b, int64_t *t_lo, int64_t *t_hi)
+{
+    int64_t lo_min = -1, hi_max = -1;
+    for (int i = b * tok; i < S_q && i < (b + 1) * tok; ++i) {
+        int64_t lo = k_start[i] < 0 ? 0 : k_start[i];
+        int64_t hi = k_end[i] > S_kv ? S_kv : k_end[i];
+        if (lo > S_kv)
+            lo = S_kv;
+        if (hi <= lo)
+            continue;
+        if (lo_min < 0 || lo < lo_min)
+            lo_min = lo;
+        if (hi > hi_max)
+            hi_max = hi;
+    }
+    if (lo_min < 0) {
+        *t_lo = *t_hi = 0;
+    } else {
+        *t_lo = lo_min / 128;
+        *t_hi = (hi_max + 127) / 128;
+    }
+}
+
+int oracle_mqa_logits_metadata(const int32_t *k_start, const int32_t *k_end, int S_q, int S_kv,
+                               int H, int num_sms, int32_t *schedule_meta /* [num_sms + 1, 2] */)
+{
+    if (S_q < 0 || S_kv < 0 || H <= 0 || H > 256 || 256 % H != 0 || num_sms <= 0)
+        return -1;
+    const int tok = 256 / H;
+    const int nb = (S_q + tok - 1) / tok;
+    int64_t total = 0;
+    for (int b = 0; b < nb; ++b) {
+        int64_t lo, hi;
+        dense_block_span(k_start, k_end, S_q, S_kv, tok, b, &lo, &hi);
+        total += hi - lo;
+    }
+    for (int k = 0; k <= num_sms; ++k) {
+        const int64_t u = (int64_t)k * total / num_sms;
+        int64_t before = 0;
+        int b = 0;
+        int32_t tile = 0;
+        for (; b < nb; ++b) {
+            int64_t lo, hi;
+            dense_block_span(k_start, k_end, S_q, S_kv, tok, b, &lo, &hi);
+            if (u < before + (hi - lo)) {
+                tile = (int32_t)(lo + (u - before));
+                break;
+            }
+            before += hi - lo;
+        }
+        schedule_meta[2 * k] = b;            /* b == nb when u == total */
+        schedule_meta[2 * k + 1] = b < nb ? tile : 0;
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * Top-k key selection per query row: the step that consumes the logits.  The
  * "FlashMLA" page (parameters of flash_mla_with_kvcache) fixes only its
  * output contract: `indices` of shape (batch, seq_len_q, topk) naming the keys

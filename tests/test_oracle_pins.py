@@ -320,3 +320,61 @@ def test_metadata_brute_force(oracle_mod, ctx, num_sms):
     assert idx == sorted(idx) and idx[0] == 0 and idx[-1] == len(units)
     sizes = np.diff(idx)
     assert sizes.max() - sizes.min() <= 1 if len(sizes) else True
+
+
+def _brute_force_dense_schedule(k_start, k_end, S_kv, H, num_sms):
+    """Units listed from the validity mask itself: block b covers every 128-key
+    tile between the tile of its first valid key and the tile of its last."""
+    tok = 256 // H
+    S_q = len(k_start)
+    cols = np.arange(S_kv)
+    units = []
+    for b in range(0, -(-S_q // tok)):
+        rows = range(b * tok, min(S_q, (b + 1) * tok))
+        valid = np.zeros(S_kv, bool)
+        for i in rows:
+            valid |= (cols >= k_start[i]) & (cols < k_end[i])
+        keys = np.nonzero(valid)[0]
+        if len(keys):
+            for t in range(keys[0] // 128, keys[-1] // 128 + 1):
+                units.append((b, t))
+    U = len(units)
+    nb = -(-S_q // tok)
+    return np.array([units[k * U // num_sms] if k * U // num_sms < U else (nb, 0)
+                     for k in range(num_sms + 1)], np.int32), units
+
+
+@pytest.mark.parametrize("S_q,S_kv,H,kind,num_sms", [
+    (128, 512, 8, "causal", 4), (2048, 4096, 32, "suffix", 152), (300, 1000, 64, "random", 7),
+    (17, 260, 64, "random", 152), (64, 300, 64, "empty", 5), (256, 2048, 64, "windows", 13),
+    (5, 129, 8, "random", 1)])
+def test_dense_metadata_brute_force(oracle_mod, S_q, S_kv, H, kind, num_sms):
+    g = np.random.default_rng(S_q + S_kv + H)
+    i = np.arange(S_q)
+    if kind == "causal":
+        ks, ke = np.zeros(S_q), S_kv - S_q + i + 1
+    elif kind == "suffix":
+        ks, ke = i, np.full(S_q, S_kv)
+    elif kind == "empty":
+        ks, ke = np.full(S_q, 10), np.full(S_q, 10)
+        ke[S_q // 2] = 300                    # one non-empty row
+    elif kind == "windows":
+        ks = g.integers(0, S_kv, S_q)
+        ke = ks + g.integers(0, 300, S_q)     # may run past S_kv (clipped)
+    else:
+        ks = g.integers(-50, S_kv, S_q)
+        ke = g.integers(-50, S_kv + 50, S_q)  # inverted, negative and clipped ranges
+    ks, ke = ks.astype(np.int32), ke.astype(np.int32)
+    meta = oracle_mod.mqa_logits_metadata(ks, ke, S_kv=S_kv, H=H, num_sms=num_sms)
+    want, units = _brute_force_dense_schedule(ks, ke, S_kv, H, num_sms)
+    assert np.array_equal(meta, want)
+    idx = [units.index(tuple(e)) if tuple(e) in units else len(units) for e in meta.tolist()]
+    assert idx == sorted(idx) and idx[0] == 0 and idx[-1] == len(units)
+
+
+def test_dense_metadata_rejects_invalid_arguments(oracle_mod):
+    z = np.zeros(4, np.int32)
+    for kw in (dict(S_kv=-1, H=64, num_sms=4), dict(S_kv=10, H=48, num_sms=4),
+               dict(S_kv=10, H=64, num_sms=0)):
+        with pytest.raises(ValueError):
+            oracle_mod.mqa_logits_metadata(z, z, **kw)
