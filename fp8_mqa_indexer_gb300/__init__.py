@@ -20,7 +20,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "MQAError", "mqa_logits", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
+    "MQAError", "mqa_logits", "mqa_logits_metadata", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
     "paged_mqa_logits_noalloc", "mqa_topk_indices", "paged_mqa_topk_indices",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
     "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS",
@@ -66,6 +66,8 @@ def load_library() -> ctypes.CDLL:
         ULL = ctypes.c_ulonglong
         sig = {
             "mqa_logits": ([P, P, P, P, P, P, P, I, I, I, I, I64, U, P], I),
+            "mqa_logits_scheduled": ([P, P, P, P, P, P, P, I, P, I, I, I, I, I64, U, P], I),
+            "mqa_logits_metadata": ([P, P, I, I, I, I, P, P], I),
             "paged_mqa_logits_metadata": ([P, I, I, I, I, P, P], I),
             "paged_mqa_logits": ([P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I64, U, P], I),
             "paged_mqa_logits_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I64, U, P], I),
@@ -122,8 +124,9 @@ def _fp8_types():
 
 def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: bool = True,
                compressed: bool = False, ldo: Optional[int] = None, check_bounds: bool = False,
-               stream=None):
-    """Dense MQA logits (C ABI ``mqa_logits``).
+               schedule_meta=None, stream=None):
+    """Dense MQA logits (C ABI ``mqa_logits``, or ``mqa_logits_scheduled`` when
+    ``schedule_meta`` from ``mqa_logits_metadata`` is given).
 
     q [S_q, H, D] and kv [S_kv, D] are E4M3 (float8_e4m3fn or raw uint8 bytes),
     kv_scale [S_kv] and weights [S_q, H] float32, k_start / k_end [S_q] int32.
@@ -159,10 +162,42 @@ def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: 
     flags = (MQA_CLEAN if clean else 0) | (MQA_COMPRESSED if compressed else 0) | \
             (MQA_CHECK_BOUNDS if check_bounds else 0)
     with torch.cuda.device(q.device):
-        _check(load_library().mqa_logits(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights),
-                                         _ptr(k_start), _ptr(k_end), _ptr(logits), S_q, S_kv, H, D,
-                                         ldo, flags, _stream_handle(stream)))
+        if schedule_meta is None:
+            _check(load_library().mqa_logits(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights),
+                                             _ptr(k_start), _ptr(k_end), _ptr(logits), S_q, S_kv,
+                                             H, D, ldo, flags, _stream_handle(stream)))
+        else:
+            _dev(schedule_meta, "schedule_meta", (torch.int32,))
+            if schedule_meta.dim() != 2 or schedule_meta.shape[1] != 2:
+                raise ValueError("schedule_meta must be an int32 [num_sms + 1, 2] tensor")
+            _check(load_library().mqa_logits_scheduled(
+                _ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights), _ptr(k_start), _ptr(k_end),
+                _ptr(schedule_meta), schedule_meta.shape[0] - 1, _ptr(logits), S_q, S_kv, H, D,
+                ldo, flags, _stream_handle(stream)))
     return logits
+
+
+def mqa_logits_metadata(k_start, k_end, *, S_kv: int, H: int, num_sms: Optional[int] = None,
+                        out=None, stream=None):
+    """Dense work schedule (C ABI ``mqa_logits_metadata``): an int32
+    [num_sms + 1, 2] tensor of (query block, 128-key tile) start points for
+    ``mqa_logits(..., schedule_meta=...)``."""
+    import torch
+    _dev(k_start, "k_start", (torch.int32,))
+    _dev(k_end, "k_end", (torch.int32,))
+    if k_start.shape != k_end.shape or k_start.dim() != 1:
+        raise ValueError("k_start and k_end must be 1-D of the same length")
+    if num_sms is None:
+        num_sms = get_num_sms(k_start.device)
+    if out is None:
+        out = torch.empty((num_sms + 1, 2), dtype=torch.int32, device=k_start.device)
+    elif out.shape != (num_sms + 1, 2) or out.dtype != torch.int32 or not out.is_contiguous():
+        raise ValueError("schedule_meta must be a contiguous int32 [num_sms + 1, 2] tensor")
+    with torch.cuda.device(k_start.device):
+        _check(load_library().mqa_logits_metadata(_ptr(k_start), _ptr(k_end), k_start.shape[0],
+                                                  S_kv, H, num_sms, _ptr(out),
+                                                  _stream_handle(stream)))
+    return out
 
 
 def get_num_sms(device=None) -> int:

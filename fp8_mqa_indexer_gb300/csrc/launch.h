@@ -43,8 +43,9 @@ cudaError_t launch_instance(const LaunchArgs& a)
             return e;
         attr_set.fetch_or(bit);
     }
-    if constexpr (PAGED) {
-        // a dependent of the preceding kernel (the work schedule): see
+    {
+        // a programmatic dependent of the preceding kernel in the stream (the
+        // work schedule, for paged and scheduled dense calls): see
         // grid_dependency_wait in the kernel
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -57,9 +58,6 @@ cudaError_t launch_instance(const LaunchArgs& a)
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_kv, a.tm_scale, a.tm_w, a.p);
-    } else {
-        kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_kv, a.tm_scale, a.tm_w, a.p);
-        return cudaGetLastError();
     }
 }
 

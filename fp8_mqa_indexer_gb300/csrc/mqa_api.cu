@@ -145,27 +145,47 @@ bool aligned(const void* p, uintptr_t a)
 }
 
 // ---------------------------------------------------------- small kernels
-// Paged work schedule (see paged_mqa_logits_metadata in mqa.h).  One CTA:
-// each thread owns a contiguous chunk of sequences, a block-wide scan gives
-// the chunk's first unit, and each thread then emits the schedule entries whose
-// start unit falls inside its chunk.  With `check` set, entries are compared
-// with `meta` instead of written, and a mismatch raises kDevErrBadSchedule.
+// Work schedules (see paged_mqa_logits_metadata and mqa_logits_metadata in
+// mqa.h).  A query block b owns the 128-key tiles [lo, hi) given by Span; its
+// units are numbered block by block, U in total, and SM k starts at unit
+// floor(k * U / num_sms).  One CTA: each thread owns a contiguous chunk of
+// blocks, a block-wide scan gives the chunk's first unit, and each thread then
+// emits the schedule entries whose start unit falls inside its chunk.  With
+// `check` set, entries are compared with `meta` instead of written, and a
+// mismatch raises kDevErrBadSchedule.
 constexpr int kMetaThreads = 1024;
 
+struct PagedSpan {   // sequence b: tiles [0, ceil(ctx / 128))
+    const int* ctx;
+    __device__ int2 operator()(int b) const { return make_int2(0, paged_tiles(ctx[b])); }
+};
+
+struct DenseSpan {   // query block b: the tiles between its rows' first and last key
+    Params p;
+    __device__ int2 operator()(int b) const
+    {
+        int lo, hi;
+        dense_block_tiles(p, b, lo, hi);
+        return make_int2(lo, hi);
+    }
+};
+
+template <class Span>
 __global__ void __launch_bounds__(kMetaThreads)
-    paged_schedule_kernel(const int* __restrict__ ctx, int B, int num_sms, int* meta, int check,
-                          unsigned* status)
+    schedule_kernel(Span span, int NB, int num_sms, int* meta, int check, unsigned* status)
 {
     __shared__ long long warp_tot[kMetaThreads / 32];
-    // the paged logits kernel that follows may start its set-up now; it waits
-    // for this kernel's completion before reading the schedule
+    // the logits kernel that follows may start its set-up now; it waits for
+    // this kernel's completion before reading the schedule
     launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int chunk = (B + kMetaThreads - 1) / kMetaThreads;
-    const int c0 = min(tid * chunk, B), c1 = min(c0 + chunk, B);
+    const int chunk = (NB + kMetaThreads - 1) / kMetaThreads;
+    const int c0 = min(tid * chunk, NB), c1 = min(c0 + chunk, NB);
     long long local = 0;
-    for (int b = c0; b < c1; ++b)
-        local += paged_tiles(ctx[b]);
+    for (int b = c0; b < c1; ++b) {
+        const int2 t = span(b);
+        local += t.y - t.x;
+    }
     long long incl = local;
     for (int o = 1; o < 32; o <<= 1) {
         long long v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -197,22 +217,24 @@ __global__ void __launch_bounds__(kMetaThreads)
         long long k = (P * num_sms + U - 1) / U;
         int b = c0;
         long long base = P;
+        int2 t = span(b);
         for (; k <= num_sms; ++k) {
             const long long u = k * U / num_sms;
             if (u >= P + local)
                 break;
-            while (u >= base + paged_tiles(ctx[b])) {
-                base += paged_tiles(ctx[b]);
+            while (u >= base + (t.y - t.x)) {
+                base += t.y - t.x;
                 ++b;
+                t = span(b);
             }
-            emit((int)k, b, (int)(u - base));
+            emit((int)k, b, t.x + (int)(u - base));
         }
     }
-    // entries at u == U mark the end: (B, 0)
+    // entries at u == U mark the end: (NB, 0)
     for (int k = tid; k <= num_sms; k += kMetaThreads) {
         const long long u = U == 0 ? 0 : (long long)k * U / num_sms;
         if (u >= U)
-            emit(k, B, 0);
+            emit(k, NB, 0);
     }
 }
 
@@ -295,6 +317,10 @@ mqa_status status_from_word(unsigned v)
         return fail(MQA_ERR_BAD_INPUT, "device bounds check failed (flags 0x%x)", v);
     return MQA_OK;
 }
+
+// Largest paged next_n: a sequence's tokens are scored in query atoms of
+// kMaxN / H tokens, one launch per atom.
+constexpr int kMaxNextN = 64;
 
 int grid_for(int n)
 {
@@ -389,17 +415,20 @@ mqa_status paged_mqa_logits_metadata(const int32_t* context_lens, int B, int nex
     mqa_status s = device_state(&dev, &st);
     if (s != MQA_OK)
         return s;
-    paged_schedule_kernel<<<1, kMetaThreads, 0, (cudaStream_t)stream>>>(context_lens, B, num_sms,
-                                                                        schedule_meta, 0, st);
+    schedule_kernel<<<1, kMetaThreads, 0, (cudaStream_t)stream>>>(PagedSpan{context_lens}, B,
+                                                                  num_sms, schedule_meta, 0, st);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? MQA_OK : cuda_fail(e, "paged schedule launch");
 }
 
-mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, const float* weights,
-                      const int32_t* k_start, const int32_t* k_end, float* logits, int S_q,
-                      int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream_)
+namespace {
+// mqa_logits and mqa_logits_scheduled: `schedule_meta` (num_sms + 1 entries
+// from mqa_logits_metadata) or null for the in-kernel split.
+mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, const float* weights,
+                      const int32_t* k_start, const int32_t* k_end, const int32_t* schedule_meta,
+                      int sched_sms, float* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
+                      unsigned flags, cudaStream_t stream)
 {
-    cudaStream_t stream = (cudaStream_t)stream_;
     const bool compressed = (flags & MQA_COMPRESSED) != 0;
     const bool clean = (flags & MQA_CLEAN) != 0;
     if (flags & ~(unsigned)(MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS))
@@ -426,12 +455,15 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
     if (!aligned(logits, 4) || !aligned(k_start, 4) || !aligned(k_end, 4))
         return fail(MQA_ERR_INVALID_ARG, "logits, k_start, k_end must be 4-byte aligned");
 
+    if (schedule_meta && (sched_sms < 1 || !aligned(schedule_meta, 4)))
+        return fail(MQA_ERR_INVALID_ARG, "schedule_meta must be 4-byte aligned and num_sms >= 1");
+
     int dev;
     unsigned* st;
     mqa_status s = device_state(&dev, &st);
     if (s != MQA_OK)
         return s;
-    const int num_sms = g_num_sms[dev];
+    const int num_sms = schedule_meta ? sched_sms : g_num_sms[dev];
 
     if (flags & MQA_CHECK_BOUNDS) {
         unsigned v = 0;
@@ -440,6 +472,18 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
             return s;
         check_dense_kernel<<<grid_for((S_q + 255) / 256), 256, 0, stream>>>(
             k_start, k_end, S_q, S_kv, (long long)ldo, compressed, st);
+        if (schedule_meta && S_kv > 0) {
+            Params sp;
+            memset(&sp, 0, sizeof(sp));
+            sp.S_q = S_q;
+            sp.S_kv = S_kv;
+            sp.k_start = k_start;
+            sp.k_end = k_end;
+            sp.tok = kMaxN / H;
+            schedule_kernel<<<1, kMetaThreads, 0, stream>>>(
+                DenseSpan{sp}, (S_q + sp.tok - 1) / sp.tok, num_sms,
+                const_cast<int32_t*>(schedule_meta), 1, st);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return cuda_fail(e, "bounds-check launch");
@@ -484,9 +528,12 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
     p.kv_scale = kv_scale;
     p.k_start = k_start;
     p.k_end = k_end;
+    p.schedule_meta = schedule_meta;
     p.width = S_kv;
     p.width_i = S_kv;
     p.tok = tok;
+    p.tok0 = 0;
+    p.blk_stride = tok;
     p.num_q_blocks = (S_q + tok - 1) / tok;
     p.rows = S_q;
     p.wait_limit = (long long)g_wait_limit.load();
@@ -499,6 +546,58 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
     if (e != cudaSuccess)
         return cuda_fail(e, "dense kernel launch");
     return MQA_OK;
+}
+}  // namespace
+
+mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, const float* weights,
+                      const int32_t* k_start, const int32_t* k_end, float* logits, int S_q,
+                      int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream)
+{
+    return dense_call(q, kv, kv_scale, weights, k_start, k_end, nullptr, 0, logits, S_q, S_kv, H,
+                      D, ldo, flags, (cudaStream_t)stream);
+}
+
+mqa_status mqa_logits_scheduled(const void* q, const void* kv, const float* kv_scale,
+                                const float* weights, const int32_t* k_start,
+                                const int32_t* k_end, const int32_t* schedule_meta, int num_sms,
+                                float* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
+                                unsigned flags, mqa_stream_t stream)
+{
+    if (!schedule_meta)
+        return fail(MQA_ERR_INVALID_ARG, "null schedule_meta");
+    return dense_call(q, kv, kv_scale, weights, k_start, k_end, schedule_meta, num_sms, logits,
+                      S_q, S_kv, H, D, ldo, flags, (cudaStream_t)stream);
+}
+
+mqa_status mqa_logits_metadata(const int32_t* k_start, const int32_t* k_end, int S_q, int S_kv,
+                               int H, int num_sms, int32_t* schedule_meta, mqa_stream_t stream)
+{
+    if (S_q < 0 || S_kv < 0 || num_sms < 1)
+        return fail(MQA_ERR_INVALID_ARG, "need S_q >= 0, S_kv >= 0, num_sms >= 1");
+    if (H != 8 && H != 32 && H != 64)
+        return fail(MQA_ERR_UNSUPPORTED, "H must be 8, 32 or 64 (got %d)", H);
+    if ((long long)S_q * H >= INT_MAX || S_kv > INT_MAX - 256)
+        return fail(MQA_ERR_INVALID_ARG, "S_q * H or S_kv too large");
+    if (!schedule_meta || (S_q > 0 && (!k_start || !k_end)))
+        return fail(MQA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(schedule_meta, 4) || (S_q > 0 && (!aligned(k_start, 4) || !aligned(k_end, 4))))
+        return fail(MQA_ERR_INVALID_ARG, "k_start, k_end and schedule_meta must be 4-byte aligned");
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+    Params sp;
+    memset(&sp, 0, sizeof(sp));
+    sp.S_q = S_q;
+    sp.S_kv = S_kv;
+    sp.k_start = k_start;
+    sp.k_end = k_end;
+    sp.tok = kMaxN / H;
+    schedule_kernel<<<1, kMetaThreads, 0, (cudaStream_t)stream>>>(
+        DenseSpan{sp}, (S_q + sp.tok - 1) / sp.tok, num_sms, schedule_meta, 0, st);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MQA_OK : cuda_fail(e, "dense schedule launch");
 }
 
 namespace {
@@ -529,8 +628,8 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_s
         return fail(MQA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", D);
     if (H != 16 && H != 32 && H != 64)
         return fail(MQA_ERR_UNSUPPORTED, "H must be 16, 32 or 64 (got %d)", H);
-    if (next_n * H > kMaxN || (next_n * H) % 16 != 0)
-        return fail(MQA_ERR_UNSUPPORTED, "next_n * H must be a multiple of 16 and <= 256");
+    if (next_n > kMaxNextN)
+        return fail(MQA_ERR_UNSUPPORTED, "next_n must be at most %d (got %d)", kMaxNextN, next_n);
     if (block_kv != 32 && block_kv != 64 && block_kv != 128)
         return fail(MQA_ERR_UNSUPPORTED, "block_kv must be 32, 64 or 128 (got %d)", block_kv);
     const long long width = (long long)max_blocks_per_seq * block_kv;
@@ -587,8 +686,8 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
         const long long total = (long long)B * max_blocks_per_seq;
         check_paged_kernel<<<grid_for((int)min(total / 256 + 1, 100000LL)), 256, 0, stream>>>(
             context_lens, block_table, B, max_blocks_per_seq, block_kv, num_blocks, st);
-        paged_schedule_kernel<<<1, kMetaThreads, 0, stream>>>(
-            context_lens, B, num_sms, const_cast<int32_t*>(schedule_meta), 1, st);
+        schedule_kernel<<<1, kMetaThreads, 0, stream>>>(
+            PagedSpan{context_lens}, B, num_sms, const_cast<int32_t*>(schedule_meta), 1, st);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return cuda_fail(e, "bounds-check launch");
@@ -602,18 +701,12 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
 
     LaunchArgs a;
     memset(&a, 0, sizeof(a));
-    const int N = next_n * H;
     const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if ((s = make_map_2d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                         (unsigned long long)B * next_n * H, D, N, D, swz, "q")) != MQA_OK ||
-        (s = make_map_2d(&a.tm_kv, kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+    if ((s = make_map_2d(&a.tm_kv, kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
                          (unsigned long long)num_blocks * block_kv, D, block_kv, D, swz,
                          "kv_cache")) != MQA_OK ||
         (s = make_map_vec_f32(&a.tm_scale, kv_scales, (unsigned long long)num_blocks * block_kv,
-                              block_kv, "kv_scales")) != MQA_OK ||
-        (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
-                         (unsigned long long)B * next_n, H, next_n, H, CU_TENSOR_MAP_SWIZZLE_NONE,
-                         "weights")) != MQA_OK)
+                              block_kv, "kv_scales")) != MQA_OK)
         return s;
     Params& p = a.p;
     p.logits = logits;
@@ -628,18 +721,34 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     p.max_blocks = max_blocks_per_seq;
     p.width = width;
     p.width_i = (int)width;
-    p.tok = next_n;
+    p.blk_stride = next_n;
     p.num_q_blocks = B;
     p.rows = B * next_n;
     p.wait_limit = (long long)g_wait_limit.load();
     p.status = st;
     a.grid = num_sms;
     a.stream = stream;
-    cudaError_t e = launch_paged(H, D, a);
-    if (e == cudaErrorNotSupported)
-        return fail(MQA_ERR_UNSUPPORTED, "no paged kernel for H=%d D=%d", H, D);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "paged kernel launch");
+    // A sequence's next_n query tokens are split into query atoms of at most
+    // kMaxN / H tokens (one accumulator of kMaxN columns holds an atom's
+    // tokens x heads); each atom is one launch over the same schedule.
+    const int atom = kMaxN / H;
+    for (int t0 = 0; t0 < next_n; t0 += atom) {
+        const int tok = next_n - t0 < atom ? next_n - t0 : atom;
+        if ((s = make_map_2d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                             (unsigned long long)B * next_n * H, D, (unsigned)(tok * H), D, swz,
+                             "q")) != MQA_OK ||
+            (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                             (unsigned long long)B * next_n, H, (unsigned)tok, H,
+                             CU_TENSOR_MAP_SWIZZLE_NONE, "weights")) != MQA_OK)
+            return s;
+        p.tok = tok;
+        p.tok0 = t0;
+        cudaError_t e = launch_paged(H, D, a);
+        if (e == cudaErrorNotSupported)
+            return fail(MQA_ERR_UNSUPPORTED, "no paged kernel for H=%d D=%d", H, D);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "paged kernel launch");
+    }
     return MQA_OK;
 }
 

@@ -102,6 +102,8 @@ struct Params {
     long long width;     // logical columns of an uncompressed row
     int width_i;         // the same, as an int (below 2^31 - 256)
     int tok;             // query tokens per work unit
+    int tok0;            // paged: first token (within its sequence) of this launch's query atom
+    int blk_stride;      // output rows between query blocks: tok (dense) or next_n (paged)
     int num_q_blocks;    // dense: ceil(S_q / tok); paged: B
     int rows;            // output rows: S_q or B * next_n
     long long wait_limit;
@@ -148,8 +150,8 @@ __device__ __forceinline__ int2 dense_range(const Params& p, int i)
     return make_int2(lo, hi);
 }
 
-// Paged range of token t of sequence with context ctx: [0, ctx - next_n + t + 1)
-// intersected with [0, width).
+// Paged range of token t (0 <= t < next_n) of a sequence with context ctx:
+// [0, ctx - next_n + t + 1) intersected with [0, width).
 __device__ __forceinline__ int2 paged_range(const Params& p, int ctx, int t)
 {
     long long hi = (long long)ctx - p.next_n + t + 1;
@@ -302,7 +304,7 @@ struct Epilogue {
         __syncwarp();
         if (a < kTokW) {
             TokRow t;
-            const int r = info.b * p.tok + tok0 + a;
+            const int r = info.b * p.blk_stride + p.tok0 + tok0 + a;
             const int2 rg = sm.range[info.qbuf][tok0 + a];   // within [0, width)
             t.slo = t.shi = t.vlo = t.vhi = 0;
             t.off = 0;
@@ -558,14 +560,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(&sm.tmem_base), 512);
         tmem_relinquish();
     }
-    // Paged calls are launched as dependents of the schedule kernel: the set-up
-    // above (shared memory and TMEM only) overlaps it; every global access
-    // below comes after it has finished.
-    if constexpr (PAGED)
-        grid_dependency_wait();
+    // Calls are launched as programmatic dependents of the preceding kernel in
+    // the stream (for the paged and the scheduled dense call, the schedule
+    // kernel): the set-up above (shared memory and TMEM only) overlaps its
+    // tail; every global access below comes after it has finished.
+    grid_dependency_wait();
 
     // Work slice of this CTA: start (block, tile) and number of units.
-    if (!PAGED) {
+    if (!PAGED && p.schedule_meta) {
+        // dense, scheduled: entries cta and cta + 1 of the schedule written by
+        // mqa_logits_metadata bound the slice; count its units over the
+        // blocks it spans (the blocks' tile spans are recomputed here)
+        const int NB = p.num_q_blocks;
+        const int b0 = __ldg(p.schedule_meta + 2 * cta);
+        const int t0 = __ldg(p.schedule_meta + 2 * cta + 1);
+        const int b1 = __ldg(p.schedule_meta + 2 * cta + 2);
+        const int t1 = __ldg(p.schedule_meta + 2 * cta + 3);
+        bool ok = b0 >= 0 && b0 <= b1 && b1 <= NB && (b0 < NB || t0 == 0) && (b1 < NB || t1 == 0) &&
+                  (b0 < b1 || t0 <= t1);
+        long long local = 0;
+        int bad = 0;
+        if (ok) {
+            for (int b = b0 + tid; b <= b1 && b < NB; b += kThreads) {
+                int tlo, thi;
+                dense_block_tiles(p, b, tlo, thi);
+                const int lo = (b == b0) ? t0 : tlo;
+                const int hi = (b == b1) ? t1 : thi;
+                if (lo < tlo || hi > thi || lo > hi)   // the slice leaves the block's span
+                    bad = 1;
+                local += hi > lo ? hi - lo : 0;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            local += __shfl_xor_sync(0xffffffffu, local, o);
+        if (lane == 0)
+            sm.scan[warp] = local;
+        ok = !__syncthreads_or(!ok || bad);
+        if (tid == 0) {
+            if (!ok)
+                atomicOr(p.status, kDevErrBadSchedule);
+            long long n = 0;
+            for (int k = 0; k < kThreads / 32; ++k)
+                n += sm.scan[k];
+            sm.n_units = ok ? (int)n : 0;
+            sm.start_b = b0;
+            sm.start_t = t0;
+        }
+    } else if (!PAGED) {
         // Prefix sum of per-block tile counts over all threads, then locate
         // units [cta*U/G, (cta+1)*U/G).
         const int NB = p.num_q_blocks;
@@ -685,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ctx = b < p.B ? max(__ldg(p.context_lens + b), 0) : 0;
                 tlo = 0;
                 thi = paged_tiles(ctx);
-                myrange = (lane < p.tok) ? paged_range(p, ctx, lane) : make_int2(0, 0);
+                myrange = (lane < p.tok) ? paged_range(p, ctx, p.tok0 + lane) : make_int2(0, 0);
                 npages = min((int)((min((long long)ctx, p.width) + p.block_kv - 1) / p.block_kv),
                              p.max_blocks);
                 wbase = (t * ppt) & ~31;
@@ -711,8 +753,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const uint32_t bar = smem_u32(&sm.q_full[qb]);
                     mbar_arrive_expect_tx(bar, (uint32_t)(N * D + p.tok * H * 4));
-                    tma_load_2d(smem_u32(sm.q[qb]), &tm_q, bar, 0, b * N);
-                    tma_load_2d(smem_u32(sm.w[qb]), &tm_w, bar, 0, b * p.tok);
+                    // the block's first query row (token b * blk_stride + tok0)
+                    const int row0 = b * p.blk_stride + p.tok0;
+                    tma_load_2d(smem_u32(sm.q[qb]), &tm_q, bar, 0, row0 * H);
+                    tma_load_2d(smem_u32(sm.w[qb]), &tm_w, bar, 0, row0);
                 }
                 ++q_issued;
             }
@@ -846,7 +890,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         regs_dec<kRegsCtl>();
         if (p.flags & kFlagClean) {
             const int fw = warp - 2;   // 0 or 1
-            for (int r = cta + fw * G; r < p.rows; r += 2 * G) {
+            // paged: the rows of this launch's query atom only
+            const int nrows = PAGED ? p.B * p.tok : p.rows;
+            for (int rr = cta + fw * G; rr < nrows; rr += 2 * G) {
+                const int r = PAGED ? (rr / p.tok) * p.next_n + p.tok0 + rr % p.tok : rr;
                 float* row = p.logits + (long long)r * p.ldo;
                 if (PAGED) {
                     const int c = max(__ldg(p.context_lens + r / p.next_n), 0);

@@ -96,6 +96,48 @@ MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_sca
                       int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
 
 /*
+ * Work schedule for a dense call ("[PR #435] Improve SM100 MX MQA logits
+ * clean-output performance": the reproducer computes get_mqa_logits_metadata
+ * once outside the timed region and passes it to the logits call as
+ * schedule_meta; section "Validation" checks that the scheduled path gives the
+ * same output as the unscheduled one).  The pages fix neither its layout nor
+ * its unit; this library's:
+ *
+ * A query block b is the tok = 256 / H query rows [b * tok, (b + 1) * tok)
+ * (the last one may be short); it spans the 128-key tiles from the first to
+ * the last key of any of its rows (ranges intersected with [0, S_kv), start >=
+ * end empty).  A unit is one block against one tile of its span, numbered
+ * block by block, U in total.  SM k starts at unit floor(k * U / num_sms);
+ * entry k is that unit's (block, absolute tile index); entry num_sms, and any
+ * entry at U, is (number of blocks, 0).
+ *
+ *   k_start, k_end [S_q] int32 (device): the ranges the logits call will get
+ *   schedule_meta  [num_sms + 1][2] int32 (device), written by this call
+ *   H in {8, 32, 64}; num_sms >= 1 (normally mqa_get_num_sms()).
+ */
+MQA_API mqa_status mqa_logits_metadata(const int32_t *k_start, const int32_t *k_end, int S_q,
+                                       int S_kv, int H, int num_sms, int32_t *schedule_meta,
+                                       mqa_stream_t stream);
+
+/*
+ * mqa_logits with a precomputed schedule: CTA k of the num_sms launched
+ * processes the units between entries k and k + 1 of schedule_meta (from
+ * mqa_logits_metadata for the same k_start, k_end, S_q, S_kv, H and num_sms)
+ * instead of deriving its slice from all the ranges.  Every output element is
+ * computed with the same arithmetic either way: the results are bitwise
+ * identical to mqa_logits.  The kernel checks that the entries it reads are
+ * ordered and inside the blocks' spans (an inconsistent schedule records
+ * MQA_ERR_BAD_INPUT for mqa_device_status and computes nothing); under
+ * MQA_CHECK_BOUNDS the whole schedule is recomputed and compared first.
+ * Other arguments and errors: as mqa_logits.
+ */
+MQA_API mqa_status mqa_logits_scheduled(const void *q, const void *kv, const float *kv_scale,
+                                        const float *weights, const int32_t *k_start,
+                                        const int32_t *k_end, const int32_t *schedule_meta,
+                                        int num_sms, float *logits, int S_q, int S_kv, int H,
+                                        int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
+
+/*
  * Work schedule for paged_mqa_logits ("[PR #314] fix: SM90 paged MQA logits
  * IMA on next_n=4", sections "a97b74d" Root cause / Fix: schedule_meta holds
  * num_sms + 1 entries and host and kernel must agree on the query atom).
@@ -132,8 +174,14 @@ MQA_API mqa_status paged_mqa_logits_metadata(const int32_t *context_lens, int B,
  *                block_kv columns, ldo >= that.  Row r scores key positions
  *                [0, context_lens[b] - next_n + t + 1); key position j is slot
  *                j % block_kv of block block_table[b, j / block_kv].
- *   H in {16, 32, 64}, D in {64, 128}, next_n * H a multiple of 16 and at
- *   most 256, block_kv in {32, 64, 128}.
+ *   H in {16, 32, 64}, D in {64, 128}, 1 <= next_n <= 64, block_kv in
+ *   {32, 64, 128}.  A sequence's next_n tokens are scored in query atoms of
+ *   at most 256 / H tokens (one kernel launch per atom over the same
+ *   schedule), as "[PR #314] ...", section "a97b74d", splits next_n into
+ *   query atoms.
+ *   num_sms      the number of schedule_meta entries minus one (the schedule's
+ *                length; the kernel runs one CTA per entry).  Not in the pages'
+ *                call, where the schedule tensor carries its own shape.
  *   flags        MQA_CLEAN | MQA_CHECK_BOUNDS (MQA_COMPRESSED is rejected)
  */
 MQA_API mqa_status paged_mqa_logits(const void *q, const void *kv_cache, const float *kv_scales,

@@ -89,7 +89,7 @@ def call_paged(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(flags=2), 2), (dict(flags=3), 2), (dict(flags=8), 1), (dict(D=32), 2), (dict(H=8), 2),
-    (dict(next_n=5), 2), (dict(block_kv=16), 2), (dict(ldo=1000), 1), (dict(num_sms=0), 1),
+    (dict(next_n=65), 2), (dict(block_kv=16), 2), (dict(ldo=1000), 1), (dict(num_sms=0), 1),
     (dict(next_n=0), 1), (dict(B=-1), 1), (dict(meta=None), 1), (dict(kv_cache=F + 1), 1),
 ])
 def test_paged_rejects_invalid_arguments(lib, kw, status):
@@ -215,3 +215,24 @@ def test_noalloc_zero_batch_is_a_no_op(lib):
 def test_metadata_rejects_misaligned_pointers(lib):
     assert lib.paged_mqa_logits_metadata(F + 2, 3, 2, 64, 8, F, None) == 1
     assert lib.paged_mqa_logits_metadata(F, 3, 2, 64, 8, F + 1, None) == 1
+
+
+@pytest.mark.parametrize("kw,status", [(dict(H=16), 2), (dict(num_sms=0), 1), (dict(S_q=-1), 1),
+                                       (dict(meta=None), 1), (dict(ks=F + 2), 1), (dict(meta=F + 1), 1)])
+def test_dense_metadata_rejects_invalid_arguments(lib, kw, status):
+    a = dict(ks=F, ke=F, S_q=4, S_kv=256, H=64, num_sms=8, meta=F)
+    a.update(kw)
+    assert lib.mqa_logits_metadata(a["ks"], a["ke"], a["S_q"], a["S_kv"], a["H"], a["num_sms"],
+                                   a["meta"], None) == status
+
+
+def test_scheduled_dense_rejects_invalid_arguments(lib):
+    def call(**kw):
+        a = dict(meta=F, num_sms=8, D=128)
+        a.update(kw)
+        return lib.mqa_logits_scheduled(F, F, F, F, F, F, a["meta"], a["num_sms"], F, 4, 256, 64,
+                                        a["D"], 256, 1, None)
+    assert call(meta=None) == 1
+    assert call(D=96) == 2
+    assert call(num_sms=0) == 1
+    assert call(meta=F + 2) == 1

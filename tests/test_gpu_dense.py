@@ -222,11 +222,30 @@ def test_full_size_mask_all_rows(big):
 
 
 def test_full_size_deterministic(big):
+    """20 repeats, bitwise ([D] "Validation": 20-repeat bitwise checks)."""
     case, d, out = big
-    for _ in range(3):
-        again = run_gpu(case, d)
+    reps = 20 if case.S_q <= 2048 else 5
+    again = torch.empty_like(out)
+    for _ in range(reps):
+        run_gpu(case, d, out=again, ldo=case.ldo)
         assert torch.equal(again.view(torch.int32), out.view(torch.int32))
-        del again
+    del again
+
+
+def test_full_size_scheduled_path_is_bitwise_identical(big):
+    """The schedule from mqa_logits_metadata (bit-exact against the oracle's)
+    gives the same output as the in-kernel split, bit for bit ([D]
+    "Validation": scheduled-path equality)."""
+    case, d, out = big
+    meta = mqa.mqa_logits_metadata(d["ks"], d["ke"], S_kv=case.S_kv, H=case.H)
+    want = oracle.mqa_logits_metadata(case.k_start, case.k_end, S_kv=case.S_kv, H=case.H,
+                                      num_sms=meta.shape[0] - 1)
+    assert np.array_equal(meta.cpu().numpy(), want)
+    again = mqa.mqa_logits(d["q"], d["kv"], d["s"], d["w"], d["ks"], d["ke"], clean=case.clean,
+                           compressed=case.compressed, ldo=case.ldo, schedule_meta=meta)
+    torch.cuda.synchronize()
+    assert mqa.device_status() == 0
+    assert torch.equal(again.view(torch.int32), out.view(torch.int32))
 
 
 def test_full_size_power_of_two_scaling_is_exact(big):
@@ -283,4 +302,52 @@ def test_check_bounds_rejects_bad_ranges(dev, bad):
     # and the context is still good
     assert mqa.device_status() == 0
     run_gpu(case, upload(case, dev))
+    assert mqa.device_status() == 0
+
+
+# ------------------------------------------------------- dense schedule
+@pytest.mark.parametrize("H,kind,num_sms", [(64, "causal_tail", None), (8, "causal_tail_inclusive", 7),
+                                            (32, "suffix", 152), (64, "custom", 5),
+                                            (64, "custom", 1000)])
+def test_scheduled_equals_unscheduled_and_oracle(dev, H, kind, num_sms):
+    ks = ke = None
+    if kind == "custom":
+        g = torch.Generator().manual_seed(11)
+        ks = torch.randint(-30, 900, (150,), generator=g)
+        ke = ks + torch.randint(-10, 400, (150,), generator=g)
+    case = wl.dense_case(150, 900, H, 128, seed=330 + H, ranges=kind, k_start=ks, k_end=ke)
+    d = upload(case, dev)
+    meta = mqa.mqa_logits_metadata(d["ks"], d["ke"], S_kv=case.S_kv, H=H, num_sms=num_sms)
+    want = oracle.mqa_logits_metadata(case.k_start, case.k_end, S_kv=case.S_kv, H=H,
+                                      num_sms=meta.shape[0] - 1)
+    assert np.array_equal(meta.cpu().numpy(), want)
+    plain = run_gpu(case, d)
+    sched = mqa.mqa_logits(d["q"], d["kv"], d["s"], d["w"], d["ks"], d["ke"], schedule_meta=meta)
+    checked = mqa.mqa_logits(d["q"], d["kv"], d["s"], d["w"], d["ks"], d["ke"], schedule_meta=meta,
+                             check_bounds=True)
+    torch.cuda.synchronize()
+    assert mqa.device_status() == 0
+    assert torch.equal(sched.view(torch.int32), plain.view(torch.int32))
+    assert torch.equal(checked.view(torch.int32), plain.view(torch.int32))
+    ref, tol = oracle_rows(case, list(range(case.S_q)))
+    assert_logits_match(sched.cpu().numpy(), ref, tol, what=f"scheduled H={H} {kind}")
+
+
+def test_scheduled_rejects_a_bad_schedule(dev):
+    case = wl.dense_case(150, 900, 64, 128, seed=340, ranges="causal_tail")
+    d = upload(case, dev)
+    meta = mqa.mqa_logits_metadata(d["ks"], d["ke"], S_kv=case.S_kv, H=64, num_sms=6)
+    bad = meta.clone()
+    bad[2, 1] += 1
+    with pytest.raises(mqa.MQAError) as e:
+        mqa.mqa_logits(d["q"], d["kv"], d["s"], d["w"], d["ks"], d["ke"], schedule_meta=bad,
+                       check_bounds=True)
+    assert e.value.status == 5
+    assert mqa.device_status() == 0
+    # without the host check, the kernel's own entry checks refuse a schedule
+    # whose slice leaves a block's span, and compute nothing for that slice
+    bad2 = meta.clone()
+    bad2[1, 1] = 1000
+    mqa.mqa_logits(d["q"], d["kv"], d["s"], d["w"], d["ks"], d["ke"], schedule_meta=bad2)
+    assert mqa.device_status() == 5
     assert mqa.device_status() == 0

@@ -58,7 +58,10 @@ def test_schedule_matches_oracle_bitwise(dev, B, lo, hi, num_sms):
 # ------------------------------------------------------------ small, full
 @pytest.mark.parametrize("next_n,block_kv,H,D", [
     (2, 64, 64, 128), (1, 64, 64, 128), (4, 64, 64, 128), (3, 32, 32, 128), (2, 128, 64, 128),
-    (2, 64, 32, 64), (1, 32, 16, 64), (6, 64, 32, 128), (16, 64, 16, 128)])
+    (2, 64, 32, 64), (1, 32, 16, 64), (6, 64, 32, 128), (16, 64, 16, 128),
+    # next_n * H above one accumulator (256 columns): query atoms of 256 / H tokens
+    (5, 64, 64, 128), (6, 32, 64, 128), (6, 64, 64, 64), (3, 64, 64, 128), (9, 64, 32, 128),
+    (20, 128, 16, 128)])
 def test_small_paged_full(dev, next_n, block_kv, H, D):
     B = 6
     ctx = [1, next_n - 1, 129, 700, 64, 511]
