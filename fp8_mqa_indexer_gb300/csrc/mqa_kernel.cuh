@@ -481,25 +481,6 @@ struct Epilogue {
             if (!one(u))
                 return;
     }
-
-    // A warp with no columns in the unit still takes part in every hand-off.
-    __device__ __forceinline__ void run_empty()
-    {
-        int stage = 0;
-        uint32_t phase = 0;
-        int k_block = -1;
-        for (int u = 0; u < n_units; ++u) {
-            Unit st;
-            if (!begin(stage, phase, u, k_block, st))
-                return;
-            release(st);
-            finish(st);
-            if (++stage == S) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-    }
 };
 
 // ------------------------------------------------------------------ kernel
@@ -533,17 +514,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta = blockIdx.x;
     const int N = p.tok * H;
 
+    // Epilogue warps whose columns hold tokens: the groups of the first N
+    // columns.  The others (a paged unit narrower than 256 columns) leave at
+    // once and take no part in any hand-off.
+    const int n_epi = 4 * min(kNumEpiWarps / 4, (N + kEpiCols - 1) / kEpiCols);
+
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
-            mbar_init(smem_u32(&sm.empty[s]), 1 + kNumEpiWarps);
+            mbar_init(smem_u32(&sm.empty[s]), 1 + n_epi);
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(smem_u32(&sm.q_full[k]), 1);
-            mbar_init(smem_u32(&sm.q_empty[k]), 1 + kNumEpiWarps);
+            mbar_init(smem_u32(&sm.q_empty[k]), 1 + n_epi);
             mbar_init(smem_u32(&sm.acc_full[k]), 1);
-            mbar_init(smem_u32(&sm.acc_empty[k]), kNumEpiWarps);
+            mbar_init(smem_u32(&sm.acc_empty[k]), n_epi);
         }
         mbar_init(smem_u32(&sm.mma_done), 1);
         sm.abort_flag = 0;
@@ -939,9 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             epi.template run<32, true>();
         } else if (nc > 0) {
             epi.template run<16, true>();
-        } else {
-            epi.run_empty();
-        }
+        }   // else: no columns in any unit of this launch; not counted by the barriers
         tc_fence_before();
     }
 
