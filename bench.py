@@ -236,15 +236,129 @@ def make_case(workload: str):
         return wl.topk_config(workload)
     if workload in wl.PAGED_CONFIGS:
         return wl.paged_config(workload)
+    if workload in wl.MX_CONFIGS:
+        return wl.mx_config(workload)
     if workload not in wl.DENSE_CONFIGS:
         raise SystemExit(f"unknown workload {workload!r}; known: "
-                         f"{sorted(wl.DENSE_CONFIGS) + sorted(wl.PAGED_CONFIGS) + sorted(wl.TOPK_CONFIGS)}")
+                         f"{sorted(wl.DENSE_CONFIGS) + sorted(wl.PAGED_CONFIGS) + sorted(wl.TOPK_CONFIGS) + sorted(wl.MX_CONFIGS)}")
     return wl.dense_config(workload)
 
 
 def is_paged(workload: str) -> bool:
     from fp8_mqa_indexer_gb300 import workloads as wl
     return workload in wl.PAGED_CONFIGS
+
+
+def is_mx(workload: str) -> bool:
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    return workload in wl.MX_CONFIGS
+
+
+# The pages' MXFP8 timings ("[PR #435] ...", section "Performance": GB200, 152
+# SMs, all-zero input, clean fp32 logits, CUDA-graph median per call), as
+# TFLOP/s of this benchmark's metric (valid logits x 2 * H * D).
+MX_PUBLISHED_US = {"mx_2k_32k_h64_d128_zeros": 412.0, "mx_8k_64k_h64_d128_zeros": 3022.2}
+
+
+def bench_mx(args, mqa, torch, dev, stream):
+    """MXFP8 dense logits (block-scaled tcgen05 MMA); the shapes of the pages'
+    MXFP8 timings."""
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    case = wl.mx_config(args.workload)
+    i = torch.arange(case.S_q, dtype=torch.int64)
+    valid = int((case.k_end.to(torch.int64).clamp(max=case.S_kv)
+                 - case.k_start.to(torch.int64).clamp(min=0)).clamp(min=0).sum())
+    flops = valid * 2.0 * case.H * 128
+    d = [t.to(dev) for t in (case.q, case.q_sf, case.kv, case.kv_sf, case.weights, case.k_start,
+                             case.k_end)]
+    out = torch.empty((case.S_q, case.ldo), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(o=out):
+        mqa.mqa_logits_mx(*d, o)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert mqa.device_status() == 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[0].strip() if vis else "0")
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    assert mqa.device_status() == 0
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_per_step = sum(times_ms) / args.steps
+    value = flops / (ms_per_step * 1e-3) / 1e12
+    graph = None
+    if not args.no_graph:
+        graph = graph_timing(torch, step, out)
+        graph["tflops_at_median"] = flops / (graph["median_ms"] * 1e-3) / 1e12
+
+    host = [t.pin_memory() for t in (case.q, case.q_sf, case.kv, case.kv_sf, case.weights,
+                                     case.k_start, case.k_end)]
+    host_out = torch.empty((case.S_q, case.ldo), dtype=torch.float32, pin_memory=True)
+
+    def e2e_step():
+        dd = [h.to(dev, non_blocking=True) for h in host]
+        mqa.mqa_logits_mx(*dd, out)
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+
+    peaks, peaks_src = load_peaks()
+    nominal_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    fp8 = None if args.no_fp8_peak else measure_fp8_peak(torch, dev)
+    peak = fp8["burst_tflops"] if fp8 else nominal_peak
+    published = MX_PUBLISHED_US.get(args.workload)
+    pub_tflops = flops / (published * 1e-6) / 1e12 if published else None
+    if graph and pub_tflops:
+        graph["vs_published_median"] = graph["tflops_at_median"] / pub_tflops
+    line = {
+        "metric": "MQA logits TFLOP/s (valid logits x 2*H*D)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": value / pub_tflops if pub_tflops else None,
+        "dtype": "mxfp8 (e4m3 x e4m3, ue8m0 block 32) -> f32", "data": "synthetic",
+        "config": {"workload": args.workload, "S_q": case.S_q, "S_kv": case.S_kv, "H": case.H,
+                   "D": 128, "valid_logits": valid, "clean": True,
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "baseline": (f"{published} us on GB200 (the pages' MXFP8 figure, all-zero input, "
+                                f"graph median) = {pub_tflops:.0f} TFLOP/s" if published else None)},
+        **percentiles(times_ms),
+        "graph_timing": graph,
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / peak, "traffic": None,
+                     "peak_source": ("measured fp8 (cuBLAS e4m3 GEMM burst on this GPU)" if fp8 else
+                                     f"{peaks_src} bf16 burst x {FP8_PER_BF16} (nominal fp8:bf16)"),
+                     "peak_bf16x2": nominal_peak, "frac_bf16x2": value / nominal_peak},
+        "fp8_peak": fp8,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
+                "d2h_bytes_per_step": host_out.numel() * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def is_topk(workload: str) -> bool:
@@ -716,6 +830,10 @@ def main():
         if world > 1:
             raise SystemExit("the paged workload is measured on one GPU")
         return bench_paged(args, mqa, torch, dev, torch.cuda.current_stream())
+    if is_mx(args.workload):
+        if world > 1:
+            raise SystemExit("the MX workloads are measured on one GPU")
+        return bench_mx(args, mqa, torch, dev, torch.cuda.current_stream())
 
     case = make_case(args.workload)
     valid = int(case.valid_counts().sum())

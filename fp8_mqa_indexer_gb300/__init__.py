@@ -20,7 +20,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "MQAError", "mqa_logits", "mqa_logits_metadata", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
+    "MQAError", "mqa_logits", "mqa_logits_metadata", "mqa_logits_mx", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
     "paged_mqa_logits_noalloc", "mqa_topk_indices", "paged_mqa_topk_indices",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
     "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS",
@@ -68,6 +68,7 @@ def load_library() -> ctypes.CDLL:
             "mqa_logits": ([P, P, P, P, P, P, P, I, I, I, I, I64, U, P], I),
             "mqa_logits_scheduled": ([P, P, P, P, P, P, P, I, P, I, I, I, I, I64, U, P], I),
             "mqa_logits_metadata": ([P, P, I, I, I, I, P, P], I),
+            "mqa_logits_mx": ([P, P, P, P, P, P, P, P, I, I, I, I, I64, U, P], I),
             "paged_mqa_logits_metadata": ([P, I, I, I, I, P, P], I),
             "paged_mqa_logits": ([P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I64, U, P], I),
             "paged_mqa_logits_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I64, U, P], I),
@@ -174,6 +175,53 @@ def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: 
                 _ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights), _ptr(k_start), _ptr(k_end),
                 _ptr(schedule_meta), schedule_meta.shape[0] - 1, _ptr(logits), S_q, S_kv, H, D,
                 ldo, flags, _stream_handle(stream)))
+    return logits
+
+
+def mqa_logits_mx(q, q_sf, kv, kv_sf, weights, k_start, k_end, logits=None, *, clean: bool = True,
+                  compressed: bool = False, ldo: Optional[int] = None, check_bounds: bool = False,
+                  stream=None):
+    """Dense MQA logits with MXFP8 inputs (C ABI ``mqa_logits_mx``).
+
+    q [S_q, H, 128] and kv [S_kv, 128] E4M3 (float8_e4m3fn or uint8 bytes);
+    q_sf [S_q, H] and kv_sf [S_kv] int32 (or uint32 bit patterns): four UE8M0
+    block scales each, byte b for elements [32 b, 32 b + 32); weights, ranges
+    and output as ``mqa_logits``.
+    """
+    import torch
+    f8 = _fp8_types()
+    _dev(q, "q", f8)
+    _dev(kv, "kv", f8)
+    _dev(q_sf, "q_sf", (torch.int32,))
+    _dev(kv_sf, "kv_sf", (torch.int32,))
+    _dev(weights, "weights", (torch.float32,))
+    _dev(k_start, "k_start", (torch.int32,))
+    _dev(k_end, "k_end", (torch.int32,))
+    if q.dim() != 3 or kv.dim() != 2:
+        raise ValueError("q must be [S_q, H, D] and kv [S_kv, D]")
+    S_q, H, D = q.shape
+    S_kv = kv.shape[0]
+    if kv.shape[1] != D or weights.shape != (S_q, H) or q_sf.shape != (S_q, H):
+        raise ValueError("shape mismatch between q, q_sf, kv and weights")
+    if kv_sf.shape != (S_kv,) or k_start.shape != (S_q,) or k_end.shape != (S_q,):
+        raise ValueError("shape mismatch in kv_sf / k_start / k_end")
+    if logits is None:
+        if ldo is None:
+            if compressed:
+                raise ValueError("compressed output needs ldo (the longest range) or a logits buffer")
+            ldo = S_kv
+        logits = torch.empty((S_q, ldo), dtype=torch.float32, device=q.device)
+    else:
+        if not (logits.is_cuda and logits.dtype == torch.float32 and logits.dim() == 2
+                and logits.stride(1) == 1 and logits.shape[0] == S_q):
+            raise ValueError("logits must be a CUDA float32 [S_q, ldo] matrix with unit column stride")
+        ldo = logits.stride(0) if ldo is None else ldo
+    flags = (MQA_CLEAN if clean else 0) | (MQA_COMPRESSED if compressed else 0) | \
+            (MQA_CHECK_BOUNDS if check_bounds else 0)
+    with torch.cuda.device(q.device):
+        _check(load_library().mqa_logits_mx(_ptr(q), _ptr(q_sf), _ptr(kv), _ptr(kv_sf), _ptr(weights),
+                                            _ptr(k_start), _ptr(k_end), _ptr(logits), S_q, S_kv, H,
+                                            D, ldo, flags, _stream_handle(stream)))
     return logits
 
 

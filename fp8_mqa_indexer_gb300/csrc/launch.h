@@ -23,12 +23,13 @@ struct LaunchArgs {
 // Both return cudaErrorNotSupported for an (H, D) pair without an instance.
 cudaError_t launch_dense(int H, int D, const LaunchArgs& a);
 cudaError_t launch_paged(int H, int D, const LaunchArgs& a);
+cudaError_t launch_dense_mx(int H, const LaunchArgs& a);
 
-template <int H, int D, bool PAGED>
+template <int H, int D, bool PAGED, bool MX = false>
 cudaError_t launch_instance(const LaunchArgs& a)
 {
-    auto kern = mqa_logits_kernel<H, D, PAGED>;
-    const size_t smem = sizeof(Smem<D>) + 1024;
+    auto kern = mqa_logits_kernel<H, D, PAGED, MX>;
+    const size_t smem = sizeof(Smem<D, MX>) + 1024;
     // The shared-memory limit is a per-device attribute of the function: set it
     // once on each device (one bit per device; setting it twice is harmless).
     static std::atomic<unsigned long long> attr_set{0};

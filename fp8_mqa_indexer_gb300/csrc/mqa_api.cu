@@ -424,11 +424,14 @@ mqa_status paged_mqa_logits_metadata(const int32_t* context_lens, int B, int nex
 namespace {
 // mqa_logits and mqa_logits_scheduled: `schedule_meta` (num_sms + 1 entries
 // from mqa_logits_metadata) or null for the in-kernel split.
+// MX calls pass q_sf and kv_sf (UE8M0 block scales) and no kv_scale.
 mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, const float* weights,
                       const int32_t* k_start, const int32_t* k_end, const int32_t* schedule_meta,
                       int sched_sms, float* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
-                      unsigned flags, cudaStream_t stream)
+                      unsigned flags, cudaStream_t stream, const uint32_t* q_sf = nullptr,
+                      const uint32_t* kv_sf = nullptr)
 {
+    const bool mx = q_sf != nullptr || kv_sf != nullptr;
     const bool compressed = (flags & MQA_COMPRESSED) != 0;
     const bool clean = (flags & MQA_CLEAN) != 0;
     if (flags & ~(unsigned)(MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS))
@@ -447,10 +450,21 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
         return fail(MQA_ERR_INVALID_ARG, "compressed output needs ldo >= 1");
     if (S_q == 0)
         return MQA_OK;
-    if (!q || !weights || !k_start || !k_end || !logits || (S_kv > 0 && (!kv || !kv_scale)))
+    if (mx) {
+        if (D != 128)
+            return fail(MQA_ERR_UNSUPPORTED, "MX calls need D = 128 (four 32-element blocks)");
+        if (schedule_meta)
+            return fail(MQA_ERR_UNSUPPORTED, "MX calls take no schedule");
+        if (!q_sf || (S_kv > 0 && !kv_sf))
+            return fail(MQA_ERR_INVALID_ARG, "null pointer");
+        if (!aligned(q_sf, 4) || (S_kv > 0 && !aligned(kv_sf, 16)))
+            return fail(MQA_ERR_INVALID_ARG, "q_sf must be 4-byte and kv_sf 16-byte aligned");
+    }
+    if (!q || !weights || !k_start || !k_end || !logits ||
+        (S_kv > 0 && (!kv || (!mx && !kv_scale))))
         return fail(MQA_ERR_INVALID_ARG, "null pointer");
-    if (!aligned(q, 16) || !aligned(weights, 16) || (S_kv > 0 && (!aligned(kv, 16) ||
-                                                                   !aligned(kv_scale, 16))))
+    if (!aligned(q, 16) || !aligned(weights, 16) ||
+        (S_kv > 0 && (!aligned(kv, 16) || (!mx && !aligned(kv_scale, 16)))))
         return fail(MQA_ERR_INVALID_ARG, "q, kv, kv_scale and weights must be 16-byte aligned");
     if (!aligned(logits, 4) || !aligned(k_start, 4) || !aligned(k_end, 4))
         return fail(MQA_ERR_INVALID_ARG, "logits, k_start, k_end must be 4-byte aligned");
@@ -508,14 +522,17 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
 
     LaunchArgs a;
     memset(&a, 0, sizeof(a));
-    const int tok = kMaxN / H;
+    // MX: 192 accumulator columns per unit (room for the scale factors in TMEM)
+    const int tok = (mx ? kMxN : kMaxN) / H;
     const int N = tok * H;
     const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if ((s = make_map_2d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (unsigned long long)S_q * H, D,
                          N, D, swz, "q")) != MQA_OK ||
         (s = make_map_2d(&a.tm_kv, kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, S_kv, D, kBlockKV, D, swz,
                          "kv")) != MQA_OK ||
-        (s = make_map_vec_f32(&a.tm_scale, kv_scale, S_kv, kBlockKV, "kv_scale")) != MQA_OK ||
+        // MX: a valid map over the key scales, never used for copies
+        (s = make_map_vec_f32(&a.tm_scale, mx ? (const void*)kv_sf : (const void*)kv_scale, S_kv,
+                              kBlockKV, "kv_scale")) != MQA_OK ||
         (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, S_q, H, tok, H,
                          CU_TENSOR_MAP_SWIZZLE_NONE, "weights")) != MQA_OK)
         return s;
@@ -529,6 +546,8 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     p.k_start = k_start;
     p.k_end = k_end;
     p.schedule_meta = schedule_meta;
+    p.q_sf = q_sf;
+    p.kv_sf = kv_sf;
     p.width = S_kv;
     p.width_i = S_kv;
     p.tok = tok;
@@ -540,7 +559,7 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     p.status = st;
     a.grid = num_sms;
     a.stream = stream;
-    cudaError_t e = launch_dense(H, D, a);
+    cudaError_t e = mx ? launch_dense_mx(H, a) : launch_dense(H, D, a);
     if (e == cudaErrorNotSupported)
         return fail(MQA_ERR_UNSUPPORTED, "no dense kernel for H=%d D=%d", H, D);
     if (e != cudaSuccess)
@@ -567,6 +586,19 @@ mqa_status mqa_logits_scheduled(const void* q, const void* kv, const float* kv_s
         return fail(MQA_ERR_INVALID_ARG, "null schedule_meta");
     return dense_call(q, kv, kv_scale, weights, k_start, k_end, schedule_meta, num_sms, logits,
                       S_q, S_kv, H, D, ldo, flags, (cudaStream_t)stream);
+}
+
+mqa_status mqa_logits_mx(const void* q, const uint32_t* q_sf, const void* kv, const uint32_t* kv_sf,
+                         const float* weights, const int32_t* k_start, const int32_t* k_end,
+                         float* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
+                         unsigned flags, mqa_stream_t stream)
+{
+    if (flags & MQA_MXFP4)
+        return fail(MQA_ERR_UNSUPPORTED, "MXFP4 elements are not supported by this library yet");
+    if (!q_sf || !kv_sf)
+        return fail(MQA_ERR_INVALID_ARG, "null scale pointer");
+    return dense_call(q, kv, nullptr, weights, k_start, k_end, nullptr, 0, logits, S_q, S_kv, H, D,
+                      ldo, flags, (cudaStream_t)stream, q_sf, kv_sf);
 }
 
 mqa_status mqa_logits_metadata(const int32_t* k_start, const int32_t* k_end, int S_q, int S_kv,

@@ -106,6 +106,10 @@ struct Params {
     int blk_stride;      // output rows between query blocks: tok (dense) or next_n (paged)
     int num_q_blocks;    // dense: ceil(S_q / tok); paged: B
     int rows;            // output rows: S_q or B * next_n
+    // MX (block-scaled) dense calls: UE8M0 scales, four per int32, byte b for
+    // elements [32 b, 32 b + 32) of a row
+    const uint32_t* q_sf;    // [S_q * H]
+    const uint32_t* kv_sf;   // [S_kv]
     long long wait_limit;
     unsigned* status;
 };
@@ -117,7 +121,15 @@ struct Cfg {
     static constexpr int kQTileBytes = kMaxN * D;
 };
 
-template <int D>
+// MX calls: accumulator columns of a unit (three tokens at H = 64), so that the
+// two 256-column buffers leave room in TMEM for the scale factors, which sit
+// at columns kMxSfCol.. of the first buffer's unused tail: SFA in two slots of
+// four columns (by unit parity), SFB in two slots of eight (by query buffer).
+constexpr int kMxN = 192;
+constexpr int kMxSfaCol = kMxN;          // 192..199
+constexpr int kMxSfbCol = kMxN + 8;      // 200..215
+
+template <int D, bool MX = false>
 struct __align__(1024) Smem {
     uint8_t q[2][Cfg<D>::kQTileBytes];
     uint8_t kv[Cfg<D>::kStages][Cfg<D>::kKVTileBytes];
@@ -139,6 +151,11 @@ struct __align__(1024) Smem {
     int n_units;
     long long scan[kThreads / 32];
     TokRow tokrow[kNumEpiWarps][kMaxTokW];   // per epilogue warp: its tokens' rows
+    // MX: scale factors laid out for tcgen05.cp (32 rows x 16 bytes, row r
+    // word j = the scales of matrix row 32 j + r): per key-tile stage (A =
+    // keys) and per query buffer, in two halves of 128 rows (B = token x head)
+    alignas(16) uint32_t sfa[MX ? Cfg<D>::kStages : 1][32][4];
+    alignas(16) uint32_t sfb[MX ? 2 : 1][2][32][4];
 };
 
 // ----------------------------------------------------------------- ranges
@@ -265,7 +282,7 @@ constexpr unsigned kMmaSleepNs = 0;
 // ReLU(y) = (y + |y|) / 2 instead: it accumulates A = sum w x and
 // B = sum w |x| and forms (s A + |s| B) / 2, which equals sum w ReLU(s x) for
 // either sign of s.
-template <int H, int D>
+template <int H, int D, bool MX = false>
 struct Epilogue {
     static_assert(H >= 8 && H <= kEpiCols, "a warp's columns must hold whole tokens");
     using C = Cfg<D>;
@@ -279,7 +296,7 @@ struct Epilogue {
         float s;
     };
 
-    Smem<D>& sm;
+    Smem<D, MX>& sm;
     const Params& p;
     const WaitCtx& wctx;
     uint32_t tmem_lane;   // TMEM address of this warp's lanes and first column
@@ -334,7 +351,8 @@ struct Epilogue {
         if (!warp_wait_fast(smem_u32(&sm.full[stage]), phase, wctx))
             return false;
         st.info = sm.info[stage];
-        st.s = sm.scale[stage][row];
+        // MX: the block scales are applied inside the MMA; no per-key scale
+        st.s = MX ? 1.f : sm.scale[stage][row];
         if (st.info.flags & kFirstOfBlock) {
             ++k_block;
             if (!warp_wait_fast(smem_u32(&sm.q_full[st.info.qbuf]), (k_block >> 1) & 1, wctx))
@@ -397,7 +415,7 @@ struct Epilogue {
                 float v;
                 if constexpr (POS) {
                     const float2 t = __fadd2_rn(a0, a1);
-                    v = st.s * (t.x + t.y);
+                    v = MX ? t.x + t.y : st.s * (t.x + t.y);
                 } else {
                     v = 0.5f * fmaf(st.s, a0.x + a0.y, fabsf(st.s) * (b0.x + b0.y));
                 }
@@ -484,7 +502,8 @@ struct Epilogue {
 };
 
 // ------------------------------------------------------------------ kernel
-template <int H, int D, bool PAGED>
+// MX = true: MXFP8 dense call (block-scaled E4M3 MMA, no per-key fp32 scale).
+template <int H, int D, bool PAGED, bool MX = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_kv,
@@ -505,7 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // through `sm` stays a shared-memory access (no generic addressing).
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-    Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw + pad);
+    Smem<D, MX>& sm = *reinterpret_cast<Smem<D, MX>*>(smem_raw + pad);
+    static_assert(!MX || (!PAGED && D == 128), "MX calls are dense with D = 128");
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -673,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // quantisation factors) the epilogue runs the ReLU-by-FMNMX form only and
     // skips the per-unit sign vote.  The paged pool is not scanned.
     int any_neg = PAGED ? 1 : 0;
-    if (!PAGED) {
+    if (!PAGED && !MX) {
         const int n4 = p.S_kv >> 2;
         const float4* s4 = reinterpret_cast<const float4*>(p.kv_scale);
         for (int k = tid; k < n4; k += kThreads) {
@@ -735,6 +755,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 if (lane < p.tok)
                     sm.range[qb][lane] = myrange;
+                if constexpr (MX) {
+                    // the block's B-operand scales, transposed for tcgen05.cp:
+                    // half c, row r, word j <- column n = 128 c + 32 j + r
+                    const long long r0 = (long long)(b * p.blk_stride + p.tok0) * H;
+                    const long long nq = (long long)p.S_q * H;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t v[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int n = 128 * c + 32 * j + lane;
+                            v[j] = (n < N && r0 + n < nq) ? __ldg(p.q_sf + r0 + n) : 0x7f7f7f7fu;
+                        }
+                        *reinterpret_cast<uint4*>(&sm.sfb[qb][c][lane][0]) =
+                            make_uint4(v[0], v[1], v[2], v[3]);
+                    }
+                    fence_proxy_async_smem();   // read by tcgen05.cp (async proxy)
+                }
                 __syncwarp();
                 if (lane == 0) {
                     const uint32_t bar = smem_u32(&sm.q_full[qb]);
@@ -747,6 +785,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++q_issued;
             }
             const int stage = u % S;
+            uint32_t ksf[4];
+            if constexpr (MX) {
+                // the tile's key scales, loaded before the wait for the stage
+                // (the wait hides their latency): word j <- key 32 j + lane
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int key = t * kBlockKV + 32 * j + lane;
+                    ksf[j] = key < p.S_kv ? __ldg(p.kv_sf + key) : 0x7f7f7f7fu;
+                }
+            }
             if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx, kProducerSleepNs))
                 break;
             const bool last = (u + 1 == n_units) || (t + 1 >= thi);
@@ -793,6 +841,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wbase += 32;
                     win0 = win1;
                     win1 = page_id(wbase + 32 + lane);
+                }
+            } else if constexpr (MX) {
+                *reinterpret_cast<uint4*>(&sm.sfa[stage][lane][0]) =
+                    make_uint4(ksf[0], ksf[1], ksf[2], ksf[3]);
+                fence_proxy_async_smem();   // read by tcgen05.cp (async proxy)
+                __syncwarp();
+                if (lane == 0) {
+                    sm.info[stage] = info;
+                    const uint32_t bar = smem_u32(&sm.full[stage]);
+                    mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * D));
+                    tma_load_2d(smem_u32(sm.kv[stage]), &tm_kv, bar, 0, t * kBlockKV);
                 }
             } else {
                 if (lane == 0) {
@@ -857,9 +916,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // buffer, 32 bytes of K per MMA
                 const uint64_t da = desc_kv0 + (uint64_t)(stage * (C::kKVTileBytes >> 4));
                 const uint64_t db = desc_q0 + (uint64_t)(info.qbuf * (C::kQTileBytes >> 4));
+                if constexpr (MX) {
+                    // scale factors into TMEM (in issue order before the MMAs
+                    // that read them): the key tile's into the slot of this
+                    // unit's parity, the query block's at its first unit
+                    const uint32_t sfa_t = tmem_base + kMxSfaCol + (uint32_t)((u & 1) * 4);
+                    const uint32_t sfb_t = tmem_base + kMxSfbCol + (uint32_t)(info.qbuf * 8);
+                    tmem_cp_32x128b_x4(sfa_t, sf_desc(smem_u32(&sm.sfa[stage][0][0])));
+                    if (info.flags & kFirstOfBlock) {
+                        tmem_cp_32x128b_x4(sfb_t, sf_desc(smem_u32(&sm.sfb[info.qbuf][0][0][0])));
+                        tmem_cp_32x128b_x4(sfb_t + 4, sf_desc(smem_u32(&sm.sfb[info.qbuf][1][0][0])));
+                    }
 #pragma unroll
-                for (int k = 0; k < D / 32; ++k)
-                    mma_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < D / 32; ++k)
+                        mma_mxf8f6f4(d_tmem, da + 2 * k, db + 2 * k,
+                                     idesc_mx_e4m3_f32(kBlockKV, (uint32_t)N, (uint32_t)k), sfa_t, sfb_t,
+                                     k > 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < D / 32; ++k)
+                        mma_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
+                }
                 mma_commit(smem_u32(&sm.empty[stage]));
                 mma_commit(smem_u32(&sm.acc_full[buf]));
                 if (info.flags & kLastOfBlock)
@@ -912,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tpg = kEpiCols / H;                   // tokens per group
         const int tok0 = g * tpg;
         const int ntok = max(0, min(tpg, p.tok - tok0));
-        Epilogue<H, D> epi{sm, p, wctx,
+        Epilogue<H, D, MX> epi{sm, p, wctx,
                            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * kEpiCols),
                            n_units, quad * 32 + lane, g * kEpiCols, tok0, ntok, warp - kEpiWarp0};
         const int nc = ntok * H;   // columns holding tokens, rounded up below

@@ -272,6 +272,48 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] (+)= (A * SFA)[smem] * (B * SFB)[smem]^T: MXFP8 (E4M3 elements,
+// one UE8M0 scale per 32 elements of K, "scale_vec::1X"), FP32 accumulation.
+// The scale factors are read from TMEM: for row m of A (M = 128), lane m,
+// column sfa + m / 32; for row n of B, lane n % 32 of every lane quadrant,
+// column sfb + n / 32; in either cell the byte given by the instruction
+// descriptor's scale-factor ids (idesc_mx_e4m3_f32).  This placement was read
+// off the hardware with all-ones operands and coded scale bytes.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                             uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 32 rows x 128 bits of shared memory (described by sf_desc) -> TMEM lanes
+// r, r + 32, r + 64, r + 96 (every lane quadrant), four 32-bit columns from
+// `taddr`: row r word j lands in column taddr + j.  Asynchronous, ordered
+// with the issuing thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc)
+                 : "memory");
+}
+
+// Descriptor of a tcgen05.cp source: 32 rows of 16 bytes, one after another
+// (no swizzle; eight-row core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= static_cast<uint64_t>(128 >> 4) << 16;            // leading byte offset
+    d |= static_cast<uint64_t>(128 >> 4) << 32;            // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+    return d;
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
@@ -303,6 +345,19 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N)
            | (0u << 7) | (0u << 10)  // A, B format: E4M3
            | ((N >> 3) << 17)        // N / 8
            | ((M >> 4) << 24);       // M / 16
+}
+
+// Instruction descriptor of the block-scaled MMA (kind::mxf8f6f4): E4M3 x
+// E4M3 -> F32, K-major, M x N, UE8M0 scales; scale-factor id `sf` (the byte
+// of each scale cell) for both operands: the K-block of this MMA.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3_f32(uint32_t M, uint32_t N, uint32_t sf)
+{
+    return (sf << 4)                 // B scale-factor id
+           | (0u << 7) | (0u << 10)  // A, B format: E4M3
+           | ((N >> 3) << 17)        // N / 8
+           | (1u << 23)              // scale type: UE8M0
+           | ((M >> 4) << 24)        // M / 16
+           | (sf << 29);             // A scale-factor id
 }
 
 // 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per

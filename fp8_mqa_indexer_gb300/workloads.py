@@ -370,3 +370,32 @@ def mx_dense_case(S_q: int, S_kv: int, H: int, *, seed: int, fp4: bool = False,
     else:
         raise ValueError(ranges)
     return MxDenseCase(name, q, q_sf, kv, kv_sf, weights, ks.contiguous(), ke.contiguous(), fp4, S_kv)
+
+
+def mx_zero_case(S_q: int, S_kv: int, H: int, *, name: str = "mx_zeros") -> MxDenseCase:
+    """The PR #435 reproducer's MXFP8 input: all-zero q, k and weights, every
+    scale byte 127 (0x7f7f7f7f: one), rows [0, S_kv - S_q + i)."""
+    D = 128
+    i = torch.arange(S_q, dtype=torch.int32)
+    one = torch.tensor(0x7F7F7F7F, dtype=torch.int32)
+    return MxDenseCase(name, torch.zeros((S_q, H, D), dtype=torch.uint8),
+                       one.repeat(S_q * H).reshape(S_q, H), torch.zeros((S_kv, D), dtype=torch.uint8),
+                       one.repeat(S_kv), torch.zeros((S_q, H)), torch.zeros_like(i),
+                       (S_kv - S_q + i).contiguous(), False, S_kv)
+
+
+# The MXFP8 timing shapes of "[PR #435] ...", section "Performance" (seeded
+# random elements and scales; "_zeros": the reproducer's all-zero input).
+MX_CONFIGS = {
+    "mx_2k_32k_h64_d128": dict(S_q=2048, S_kv=32768, H=64, seed=1010),
+    "mx_8k_64k_h64_d128": dict(S_q=8192, S_kv=65536, H=64, seed=1011),
+    "mx_2k_32k_h64_d128_zeros": dict(S_q=2048, S_kv=32768, H=64, zeros=True),
+    "mx_8k_64k_h64_d128_zeros": dict(S_q=8192, S_kv=65536, H=64, zeros=True),
+}
+
+
+def mx_config(name: str) -> MxDenseCase:
+    kw = dict(MX_CONFIGS[name])
+    if kw.pop("zeros", False):
+        return mx_zero_case(kw["S_q"], kw["S_kv"], kw["H"], name=name)
+    return mx_dense_case(kw["S_q"], kw["S_kv"], kw["H"], seed=kw["seed"], name=name)

@@ -96,6 +96,32 @@ MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_sca
                       int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
 
 /*
+ * Dense MQA logits with MXFP8 inputs ("[PR #435] Improve SM100 MX MQA logits
+ * clean-output performance": sections "Performance" (MXFP8 timings at H=64,
+ * D=128) and "Standalone performance reproducer" (q [S_q, H, D] with q_sf
+ * [S_q, H] int32, k [S_kv, D] with ks [S_kv] int32, 0x7f7f7f7f = unit scales)).
+ *
+ *   logits[i, j] = sum_h w[i,h] * ReLU(x),  x = sum_b 2^(eq_b - 127) * 2^(ek_b - 127)
+ *                                              * sum_{d in block b} q[i,h,d] * kv[j,d]
+ *
+ *   q        [S_q, H, 128] E4M3 bytes, 16-byte aligned
+ *   q_sf     [S_q, H] uint32: byte b (b = 0..3, little end first) is the UE8M0
+ *            scale eq_b of elements [32 b, 32 b + 32) of q[i,h,:]; 4-byte aligned
+ *   kv       [S_kv, 128] E4M3 bytes, 16-byte aligned
+ *   kv_sf    [S_kv] uint32, the same for kv[j,:]; 16-byte aligned
+ *   weights, k_start, k_end, logits, ldo, flags: as mqa_logits.
+ *   D must be 128; H in {8, 32, 64}.  A scale byte of 255 (not a number in
+ *   UE8M0) is not allowed.  flags may not hold MQA_MXFP4 (MXFP4 elements: not
+ *   supported yet, MQA_ERR_UNSUPPORTED).
+ */
+enum { MQA_MXFP4 = 8u };
+MQA_API mqa_status mqa_logits_mx(const void *q, const uint32_t *q_sf, const void *kv,
+                                 const uint32_t *kv_sf, const float *weights,
+                                 const int32_t *k_start, const int32_t *k_end, float *logits,
+                                 int S_q, int S_kv, int H, int D, int64_t ldo, unsigned flags,
+                                 mqa_stream_t stream);
+
+/*
  * Work schedule for a dense call ("[PR #435] Improve SM100 MX MQA logits
  * clean-output performance": the reproducer computes get_mqa_logits_metadata
  * once outside the timed region and passes it to the logits call as

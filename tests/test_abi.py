@@ -236,3 +236,12 @@ def test_scheduled_dense_rejects_invalid_arguments(lib):
     assert call(D=96) == 2
     assert call(num_sms=0) == 1
     assert call(meta=F + 2) == 1
+
+
+@pytest.mark.parametrize("kw,status", [(dict(D=64), 2), (dict(flags=1 | 8), 2), (dict(q_sf=None), 1),
+                                       (dict(kv_sf=F + 4), 1), (dict(H=16), 2), (dict(ldo=255), 1)])
+def test_mx_rejects_invalid_arguments(lib, kw, status):
+    a = dict(q=F, q_sf=F, kv=F, kv_sf=F, D=128, H=64, ldo=256, flags=1)
+    a.update(kw)
+    assert lib.mqa_logits_mx(a["q"], a["q_sf"], a["kv"], a["kv_sf"], F, F, F, F, 4, 256, a["H"],
+                             a["D"], a["ldo"], a["flags"], None) == status
