@@ -710,9 +710,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_units = sm.n_units;
     WaitCtx wctx{&sm.abort_flag, p.status, p.wait_limit};
 
-    if (warp == 0) {
+    // Paged calls have two producer warps (0 and 2), each issuing the copies of
+    // every other unit: a unit's page-id lookups and four copy requests keep
+    // one warp busy longer than the rest of the pipeline needs per unit.
+    constexpr int kProducers = PAGED ? 2 : 1;
+    if (warp == 0 || (PAGED && warp == 2)) {
         // ================================================= TMA producer
         regs_dec<kRegsCtl>();
+        const int pid = warp == 0 ? 0 : 1;   // units u with u % kProducers == pid are this warp's
         int b = sm.start_b;
         int t = sm.start_t;
         int k_block = 0;
@@ -746,9 +751,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n_units > 0)
             enter_block();
         bool first = true;
-        int n_issued = 0, q_issued = 0;
+        int u_end = 0;
+        int q_blk[2] = {-1, -1};   // the last two query blocks whose copies this warp issued
         for (int u = 0; u < n_units; ++u) {
-            if (first) {
+            u_end = u;
+            const bool mine = u % kProducers == pid;
+            if (first && mine) {
                 const int qb = k_block & 1;
                 if (!warp_wait(smem_u32(&sm.q_empty[qb]), ((k_block >> 1) & 1) ^ 1, wctx,
                                kProducerSleepNs))
@@ -782,87 +790,96 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(smem_u32(sm.q[qb]), &tm_q, bar, 0, row0 * H);
                     tma_load_2d(smem_u32(sm.w[qb]), &tm_w, bar, 0, row0);
                 }
-                ++q_issued;
+                q_blk[k_block & 1] = k_block;
             }
             const int stage = u % S;
             uint32_t ksf[4];
-            if constexpr (MX) {
-                // the tile's key scales, loaded before the wait for the stage
-                // (the wait hides their latency): word j <- key 32 j + lane
+            if (mine) {
+                if constexpr (MX) {
+                    // the tile's key scales, loaded before the wait for the stage
+                    // (the wait hides their latency): word j <- key 32 j + lane
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int key = t * kBlockKV + 32 * j + lane;
-                    ksf[j] = key < p.S_kv ? __ldg(p.kv_sf + key) : 0x7f7f7f7fu;
-                }
-            }
-            if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx, kProducerSleepNs))
-                break;
-            const bool last = (u + 1 == n_units) || (t + 1 >= thi);
-            const UnitInfo info{b, t, k_block & 1,
-                                (first ? kFirstOfBlock : 0) | (last ? kLastOfBlock : 0)};
-            if (PAGED) {
-                // gather the pages of tile t through the block table
-                const long long keys = min((long long)ctx, p.width);
-                int ids[4];
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    ids[k] = -1;
-                    if (k < ppt) {
-                        const int pg = t * ppt + k;
-                        if (pg < wbase || pg >= wbase + 32) {   // not sequential: reload
-                            wbase = pg & ~31;
-                            win0 = page_id(wbase + lane);
-                            win1 = page_id(wbase + 32 + lane);
-                        }
-                        const int id = __shfl_sync(0xffffffffu, win0, pg - wbase);
-                        if ((long long)pg * p.block_kv < keys && pg < p.max_blocks) {
-                            ids[k] = id;
-                            bytes += (uint32_t)(p.block_kv * (D + 4));
-                        }
+                    for (int j = 0; j < 4; ++j) {
+                        const int key = t * kBlockKV + 32 * j + lane;
+                        ksf[j] = key < p.S_kv ? __ldg(p.kv_sf + key) : 0x7f7f7f7fu;
                     }
                 }
-                if (lane == 0) {
-                    sm.info[stage] = info;
-                    const uint32_t bar = smem_u32(&sm.full[stage]);
-                    mbar_arrive_expect_tx(bar, bytes);
+                if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx, kProducerSleepNs))
+                    break;
+                const bool last = (u + 1 == n_units) || (t + 1 >= thi);
+                const UnitInfo info{b, t, k_block & 1,
+                                    (first ? kFirstOfBlock : 0) | (last ? kLastOfBlock : 0)};
+                if (PAGED) {
+                    // gather the pages of tile t through the block table
+                    const long long keys = min((long long)ctx, p.width);
+                    int ids[4];
+                    uint32_t bytes = 0;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        if (k < ppt && ids[k] >= 0) {
-                            tma_load_2d(smem_u32(sm.kv[stage]) + k * p.block_kv * D, &tm_kv, bar, 0,
-                                        ids[k] * p.block_kv);
-                            tma_load_2d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale, bar,
-                                        ids[k] * p.block_kv, 0);
+                        ids[k] = -1;
+                        if (k < ppt) {
+                            const int pg = t * ppt + k;
+                            if (pg < wbase || pg >= wbase + 32) {   // not sequential: reload
+                                wbase = pg & ~31;
+                                win0 = page_id(wbase + lane);
+                                win1 = page_id(wbase + 32 + lane);
+                            }
+                            const int id = __shfl_sync(0xffffffffu, win0, pg - wbase);
+                            if ((long long)pg * p.block_kv < keys && pg < p.max_blocks) {
+                                ids[k] = id;
+                                bytes += (uint32_t)(p.block_kv * (D + 4));
+                            }
                         }
                     }
+                    if (lane == 0) {
+                        sm.info[stage] = info;
+                        const uint32_t bar = smem_u32(&sm.full[stage]);
+                        mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (k < ppt && ids[k] >= 0) {
+                                tma_load_2d(smem_u32(sm.kv[stage]) + k * p.block_kv * D, &tm_kv, bar, 0,
+                                            ids[k] * p.block_kv);
+                                tma_load_2d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale, bar,
+                                            ids[k] * p.block_kv, 0);
+                            }
+                        }
+                    }
+                    // slide the window: the prefetched half becomes current
+                    if ((t + 1) * ppt >= wbase + 32) {
+                        wbase += 32;
+                        win0 = win1;
+                        win1 = page_id(wbase + 32 + lane);
+                    }
+                } else if constexpr (MX) {
+                    *reinterpret_cast<uint4*>(&sm.sfa[stage][lane][0]) =
+                        make_uint4(ksf[0], ksf[1], ksf[2], ksf[3]);
+                    fence_proxy_async_smem();   // read by tcgen05.cp (async proxy)
+                    __syncwarp();
+                    if (lane == 0) {
+                        sm.info[stage] = info;
+                        const uint32_t bar = smem_u32(&sm.full[stage]);
+                        mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * D));
+                        tma_load_2d(smem_u32(sm.kv[stage]), &tm_kv, bar, 0, t * kBlockKV);
+                    }
+                } else {
+                    if (lane == 0) {
+                        sm.info[stage] = info;
+                        const uint32_t bar = smem_u32(&sm.full[stage]);
+                        mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * D + kBlockKV * 4));
+                        tma_load_2d(smem_u32(sm.kv[stage]), &tm_kv, bar, 0, t * kBlockKV);
+                        tma_load_2d(smem_u32(sm.scale[stage]), &tm_scale, bar, t * kBlockKV, 0);
+                    }
                 }
-                // slide the window: the prefetched half becomes current
+            } else if (PAGED) {
+                // another producer's unit: keep the page window moving
                 if ((t + 1) * ppt >= wbase + 32) {
                     wbase += 32;
                     win0 = win1;
                     win1 = page_id(wbase + 32 + lane);
                 }
-            } else if constexpr (MX) {
-                *reinterpret_cast<uint4*>(&sm.sfa[stage][lane][0]) =
-                    make_uint4(ksf[0], ksf[1], ksf[2], ksf[3]);
-                fence_proxy_async_smem();   // read by tcgen05.cp (async proxy)
-                __syncwarp();
-                if (lane == 0) {
-                    sm.info[stage] = info;
-                    const uint32_t bar = smem_u32(&sm.full[stage]);
-                    mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * D));
-                    tma_load_2d(smem_u32(sm.kv[stage]), &tm_kv, bar, 0, t * kBlockKV);
-                }
-            } else {
-                if (lane == 0) {
-                    sm.info[stage] = info;
-                    const uint32_t bar = smem_u32(&sm.full[stage]);
-                    mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * D + kBlockKV * 4));
-                    tma_load_2d(smem_u32(sm.kv[stage]), &tm_kv, bar, 0, t * kBlockKV);
-                    tma_load_2d(smem_u32(sm.scale[stage]), &tm_scale, bar, t * kBlockKV, 0);
-                }
             }
-            ++n_issued;
+            u_end = u + 1;
             // advance to the next unit, skipping blocks with no work
             first = false;
             ++t;
@@ -882,10 +899,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Drain: every copy this warp issued must have landed before exit,
         // also when some role gave up (wait_drain ignores the abort flag).
         if (lane == 0) {
-            for (int u = max(0, n_issued - S); u < n_issued; ++u)
-                wait_drain(smem_u32(&sm.full[u % S]), (u / S) & 1, wctx);
-            for (int k = max(0, q_issued - 2); k < q_issued; ++k)
-                wait_drain(smem_u32(&sm.q_full[k & 1]), (k >> 1) & 1, wctx);
+            for (int u = max(0, u_end - S); u < u_end; ++u)
+                if (u % kProducers == pid)
+                    wait_drain(smem_u32(&sm.full[u % S]), (u / S) & 1, wctx);
+            // Only the last two query blocks can still be landing: an older
+            // block's buffer was reloaded after its consumers released it,
+            // which they did after its copy landed.  (With two producers a
+            // buffer's barrier may have moved past an older block's phase, so
+            // waiting on that phase would never end.)
+            for (int i = 0; i < 2; ++i)
+                if (q_blk[i] >= 0 && q_blk[i] >= k_block - 1)
+                    wait_drain(smem_u32(&sm.q_full[q_blk[i] & 1]), (q_blk[i] >> 1) & 1, wctx);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -952,10 +976,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================= -inf fill
         regs_dec<kRegsCtl>();
         if (p.flags & kFlagClean) {
-            const int fw = warp - 2;   // 0 or 1
+            // fill warps: 2 and 3 (dense); 3 alone (paged: warp 2 produces)
+            constexpr int nfw = PAGED ? 1 : 2;
+            const int fw = warp - (kEpiWarp0 - nfw);
             // paged: the rows of this launch's query atom only
             const int nrows = PAGED ? p.B * p.tok : p.rows;
-            for (int rr = cta + fw * G; rr < nrows; rr += 2 * G) {
+            for (int rr = cta + fw * G; rr < nrows; rr += nfw * G) {
                 const int r = PAGED ? (rr / p.tok) * p.next_n + p.tok0 + rr % p.tok : rr;
                 float* row = p.logits + (long long)r * p.ldo;
                 if (PAGED) {
