@@ -23,12 +23,13 @@ __all__ = [
     "MQAError", "mqa_logits", "mqa_logits_metadata", "mqa_logits_mx", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
     "paged_mqa_logits_noalloc", "mqa_topk_indices", "paged_mqa_topk_indices",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
-    "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS",
+    "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS", "MQA_OUT_BF16",
 ]
 
 MQA_CLEAN = 1
 MQA_COMPRESSED = 2
 MQA_CHECK_BOUNDS = 4
+MQA_OUT_BF16 = 16
 
 STATUS_NAMES = {0: "MQA_OK", 1: "MQA_ERR_INVALID_ARG", 2: "MQA_ERR_UNSUPPORTED", 3: "MQA_ERR_CUDA",
                 4: "MQA_ERR_TIMEOUT", 5: "MQA_ERR_BAD_INPUT"}
@@ -118,6 +119,29 @@ def _dev(t, name: str, dtypes) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def _dense_out(logits, S_q, ldo, compressed, S_kv, out_dtype, device):
+    """The [S_q, ldo] output (allocated if None) and its flag bits."""
+    import torch
+    if logits is None:
+        dt = torch.float32 if out_dtype is None else out_dtype
+        if dt not in (torch.float32, torch.bfloat16):
+            raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+        if ldo is None:
+            if compressed:
+                raise ValueError("compressed output needs ldo (the longest range) or a logits buffer")
+            ldo = S_kv
+        logits = torch.empty((S_q, ldo), dtype=dt, device=device)
+    else:
+        if not (logits.is_cuda and logits.dtype in (torch.float32, torch.bfloat16)
+                and logits.dim() == 2 and logits.stride(1) == 1 and logits.shape[0] == S_q):
+            raise ValueError("logits must be a CUDA float32 or bfloat16 [S_q, ldo] matrix with unit "
+                             "column stride")
+        if out_dtype is not None and out_dtype != logits.dtype:
+            raise ValueError("out_dtype differs from the logits buffer's dtype")
+        ldo = logits.stride(0) if ldo is None else ldo
+    return logits, ldo, (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0)
+
+
 def _fp8_types():
     import torch
     return (torch.float8_e4m3fn, torch.uint8)
@@ -125,14 +149,15 @@ def _fp8_types():
 
 def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: bool = True,
                compressed: bool = False, ldo: Optional[int] = None, check_bounds: bool = False,
-               schedule_meta=None, stream=None):
+               schedule_meta=None, out_dtype=None, stream=None):
     """Dense MQA logits (C ABI ``mqa_logits``, or ``mqa_logits_scheduled`` when
     ``schedule_meta`` from ``mqa_logits_metadata`` is given).
 
     q [S_q, H, D] and kv [S_kv, D] are E4M3 (float8_e4m3fn or raw uint8 bytes),
     kv_scale [S_kv] and weights [S_q, H] float32, k_start / k_end [S_q] int32.
-    Returns ``logits`` [S_q, ldo] float32 (allocated when not given; ``ldo``
-    defaults to S_kv and must be given for compressed output).
+    Returns ``logits`` [S_q, ldo] float32, or bfloat16 with ``out_dtype``
+    (allocated when not given; ``ldo`` defaults to S_kv and must be given for
+    compressed output).
     """
     import torch
     f8 = _fp8_types()
@@ -148,20 +173,9 @@ def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: 
         raise ValueError("shape mismatch between q, kv and weights")
     if kv_scale.shape != (S_kv,) or k_start.shape != (S_q,) or k_end.shape != (S_q,):
         raise ValueError("shape mismatch in kv_scale / k_start / k_end")
-    if logits is None:
-        if ldo is None:
-            if compressed:
-                raise ValueError("compressed output needs ldo (the longest range) or a logits buffer")
-            ldo = S_kv
-        logits = torch.empty((S_q, ldo), dtype=torch.float32, device=q.device)
-    else:
-        _dev_out = logits
-        if not (_dev_out.is_cuda and _dev_out.dtype == torch.float32 and _dev_out.dim() == 2
-                and _dev_out.stride(1) == 1 and _dev_out.shape[0] == S_q):
-            raise ValueError("logits must be a CUDA float32 [S_q, ldo] matrix with unit column stride")
-        ldo = _dev_out.stride(0) if ldo is None else ldo
+    logits, ldo, fo = _dense_out(logits, S_q, ldo, compressed, S_kv, out_dtype, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_COMPRESSED if compressed else 0) | \
-            (MQA_CHECK_BOUNDS if check_bounds else 0)
+            (MQA_CHECK_BOUNDS if check_bounds else 0) | fo
     with torch.cuda.device(q.device):
         if schedule_meta is None:
             _check(load_library().mqa_logits(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights),
@@ -180,7 +194,7 @@ def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: 
 
 def mqa_logits_mx(q, q_sf, kv, kv_sf, weights, k_start, k_end, logits=None, *, clean: bool = True,
                   compressed: bool = False, ldo: Optional[int] = None, check_bounds: bool = False,
-                  stream=None):
+                  out_dtype=None, stream=None):
     """Dense MQA logits with MXFP8 inputs (C ABI ``mqa_logits_mx``).
 
     q [S_q, H, 128] and kv [S_kv, 128] E4M3 (float8_e4m3fn or uint8 bytes);
@@ -205,19 +219,9 @@ def mqa_logits_mx(q, q_sf, kv, kv_sf, weights, k_start, k_end, logits=None, *, c
         raise ValueError("shape mismatch between q, q_sf, kv and weights")
     if kv_sf.shape != (S_kv,) or k_start.shape != (S_q,) or k_end.shape != (S_q,):
         raise ValueError("shape mismatch in kv_sf / k_start / k_end")
-    if logits is None:
-        if ldo is None:
-            if compressed:
-                raise ValueError("compressed output needs ldo (the longest range) or a logits buffer")
-            ldo = S_kv
-        logits = torch.empty((S_q, ldo), dtype=torch.float32, device=q.device)
-    else:
-        if not (logits.is_cuda and logits.dtype == torch.float32 and logits.dim() == 2
-                and logits.stride(1) == 1 and logits.shape[0] == S_q):
-            raise ValueError("logits must be a CUDA float32 [S_q, ldo] matrix with unit column stride")
-        ldo = logits.stride(0) if ldo is None else ldo
+    logits, ldo, fo = _dense_out(logits, S_q, ldo, compressed, S_kv, out_dtype, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_COMPRESSED if compressed else 0) | \
-            (MQA_CHECK_BOUNDS if check_bounds else 0)
+            (MQA_CHECK_BOUNDS if check_bounds else 0) | fo
     with torch.cuda.device(q.device):
         _check(load_library().mqa_logits_mx(_ptr(q), _ptr(q_sf), _ptr(kv), _ptr(kv_sf), _ptr(weights),
                                             _ptr(k_start), _ptr(k_end), _ptr(logits), S_q, S_kv, H,
@@ -318,21 +322,27 @@ def paged_shapes(q, kv_cache, kv_scales, weights, context_lens, block_table, nex
     return R, H, D, B, next_n, num_blocks, block_kv, block_table[1]
 
 
-def _paged_logits_out(logits, R, width, device):
+def _paged_logits_out(logits, R, width, device, out_dtype=None):
     import torch
     if logits is None:
-        return torch.empty((R, width), dtype=torch.float32, device=device)
-    if not (isinstance(logits, torch.Tensor) and logits.is_cuda and logits.dtype == torch.float32
+        dt = torch.float32 if out_dtype is None else out_dtype
+        if dt not in (torch.float32, torch.bfloat16):
+            raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+        return torch.empty((R, width), dtype=dt, device=device)
+    if not (isinstance(logits, torch.Tensor) and logits.is_cuda
+            and logits.dtype in (torch.float32, torch.bfloat16)
             and logits.dim() == 2 and logits.stride(1) == 1 and logits.shape[0] == R
             and logits.shape[1] >= width):
-        raise ValueError("logits must be a CUDA float32 [B*next_n, >= max_blocks_per_seq*block_kv] "
-                         "matrix with unit column stride")
+        raise ValueError("logits must be a CUDA float32 or bfloat16 [B*next_n, >= max_blocks_per_seq"
+                         "*block_kv] matrix with unit column stride")
+    if out_dtype is not None and out_dtype != logits.dtype:
+        raise ValueError("out_dtype differs from the logits buffer's dtype")
     return logits
 
 
 def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table, schedule_meta,
                      logits=None, *, next_n: Optional[int] = None, clean: bool = True,
-                     check_bounds: bool = False, stream=None):
+                     check_bounds: bool = False, out_dtype=None, stream=None):
     """Paged decode MQA logits (C ABI ``paged_mqa_logits``).
 
     q [B*next_n, H, D] E4M3, kv_cache [num_blocks, block_kv, D] E4M3, kv_scales
@@ -348,8 +358,9 @@ def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
     if schedule_meta.dim() != 2 or schedule_meta.shape[1] != 2:
         raise ValueError("schedule_meta must be an int32 [num_sms + 1, 2] tensor")
     num_sms = schedule_meta.shape[0] - 1
-    logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device)
-    flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0)
+    logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device, out_dtype)
+    flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0) | \
+        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0)
     with torch.cuda.device(q.device):
         _check(load_library().paged_mqa_logits(_ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights),
                                                _ptr(context_lens), _ptr(block_table), max_blocks,
@@ -372,7 +383,8 @@ def paged_mqa_logits_noalloc(q, kv_cache, kv_scales, weights, context_lens, bloc
     if logits is None:
         raise ValueError("paged_mqa_logits_noalloc needs a caller-provided logits buffer")
     logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device)
-    flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0)
+    flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0) | \
+        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0)
     with torch.cuda.device(q.device):
         _check(load_library().paged_mqa_logits_noalloc(
             _ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights), _ptr(context_lens),

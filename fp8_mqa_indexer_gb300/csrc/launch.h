@@ -21,14 +21,17 @@ struct LaunchArgs {
 };
 
 // Both return cudaErrorNotSupported for an (H, D) pair without an instance.
-cudaError_t launch_dense(int H, int D, const LaunchArgs& a);
-cudaError_t launch_paged(int H, int D, const LaunchArgs& a);
-cudaError_t launch_dense_mx(int H, const LaunchArgs& a);
+// bf16: __nv_bfloat16 logits instead of float.
+cudaError_t launch_dense(int H, int D, bool bf16, const LaunchArgs& a);
+cudaError_t launch_paged(int H, int D, bool bf16, const LaunchArgs& a);
+cudaError_t launch_dense_mx(int H, bool bf16, const LaunchArgs& a);
+cudaError_t launch_dense_bf16(int H, int D, const LaunchArgs& a);
+cudaError_t launch_paged_bf16(int H, int D, const LaunchArgs& a);
 
-template <int H, int D, bool PAGED, bool MX = false>
+template <int H, int D, bool PAGED, bool MX = false, typename OutT = float>
 cudaError_t launch_instance(const LaunchArgs& a)
 {
-    auto kern = mqa_logits_kernel<H, D, PAGED, MX>;
+    auto kern = mqa_logits_kernel<H, D, PAGED, MX, OutT>;
     const size_t smem = sizeof(Smem<D, MX>) + 1024;
     // The shared-memory limit is a per-device attribute of the function: set it
     // once on each device (one bit per device; setting it twice is harmless).

@@ -267,11 +267,12 @@ __global__ void check_paged_kernel(const int* __restrict__ ctx, const int* __res
     }
 }
 
-__global__ void fill_rows_kernel(float* out, int rows, long long ldo, long long c0, long long c1)
+template <typename OutT>
+__global__ void fill_rows_kernel(OutT* out, int rows, long long ldo, long long c0, long long c1)
 {
     for (int r = blockIdx.x; r < rows; r += gridDim.x)
         for (long long c = c0 + threadIdx.x; c < c1; c += blockDim.x)
-            out[r * ldo + c] = __int_as_float(0xff800000u);
+            out[r * ldo + c] = neg_inf<OutT>();
 }
 
 __global__ void selftest_wait_kernel(long long limit, unsigned* status)
@@ -427,14 +428,15 @@ namespace {
 // MX calls pass q_sf and kv_sf (UE8M0 block scales) and no kv_scale.
 mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, const float* weights,
                       const int32_t* k_start, const int32_t* k_end, const int32_t* schedule_meta,
-                      int sched_sms, float* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
+                      int sched_sms, void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                       unsigned flags, cudaStream_t stream, const uint32_t* q_sf = nullptr,
                       const uint32_t* kv_sf = nullptr)
 {
     const bool mx = q_sf != nullptr || kv_sf != nullptr;
     const bool compressed = (flags & MQA_COMPRESSED) != 0;
     const bool clean = (flags & MQA_CLEAN) != 0;
-    if (flags & ~(unsigned)(MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS))
+    const bool bf16 = (flags & MQA_OUT_BF16) != 0;
+    if (flags & ~(unsigned)(MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16))
         return fail(MQA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
     if (S_q < 0 || S_kv < 0)
         return fail(MQA_ERR_INVALID_ARG, "S_q and S_kv must be >= 0");
@@ -466,8 +468,9 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     if (!aligned(q, 16) || !aligned(weights, 16) ||
         (S_kv > 0 && (!aligned(kv, 16) || (!mx && !aligned(kv_scale, 16)))))
         return fail(MQA_ERR_INVALID_ARG, "q, kv, kv_scale and weights must be 16-byte aligned");
-    if (!aligned(logits, 4) || !aligned(k_start, 4) || !aligned(k_end, 4))
-        return fail(MQA_ERR_INVALID_ARG, "logits, k_start, k_end must be 4-byte aligned");
+    if (!aligned(logits, bf16 ? 2 : 4) || !aligned(k_start, 4) || !aligned(k_end, 4))
+        return fail(MQA_ERR_INVALID_ARG,
+                    "logits must be aligned to its element, k_start and k_end to 4 bytes");
 
     if (schedule_meta && (sched_sms < 1 || !aligned(schedule_meta, 4)))
         return fail(MQA_ERR_INVALID_ARG, "schedule_meta must be 4-byte aligned and num_sms >= 1");
@@ -511,8 +514,12 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     if (S_kv == 0) {
         // no keys: every row is empty; only compressed clean rows have padding
         if (compressed && clean) {
-            fill_rows_kernel<<<grid_for(S_q), 256, 0, stream>>>(logits, S_q, (long long)ldo, 0,
-                                                                (long long)ldo);
+            if (bf16)
+                fill_rows_kernel<<<grid_for(S_q), 256, 0, stream>>>(
+                    static_cast<__nv_bfloat16*>(logits), S_q, (long long)ldo, 0, (long long)ldo);
+            else
+                fill_rows_kernel<<<grid_for(S_q), 256, 0, stream>>>(
+                    static_cast<float*>(logits), S_q, (long long)ldo, 0, (long long)ldo);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess)
                 return cuda_fail(e, "fill launch");
@@ -559,7 +566,7 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     p.status = st;
     a.grid = num_sms;
     a.stream = stream;
-    cudaError_t e = mx ? launch_dense_mx(H, a) : launch_dense(H, D, a);
+    cudaError_t e = mx ? launch_dense_mx(H, bf16, a) : launch_dense(H, D, bf16, a);
     if (e == cudaErrorNotSupported)
         return fail(MQA_ERR_UNSUPPORTED, "no dense kernel for H=%d D=%d", H, D);
     if (e != cudaSuccess)
@@ -569,7 +576,7 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
 }  // namespace
 
 mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, const float* weights,
-                      const int32_t* k_start, const int32_t* k_end, float* logits, int S_q,
+                      const int32_t* k_start, const int32_t* k_end, void* logits, int S_q,
                       int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream)
 {
     return dense_call(q, kv, kv_scale, weights, k_start, k_end, nullptr, 0, logits, S_q, S_kv, H,
@@ -579,7 +586,7 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
 mqa_status mqa_logits_scheduled(const void* q, const void* kv, const float* kv_scale,
                                 const float* weights, const int32_t* k_start,
                                 const int32_t* k_end, const int32_t* schedule_meta, int num_sms,
-                                float* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
+                                void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                                 unsigned flags, mqa_stream_t stream)
 {
     if (!schedule_meta)
@@ -590,7 +597,7 @@ mqa_status mqa_logits_scheduled(const void* q, const void* kv, const float* kv_s
 
 mqa_status mqa_logits_mx(const void* q, const uint32_t* q_sf, const void* kv, const uint32_t* kv_sf,
                          const float* weights, const int32_t* k_start, const int32_t* k_end,
-                         float* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
+                         void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                          unsigned flags, mqa_stream_t stream)
 {
     if (flags & MQA_MXFP4)
@@ -639,7 +646,7 @@ namespace {
 mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_scales,
                           const float* weights, const int32_t* context_lens,
                           const int32_t* block_table, int max_blocks_per_seq,
-                          const int32_t* schedule_meta, const float* logits, int B, int next_n,
+                          const int32_t* schedule_meta, const void* logits, int B, int next_n,
                           int H, int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
                           unsigned flags, bool own_schedule, bool* nothing_to_do)
 {
@@ -650,9 +657,10 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_s
         num_sms = 1;
     }
     *nothing_to_do = false;
-    if (flags & ~(unsigned)(MQA_CLEAN | MQA_CHECK_BOUNDS))
+    if (flags & ~(unsigned)(MQA_CLEAN | MQA_CHECK_BOUNDS | MQA_OUT_BF16))
         return fail((flags & MQA_COMPRESSED) ? MQA_ERR_UNSUPPORTED : MQA_ERR_INVALID_ARG,
-                    "paged logits take only MQA_CLEAN and MQA_CHECK_BOUNDS (flags 0x%x)", flags);
+                    "paged logits take only MQA_CLEAN, MQA_CHECK_BOUNDS and MQA_OUT_BF16 "
+                    "(flags 0x%x)", flags);
     if (B < 0 || next_n < 1 || num_blocks < 1 || max_blocks_per_seq < 1 || num_sms < 1)
         return fail(MQA_ERR_INVALID_ARG,
                     "need B >= 0, next_n >= 1, num_blocks >= 1, max_blocks_per_seq >= 1, num_sms >= 1");
@@ -681,9 +689,10 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_s
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(kv_scales, 16) || !aligned(weights, 16))
         return fail(MQA_ERR_INVALID_ARG,
                     "q, kv_cache, kv_scales and weights must be 16-byte aligned");
-    if (!aligned(logits, 4) || !aligned(context_lens, 4) || !aligned(block_table, 4) ||
-        !aligned(schedule_meta, 4))
-        return fail(MQA_ERR_INVALID_ARG, "int and float arrays must be 4-byte aligned");
+    if (!aligned(logits, (flags & MQA_OUT_BF16) ? 2 : 4) || !aligned(context_lens, 4) ||
+        !aligned(block_table, 4) || !aligned(schedule_meta, 4))
+        return fail(MQA_ERR_INVALID_ARG,
+                    "logits must be aligned to its element, the int arrays to 4 bytes");
     return MQA_OK;
 }
 }  // namespace
@@ -691,7 +700,7 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_s
 mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv_scales,
                             const float* weights, const int32_t* context_lens,
                             const int32_t* block_table, int max_blocks_per_seq,
-                            const int32_t* schedule_meta, float* logits, int B, int next_n, int H,
+                            const int32_t* schedule_meta, void* logits, int B, int next_n, int H,
                             int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
                             unsigned flags, mqa_stream_t stream_)
 {
@@ -775,7 +784,7 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
             return s;
         p.tok = tok;
         p.tok0 = t0;
-        cudaError_t e = launch_paged(H, D, a);
+        cudaError_t e = launch_paged(H, D, (flags & MQA_OUT_BF16) != 0, a);
         if (e == cudaErrorNotSupported)
             return fail(MQA_ERR_UNSUPPORTED, "no paged kernel for H=%d D=%d", H, D);
         if (e != cudaSuccess)
@@ -798,7 +807,7 @@ int32_t* g_noalloc_ptr[kMaxDevices];
 mqa_status paged_mqa_logits_noalloc(const void* q, const void* kv_cache, const float* kv_scales,
                                     const float* weights, const int32_t* context_lens,
                                     const int32_t* block_table, int max_blocks_per_seq,
-                                    float* logits, int B, int next_n, int H, int D, int block_kv,
+                                    void* logits, int B, int next_n, int H, int D, int block_kv,
                                     int num_blocks, int64_t ldo, unsigned flags,
                                     mqa_stream_t stream)
 {

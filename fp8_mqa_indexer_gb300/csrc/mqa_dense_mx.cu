@@ -4,8 +4,16 @@
 
 namespace mqa {
 
-cudaError_t launch_dense_mx(int H, const LaunchArgs& a)
+cudaError_t launch_dense_mx(int H, bool bf16, const LaunchArgs& a)
 {
+    if (bf16) {
+        switch (H) {
+        case 8: return launch_instance<8, 128, false, true, __nv_bfloat16>(a);
+        case 32: return launch_instance<32, 128, false, true, __nv_bfloat16>(a);
+        case 64: return launch_instance<64, 128, false, true, __nv_bfloat16>(a);
+        }
+        return cudaErrorNotSupported;
+    }
     switch (H) {
     case 8: return launch_instance<8, 128, false, true>(a);
     case 32: return launch_instance<32, 128, false, true>(a);

@@ -33,6 +33,8 @@
 //    accumulators of 256 columns; every hand-off is an mbarrier, every wait is
 //    bounded (ptx.cuh, wait_bounded).
 #pragma once
+#include <cuda_bf16.h>
+
 #include <climits>
 #include <cstdint>
 
@@ -81,7 +83,7 @@ struct __align__(16) TokRow {
 };
 
 struct Params {
-    float* logits;
+    void* logits;            // float, or __nv_bfloat16 (bf16 instances)
     long long ldo;
     unsigned flags;
     // dense
@@ -233,26 +235,45 @@ __device__ __forceinline__ long long block_units(const Params& p, bool paged, in
 }
 
 // -------------------------------------------------------- -inf fill of rows
+// -inf of the output element type (fp32 0xff800000, bf16 0xff80).
+template <typename OutT> __device__ __forceinline__ OutT neg_inf();
+template <> __device__ __forceinline__ float neg_inf<float>() { return __int_as_float(0xff800000u); }
+template <> __device__ __forceinline__ __nv_bfloat16 neg_inf<__nv_bfloat16>()
+{
+    return __ushort_as_bfloat16((unsigned short)0xff80u);
+}
+
+template <typename OutT> __device__ __forceinline__ OutT to_out(float v);
+template <> __device__ __forceinline__ float to_out<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float v)
+{
+    return __float2bfloat16_rn(v);
+}
+
 // Writes -inf to row[c0, c1) with one warp: scalar head to a 16-byte boundary,
-// float4 body, scalar tail.
-__device__ __forceinline__ void warp_fill_neg_inf(float* row, long long c0, long long c1, int lane)
+// 16-byte body, scalar tail.
+template <typename OutT>
+__device__ __forceinline__ void warp_fill_neg_inf(OutT* row, long long c0, long long c1, int lane)
 {
     if (c0 >= c1)
         return;
-    const float ninf = __int_as_float(0xff800000u);
-    const long long mis = (long long)((reinterpret_cast<uintptr_t>(row + c0) >> 2) & 3u);
-    const long long head = min((4 - mis) & 3, c1 - c0);
+    constexpr int kVec = 16 / sizeof(OutT);   // elements per 16-byte store
+    const OutT ninf = neg_inf<OutT>();
+    const long long mis =
+        (long long)((reinterpret_cast<uintptr_t>(row + c0) / sizeof(OutT)) & (kVec - 1));
+    const long long head = min((kVec - mis) & (kVec - 1), c1 - c0);
     if (lane < head)
         row[c0 + lane] = ninf;
     long long a = c0 + head;
-    const long long nvec = (c1 - a) >> 2;
-    float4* v = reinterpret_cast<float4*>(row + a);
-    const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
+    const long long nvec = (c1 - a) / kVec;
+    uint4* v = reinterpret_cast<uint4*>(row + a);
+    const uint32_t w = sizeof(OutT) == 4 ? 0xff800000u : 0xff80ff80u;   // -inf, packed
+    const uint4 f4 = make_uint4(w, w, w, w);
     for (long long k = lane; k < nvec; k += 32)
         v[k] = f4;
-    a += nvec << 2;
-    if (lane < c1 - a)
-        row[a + lane] = ninf;
+    a += nvec * kVec;
+    for (long long c = a + lane; c < c1; c += 32)
+        row[c] = ninf;
 }
 
 // A bounded wait taken by a whole warp: every lane gets the same answer, so a
@@ -282,7 +303,7 @@ constexpr unsigned kMmaSleepNs = 0;
 // ReLU(y) = (y + |y|) / 2 instead: it accumulates A = sum w x and
 // B = sum w |x| and forms (s A + |s| B) / 2, which equals sum w ReLU(s x) for
 // either sign of s.
-template <int H, int D, bool MX = false>
+template <int H, int D, bool MX = false, typename OutT = float>
 struct Epilogue {
     static_assert(H >= 8 && H <= kEpiCols, "a warp's columns must hold whole tokens");
     using C = Cfg<D>;
@@ -390,7 +411,8 @@ struct Epilogue {
         const int j = st.info.t * kBlockKV + row;
         // one predicated store: the logit, -inf (clean) or nothing
         if (j >= t.slo && j < t.shi)
-            p.logits[t.off + j] = (j >= t.vlo && j < t.vhi) ? v : __int_as_float(0xff800000u);
+            static_cast<OutT*>(p.logits)[t.off + j] =
+                (j >= t.vlo && j < t.vhi) ? to_out<OutT>(v) : neg_inf<OutT>();
     }
 
     // Columns [c0, c0 + P) of the warp's slice, already in x.
@@ -503,7 +525,8 @@ struct Epilogue {
 
 // ------------------------------------------------------------------ kernel
 // MX = true: MXFP8 dense call (block-scaled E4M3 MMA, no per-key fp32 scale).
-template <int H, int D, bool PAGED, bool MX = false>
+// OutT: float or __nv_bfloat16 logits (each fp32 logit rounded to nearest even).
+template <int H, int D, bool PAGED, bool MX = false, typename OutT = float>
 __global__ void __launch_bounds__(kThreads, 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_kv,
@@ -983,7 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nrows = PAGED ? p.B * p.tok : p.rows;
             for (int rr = cta + fw * G; rr < nrows; rr += nfw * G) {
                 const int r = PAGED ? (rr / p.tok) * p.next_n + p.tok0 + rr % p.tok : rr;
-                float* row = p.logits + (long long)r * p.ldo;
+                OutT* row = static_cast<OutT*>(p.logits) + (long long)r * p.ldo;
                 if (PAGED) {
                     const int c = max(__ldg(p.context_lens + r / p.next_n), 0);
                     const long long covered = min((long long)paged_tiles(c) * kBlockKV, p.width);
@@ -1015,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tpg = kEpiCols / H;                   // tokens per group
         const int tok0 = g * tpg;
         const int ntok = max(0, min(tpg, p.tok - tok0));
-        Epilogue<H, D, MX> epi{sm, p, wctx,
+        Epilogue<H, D, MX, OutT> epi{sm, p, wctx,
                            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * kEpiCols),
                            n_units, quad * 32 + lane, g * kEpiCols, tok0, ntok, warp - kEpiWarp0};
         const int nc = ntok * H;   // columns holding tokens, rounded up below

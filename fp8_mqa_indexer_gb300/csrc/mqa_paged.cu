@@ -3,8 +3,10 @@
 
 namespace mqa {
 
-cudaError_t launch_paged(int H, int D, const LaunchArgs& a)
+cudaError_t launch_paged(int H, int D, bool bf16, const LaunchArgs& a)
 {
+    if (bf16)
+        return launch_paged_bf16(H, D, a);
     if (D == 128) {
         switch (H) {
         case 16: return launch_instance<16, 128, true>(a);

@@ -72,7 +72,13 @@ enum {
      * lengths, block ids, schedule).  The call then synchronizes `stream` and
      * returns MQA_ERR_BAD_INPUT without computing if any check fails.  Not for
      * use inside CUDA graph capture. */
-    MQA_CHECK_BOUNDS = 4u
+    MQA_CHECK_BOUNDS = 4u,
+    /* Logits as bf16 (each fp32 logit rounded to the nearest even bf16; -inf
+     * stays -inf): the `logits` buffer holds 2-byte elements, ldo counts
+     * elements.  For mqa_logits, mqa_logits_scheduled, mqa_logits_mx and the
+     * paged calls ("[PR #435] ...", section "Validation": FP32/BF16 output).
+     * The top-k calls read fp32 logits only. */
+    MQA_OUT_BF16 = 16u
 };
 
 /*
@@ -85,14 +91,15 @@ enum {
  *   kv_scale  [S_kv]       fp32 per-key scale, 16-byte aligned
  *   weights   [S_q, H]     fp32 per-(token, head) weight, 16-byte aligned
  *   k_start, k_end [S_q]   int32 half-open key range of each query row
- *   logits    [S_q, ldo]   fp32 output, 4-byte aligned.  Uncompressed: row i
+ *   logits    [S_q, ldo]   fp32 output, 4-byte aligned (bf16, 2-byte aligned,
+ *             with MQA_OUT_BF16).  Uncompressed: row i
  *             has S_kv columns and ldo >= S_kv (columns [S_kv, ldo) are never
  *             written).  Compressed: ldo >= every row's range length.
  *   H in {8, 32, 64}, D in {64, 128}; S_q, S_kv >= 0; S_q * H < 2^31.
- *   flags     MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS
+ *   flags     MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16
  */
 MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_scale, const float *weights,
-                      const int32_t *k_start, const int32_t *k_end, float *logits, int S_q,
+                      const int32_t *k_start, const int32_t *k_end, void *logits, int S_q,
                       int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
 
 /*
@@ -114,10 +121,10 @@ MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_sca
  *   UE8M0) is not allowed.  flags may not hold MQA_MXFP4 (MXFP4 elements: not
  *   supported yet, MQA_ERR_UNSUPPORTED).
  */
-enum { MQA_MXFP4 = 8u };
+enum { MQA_MXFP4 = 8u };   /* flag of mqa_logits_mx */
 MQA_API mqa_status mqa_logits_mx(const void *q, const uint32_t *q_sf, const void *kv,
                                  const uint32_t *kv_sf, const float *weights,
-                                 const int32_t *k_start, const int32_t *k_end, float *logits,
+                                 const int32_t *k_start, const int32_t *k_end, void *logits,
                                  int S_q, int S_kv, int H, int D, int64_t ldo, unsigned flags,
                                  mqa_stream_t stream);
 
@@ -160,7 +167,7 @@ MQA_API mqa_status mqa_logits_metadata(const int32_t *k_start, const int32_t *k_
 MQA_API mqa_status mqa_logits_scheduled(const void *q, const void *kv, const float *kv_scale,
                                         const float *weights, const int32_t *k_start,
                                         const int32_t *k_end, const int32_t *schedule_meta,
-                                        int num_sms, float *logits, int S_q, int S_kv, int H,
+                                        int num_sms, void *logits, int S_q, int S_kv, int H,
                                         int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
 
 /*
@@ -213,7 +220,7 @@ MQA_API mqa_status paged_mqa_logits_metadata(const int32_t *context_lens, int B,
 MQA_API mqa_status paged_mqa_logits(const void *q, const void *kv_cache, const float *kv_scales,
                             const float *weights, const int32_t *context_lens,
                             const int32_t *block_table, int max_blocks_per_seq,
-                            const int32_t *schedule_meta, float *logits, int B, int next_n, int H,
+                            const int32_t *schedule_meta, void *logits, int B, int next_n, int H,
                             int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
                             unsigned flags, mqa_stream_t stream);
 
@@ -246,7 +253,7 @@ MQA_API mqa_status paged_mqa_logits_noalloc(const void *q, const void *kv_cache,
                                             const float *kv_scales, const float *weights,
                                             const int32_t *context_lens,
                                             const int32_t *block_table, int max_blocks_per_seq,
-                                            float *logits, int B, int next_n, int H, int D,
+                                            void *logits, int B, int next_n, int H, int D,
                                             int block_kv, int num_blocks, int64_t ldo,
                                             unsigned flags, mqa_stream_t stream);
 
