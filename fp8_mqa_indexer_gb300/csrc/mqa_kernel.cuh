@@ -492,10 +492,12 @@ struct Epilogue {
         int stage = 0;
         uint32_t phase = 0;
         int k_block = -1;
-        // Eight units per trip: the accumulator buffer of each (and, with eight
-        // key-tile stages, the stage too) is then known at compile time, the
-        // loop's bookkeeping is shared, and the compiler can schedule one
-        // unit's tail against the next unit's hand-offs.
+        // Eight units per trip (four below 64 heads, where a warp's columns
+        // hold several tokens and the longer body runs out of instruction
+        // cache): the accumulator buffer of each (and, with eight key-tile
+        // stages, the stage too) is then known at compile time, the loop's
+        // bookkeeping is shared, and the compiler can schedule one unit's tail
+        // against the next unit's hand-offs.
         auto one = [&](int u) -> bool {
             Unit st;
             if (!begin(stage, phase, u, k_block, st))
@@ -512,10 +514,17 @@ struct Epilogue {
             return true;
         };
         int u = 0;
-        for (; u + 7 < n_units; u += 8) {
-            if (!one(u) || !one(u + 1) || !one(u + 2) || !one(u + 3) || !one(u + 4) ||
-                !one(u + 5) || !one(u + 6) || !one(u + 7))
-                return;
+        if constexpr (H >= 64) {
+            for (; u + 7 < n_units; u += 8) {
+                if (!one(u) || !one(u + 1) || !one(u + 2) || !one(u + 3) || !one(u + 4) ||
+                    !one(u + 5) || !one(u + 6) || !one(u + 7))
+                    return;
+            }
+        } else {
+            for (; u + 3 < n_units; u += 4) {
+                if (!one(u) || !one(u + 1) || !one(u + 2) || !one(u + 3))
+                    return;
+            }
         }
         for (; u < n_units; ++u)
             if (!one(u))
