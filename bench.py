@@ -346,7 +346,7 @@ def bench_mx(args, mqa, torch, dev, stream):
         **percentiles(times_ms),
         "graph_timing": graph,
         "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
-                     "frac": value / peak, "traffic": None,
+                     "frac": value / peak, "traffic": recorded_traffic(args.workload),
                      "peak_source": ("measured fp8 (cuBLAS e4m3 GEMM burst on this GPU)" if fp8 else
                                      f"{peaks_src} bf16 burst x {FP8_PER_BF16} (nominal fp8:bf16)"),
                      "peak_bf16x2": nominal_peak, "frac_bf16x2": value / nominal_peak},
@@ -653,6 +653,10 @@ def oracle_sample(case, budget_s: float, max_rows: int = 4096):
         k += len(batch)
 
         def one(r):
+            if hasattr(case, "q_sf"):   # MXFP8 input
+                return oracle.mx_mqa_logits(case.q, case.q_sf, case.kv, case.kv_sf, case.weights,
+                                            case.k_start, case.k_end, fp4=case.fp4, ldo=case.ldo,
+                                            rows=(r, r + 1))
             return oracle.mqa_logits(case.q, case.kv, case.kv_scale, case.weights, case.k_start,
                                      case.k_end, ldo=case.ldo, clean=case.clean,
                                      compressed=case.compressed, rows=(r, r + 1))

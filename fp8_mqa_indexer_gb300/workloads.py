@@ -332,6 +332,16 @@ class MxDenseCase:
     def S_kv(self):
         return self.kv.shape[0]
 
+    D = 128
+    clean = True
+    compressed = False
+
+    def valid_counts(self) -> torch.Tensor:
+        """Number of scored keys per row (range clipped to [0, S_kv))."""
+        lo = self.k_start.clamp(min=0).to(torch.int64)
+        hi = self.k_end.clamp(max=self.S_kv).to(torch.int64)
+        return (hi - lo).clamp(min=0)
+
 
 def packed_scales(shape, lo: int, hi: int, g: torch.Generator) -> torch.Tensor:
     """int32 tensor whose four bytes are independent UE8M0 codes in [lo, hi]."""
