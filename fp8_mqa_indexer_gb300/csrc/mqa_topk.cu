@@ -14,11 +14,14 @@
 // order is totalOrder, and a radix select over three digits (bits 31..20,
 // 19..8, 7..0) finds the k-th largest key T:
 //   0. (rows with k <= 2048 and at least max(8192, 4 k) keys) a sample of
-//      1/16 of the row sets a threshold t0 that about 1.4 k keys clear; one
-//      ordered pass compacts every key >= t0 into shared memory and, when
-//      that list holds between k and its capacity of keys, steps 3 and 4 (and
-//      the digit-1 histogram) run on the list alone: the row is read from HBM
-//      once.  Otherwise:
+//      1/16 of the row (whole 128-byte lines, one in every 16) sets a
+//      threshold t0 that about 1.4 k keys clear; one ordered pass compacts
+//      every key >= t0 into shared memory and, when that list holds between k
+//      and its capacity of keys, the selection runs on the list alone, with
+//      two 12-bit digits of key - t0 in place of steps 1 to 3 (the list's keys
+//      spread over those digits, so their histogram atomics rarely collide,
+//      where the absolute digit 1 of keys near t0 falls in a few bins): the
+//      row is read from HBM once.  Otherwise:
 //   1. histogram of digit 1 over the row (the row's read from HBM) gives the
 //      bin holding the k-th largest key;
 //   2. every element in or above that bin is compacted, in key order, into
@@ -316,6 +319,10 @@ __device__ __forceinline__ void clear_hist(TopkSmem& sm)
     __syncthreads();
 }
 
+template <class Walk>
+__device__ __forceinline__ void write_selected(TopkSmem& sm, Walk&& each, unsigned T, unsigned r,
+                                               unsigned k, int* out, int& buf);
+
 // Digits 2 and 3 over `each` (a row or list walk), then the ordered write of
 // the selection.  b1 / above1 come from digit 1.
 template <class Walk>
@@ -344,7 +351,16 @@ __device__ __forceinline__ void finish_row(TopkSmem& sm, Walk&& each, unsigned b
     unsigned b3, above3;
     select_bin<kBins8>(sm, k - above1 - above2, buf, b3, above3, cnt);
     const unsigned T = (prefix << 8) | b3;
-    const unsigned r = k - above1 - above2 - above3;   // keys equal to T that are taken
+    write_selected(sm, each, T, k - above1 - above2 - above3, k, out, buf);
+}
+
+// The ordered write of a selection: every key above T, and the first r keys
+// equal to T, each at its rank in key order: (keys above T before it) +
+// min(keys equal to T before it, r).
+template <class Walk>
+__device__ __forceinline__ void write_selected(TopkSmem& sm, Walk&& each, unsigned T, unsigned r,
+                                               unsigned k, int* out, int& buf)
+{
     unsigned gt_run = 0, eq_run = 0;
     each([&](const unsigned(&key)[kPer], unsigned okm, auto idx) {
         unsigned gm = 0, qm = 0;
@@ -453,15 +469,18 @@ __device__ __forceinline__ unsigned compact_row(TopkSmem& sm, const RowView& r,
 __device__ __forceinline__ bool sample_threshold(TopkSmem& sm, const RowView& r, unsigned n,
                                                  unsigned k, int& buf, unsigned& t0)
 {
-    const long long span = r.c_hi - r.c_start;
+    // whole 128-byte lines (8 float4), one line in every 8 * stride elements
+    const long long c128 =
+        r.c_lo - (long long)((reinterpret_cast<unsigned long long>(r.ptr + r.c_lo) >> 2) & 31);
+    const long long span = r.c_hi - c128;
     long long stride = 64;
-    while ((span + stride - 1) / stride > kCap / 4)
+    while (((span + 8 * stride - 1) / (8 * stride)) * 8 > kCap / 4)
         stride *= 2;
-    const int nf4 = (int)((span + stride - 1) / stride);
+    const int nf4 = (int)(((span + 8 * stride - 1) / (8 * stride)) * 8);
     clear_hist<kBins12>(sm);
     unsigned valid = 0;
     for (int f = threadIdx.x; f < nf4; f += kNT) {
-        const long long c = r.c_start + f * stride;
+        const long long c = c128 + (long long)(f >> 3) * (8 * stride) + 4 * (f & 7);
         uint4 kk = make_uint4(0u, 0u, 0u, 0u);   // key 0: not a sample
         if (c >= r.c_lo && c + 4 <= r.c_hi) {
             const float4 x = load4(r.ptr + c);
@@ -496,6 +515,44 @@ __device__ __forceinline__ bool sample_threshold(TopkSmem& sm, const RowView& r,
     unsigned b2, above2, cnt2;
     select_bin<kBins12>(sm, need - above1, buf, b2, above2, cnt2);
     t0 = (b1 << 20) | (b2 << 8);
+    return true;
+}
+
+// Exact selection from the first m list entries (in key order), all of them
+// keys >= t0, when the k-th largest lies below t0 + 2^24 - 4096: two 12-bit
+// digits of key - t0 (the first clamped to 4095) instead of three absolute
+// ones.  The list's keys are spread over the relative digits, so the
+// histogram atomics rarely collide.  Returns false, having written nothing,
+// when the k-th largest falls in the clamped bin.
+__device__ __forceinline__ bool select_from_list_rel(TopkSmem& sm, unsigned m, unsigned k,
+                                                     unsigned t0, int* out, int& buf)
+{
+    auto d1 = [t0](unsigned key) { return min((key - t0) >> 12, (unsigned)(kBins12 - 1)); };
+    clear_hist<kBins12>(sm);
+    for_cand(sm, m, [&](const unsigned(&key)[kPer], unsigned okm, auto) {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            if ((okm >> e) & 1u)
+                atomicAdd(&sm.hist[d1(key[e])], 1u);
+    });
+    __syncthreads();
+    unsigned c1, above1, n1;
+    select_bin<kBins12>(sm, k, buf, c1, above1, n1);
+    if (c1 == kBins12 - 1)
+        return false;
+    clear_hist<kBins12>(sm);
+    for_cand(sm, m, [&](const unsigned(&key)[kPer], unsigned okm, auto) {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            if (((okm >> e) & 1u) && d1(key[e]) == c1)
+                atomicAdd(&sm.hist[(key[e] - t0) & 0xfffu], 1u);
+    });
+    __syncthreads();
+    unsigned c2, above2, n2;
+    select_bin<kBins12>(sm, k - above1, buf, c2, above2, n2);
+    write_selected(
+        sm, [&](auto&& f) { for_cand(sm, m, f); }, t0 + (c1 << 12) + c2, k - above1 - above2, k, out,
+        buf);
     return true;
 }
 
@@ -562,7 +619,8 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
                 sample_threshold(sm, r, n, k, buf, t0)) {
                 const unsigned m = compact_row<false>(sm, r, 0ull, t0, buf);
                 if (m >= k && m <= (unsigned)kCap) {
-                    select_from_list(sm, m, k, out, buf);
+                    if (!select_from_list_rel(sm, m, k, t0, out, buf))
+                        select_from_list(sm, m, k, out, buf);
                     done = true;
                 }
             }

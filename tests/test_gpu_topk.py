@@ -145,6 +145,37 @@ def test_long_rows(dev):
     check(case, dev)
 
 
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
+def test_one_pass_rows_unaligned(dev, offset):
+    """Rows long enough for the sampled one-pass selection, starting and ending
+    at every alignment (row starts shifted off 16 bytes, ldo odd, range ends
+    at arbitrary columns), uncompressed and compressed."""
+    n_cols, rows = 20001, 12
+    g = torch.Generator().manual_seed(770 + offset)
+    ks = torch.randint(0, 40, (rows,), generator=g, dtype=torch.int32)
+    ke = n_cols - torch.randint(0, 40, (rows,), generator=g, dtype=torch.int32)
+    case = wl.topk_case(rows, n_cols, 1000, seed=771 + offset, ranges="custom", k_start=ks,
+                        k_end=ke, ldo=n_cols + 2, name=f"one-pass +{offset}")
+    check(case, dev, offset=offset)
+    case = wl.topk_case(rows, n_cols, 1000, seed=775 + offset, ranges="custom", k_start=ks,
+                        k_end=ke, ldo=n_cols + 2, name=f"one-pass compressed +{offset}")
+    case.compressed = True
+    check(case, dev, offset=offset)
+
+
+def test_rows_around_the_staging_size(dev):
+    """Row lengths on both sides of the longest row the selection copies into
+    shared memory (34808 keys), and far beyond it, in one call."""
+    lens = [34806, 34807, 34808, 34809, 34810, 34812, 40000, 8192]
+    n_cols = max(lens) + 5
+    ks = torch.tensor([1, 2, 3, 0, 4, 1, 0, 7], dtype=torch.int32)
+    ke = ks + torch.tensor(lens, dtype=torch.int32)
+    case = wl.topk_case(len(lens), n_cols, 2048, seed=780, ranges="custom", k_start=ks, k_end=ke,
+                        name="staging boundary")
+    check(case, dev)
+    check(case, dev, offset=1)
+
+
 def test_deterministic(dev):
     case = wl.topk_case(64, 20000, 2048, seed=760, ranges="causal_tail", levels=3)
     Ld = case.logits.to(dev)
