@@ -163,15 +163,16 @@ def test_one_pass_rows_unaligned(dev, offset):
     check(case, dev, offset=offset)
 
 
-def test_rows_around_the_staging_size(dev):
-    """Row lengths on both sides of the longest row the selection copies into
-    shared memory (34808 keys), and far beyond it, in one call."""
-    lens = [34806, 34807, 34808, 34809, 34810, 34812, 40000, 8192]
+def test_rows_around_the_one_pass_limits(dev):
+    """Row lengths on both sides of the shortest row that takes the sampled
+    one-pass selection at k = 2048 (8192 keys), just above k, and long rows,
+    in one call."""
+    lens = [8190, 8191, 8192, 8193, 2049, 34809, 40000, 2048]
     n_cols = max(lens) + 5
     ks = torch.tensor([1, 2, 3, 0, 4, 1, 0, 7], dtype=torch.int32)
     ke = ks + torch.tensor(lens, dtype=torch.int32)
     case = wl.topk_case(len(lens), n_cols, 2048, seed=780, ranges="custom", k_start=ks, k_end=ke,
-                        name="staging boundary")
+                        name="one-pass limits")
     check(case, dev)
     check(case, dev, offset=1)
 
