@@ -266,12 +266,13 @@ def is_mx(workload: str) -> bool:
 # The pages' MXFP8 timings ("[PR #435] ...", section "Performance": GB200, 152
 # SMs, all-zero input, clean fp32 logits, CUDA-graph median per call), as
 # TFLOP/s of this benchmark's metric (valid logits x 2 * H * D).
-MX_PUBLISHED_US = {"mx_2k_32k_h64_d128_zeros": 412.0, "mx_8k_64k_h64_d128_zeros": 3022.2}
+MX_PUBLISHED_US = {"mx_2k_32k_h64_d128_zeros": 412.0, "mx_8k_64k_h64_d128_zeros": 3022.2,
+                   "mx4_2k_32k_h64_d128_zeros": 407.9, "mx4_8k_64k_h64_d128_zeros": 2968.9}
 
 
 def bench_mx(args, mqa, torch, dev, stream):
-    """MXFP8 dense logits (block-scaled tcgen05 MMA); the shapes of the pages'
-    MXFP8 timings."""
+    """MXFP8 or MXFP4 dense logits (block-scaled tcgen05 MMA); the shapes of
+    the pages' MX timings."""
     from fp8_mqa_indexer_gb300 import workloads as wl
     case = wl.mx_config(args.workload)
     i = torch.arange(case.S_q, dtype=torch.int64)
@@ -284,7 +285,7 @@ def bench_mx(args, mqa, torch, dev, stream):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step(o=out):
-        mqa.mqa_logits_mx(*d, o)
+        mqa.mqa_logits_mx(*d, o, fp4=case.fp4)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -321,7 +322,7 @@ def bench_mx(args, mqa, torch, dev, stream):
 
     def e2e_step():
         dd = [h.to(dev, non_blocking=True) for h in host]
-        mqa.mqa_logits_mx(*dd, out)
+        mqa.mqa_logits_mx(*dd, out, fp4=case.fp4)
         host_out.copy_(out, non_blocking=True)
 
     e2e_step()
@@ -347,11 +348,13 @@ def bench_mx(args, mqa, torch, dev, stream):
         "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": value / pub_tflops if pub_tflops else None,
-        "dtype": "mxfp8 (e4m3 x e4m3, ue8m0 block 32) -> f32", "data": "synthetic",
+        "dtype": ("mxfp4 (e2m1 x e2m1" if case.fp4 else "mxfp8 (e4m3 x e4m3") +
+                 ", ue8m0 block 32) -> f32", "data": "synthetic",
         "config": {"workload": args.workload, "S_q": case.S_q, "S_kv": case.S_kv, "H": case.H,
                    "D": 128, "valid_logits": valid, "clean": True,
                    "l2": "flushed (256 MiB write) before every timed step",
-                   "baseline": (f"{published} us on GB200 (the pages' MXFP8 figure, all-zero input, "
+                   "baseline": (f"{published} us on GB200 (the pages' "
+                                f"{'MXFP4' if case.fp4 else 'MXFP8'} figure, all-zero input, "
                                 f"graph median) = {pub_tflops:.0f} TFLOP/s" if published else None)},
         **percentiles(times_ms),
         "graph_timing": graph,

@@ -29,6 +29,7 @@ __all__ = [
 MQA_CLEAN = 1
 MQA_COMPRESSED = 2
 MQA_CHECK_BOUNDS = 4
+MQA_MXFP4 = 8
 MQA_OUT_BF16 = 16
 
 STATUS_NAMES = {0: "MQA_OK", 1: "MQA_ERR_INVALID_ARG", 2: "MQA_ERR_UNSUPPORTED", 3: "MQA_ERR_CUDA",
@@ -194,16 +195,17 @@ def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: 
 
 def mqa_logits_mx(q, q_sf, kv, kv_sf, weights, k_start, k_end, logits=None, *, clean: bool = True,
                   compressed: bool = False, ldo: Optional[int] = None, check_bounds: bool = False,
-                  out_dtype=None, stream=None):
-    """Dense MQA logits with MXFP8 inputs (C ABI ``mqa_logits_mx``).
+                  out_dtype=None, fp4: bool = False, stream=None):
+    """Dense MQA logits with MX inputs (C ABI ``mqa_logits_mx``).
 
-    q [S_q, H, 128] and kv [S_kv, 128] E4M3 (float8_e4m3fn or uint8 bytes);
-    q_sf [S_q, H] and kv_sf [S_kv] int32 (or uint32 bit patterns): four UE8M0
-    block scales each, byte b for elements [32 b, 32 b + 32); weights, ranges
-    and output as ``mqa_logits``.
+    MXFP8: q [S_q, H, 128] and kv [S_kv, 128] E4M3 (float8_e4m3fn or uint8
+    bytes).  ``fp4``: MXFP4, q [S_q, H, 64] and kv [S_kv, 64] bytes (uint8 or
+    int8) holding two E2M1 codes each.  q_sf [S_q, H] and kv_sf [S_kv] int32
+    (or uint32 bit patterns): four UE8M0 block scales each, byte b for elements
+    [32 b, 32 b + 32); weights, ranges and output as ``mqa_logits``.
     """
     import torch
-    f8 = _fp8_types()
+    f8 = (torch.uint8, torch.int8) if fp4 else _fp8_types()
     _dev(q, "q", f8)
     _dev(kv, "kv", f8)
     _dev(q_sf, "q_sf", (torch.int32,))
@@ -213,15 +215,16 @@ def mqa_logits_mx(q, q_sf, kv, kv_sf, weights, k_start, k_end, logits=None, *, c
     _dev(k_end, "k_end", (torch.int32,))
     if q.dim() != 3 or kv.dim() != 2:
         raise ValueError("q must be [S_q, H, D] and kv [S_kv, D]")
-    S_q, H, D = q.shape
+    S_q, H, Db = q.shape
     S_kv = kv.shape[0]
-    if kv.shape[1] != D or weights.shape != (S_q, H) or q_sf.shape != (S_q, H):
+    if kv.shape[1] != Db or weights.shape != (S_q, H) or q_sf.shape != (S_q, H):
         raise ValueError("shape mismatch between q, q_sf, kv and weights")
     if kv_sf.shape != (S_kv,) or k_start.shape != (S_q,) or k_end.shape != (S_q,):
         raise ValueError("shape mismatch in kv_sf / k_start / k_end")
+    D = 2 * Db if fp4 else Db   # elements per row
     logits, ldo, fo = _dense_out(logits, S_q, ldo, compressed, S_kv, out_dtype, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_COMPRESSED if compressed else 0) | \
-            (MQA_CHECK_BOUNDS if check_bounds else 0) | fo
+            (MQA_CHECK_BOUNDS if check_bounds else 0) | (MQA_MXFP4 if fp4 else 0) | fo
     with torch.cuda.device(q.device):
         _check(load_library().mqa_logits_mx(_ptr(q), _ptr(q_sf), _ptr(kv), _ptr(kv_sf), _ptr(weights),
                                             _ptr(k_start), _ptr(k_end), _ptr(logits), S_q, S_kv, H,

@@ -98,16 +98,18 @@ EncodeTiledFn encode_fn()
 }
 
 // 2-D map over a row-major [rows, cols] matrix of `esize`-byte elements with a
-// [box_rows, box_cols] box.
+// [box_rows, box_cols] box; `row_bytes` (if nonzero) overrides the row stride
+// (packed 4-bit elements: cols / 2 bytes).
 mqa_status make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
                        unsigned long long rows, unsigned long long cols, unsigned box_rows,
-                       unsigned box_cols, CUtensorMapSwizzle swz, const char* what)
+                       unsigned box_cols, CUtensorMapSwizzle swz, const char* what,
+                       unsigned long long row_bytes = 0)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * (unsigned long long)esize};
+    cuuint64_t strides[1] = {row_bytes ? row_bytes : cols * (unsigned long long)esize};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -425,12 +427,13 @@ mqa_status paged_mqa_logits_metadata(const int32_t* context_lens, int B, int nex
 namespace {
 // mqa_logits and mqa_logits_scheduled: `schedule_meta` (num_sms + 1 entries
 // from mqa_logits_metadata) or null for the in-kernel split.
-// MX calls pass q_sf and kv_sf (UE8M0 block scales) and no kv_scale.
+// MX calls pass q_sf and kv_sf (UE8M0 block scales) and no kv_scale; fp4:
+// MXFP4 elements (two E2M1 codes per byte, D / 2 bytes per row).
 mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, const float* weights,
                       const int32_t* k_start, const int32_t* k_end, const int32_t* schedule_meta,
                       int sched_sms, void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                       unsigned flags, cudaStream_t stream, const uint32_t* q_sf = nullptr,
-                      const uint32_t* kv_sf = nullptr)
+                      const uint32_t* kv_sf = nullptr, bool fp4 = false)
 {
     const bool mx = q_sf != nullptr || kv_sf != nullptr;
     const bool compressed = (flags & MQA_COMPRESSED) != 0;
@@ -461,6 +464,10 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
             return fail(MQA_ERR_INVALID_ARG, "null pointer");
         if (!aligned(q_sf, 4) || (S_kv > 0 && !aligned(kv_sf, 16)))
             return fail(MQA_ERR_INVALID_ARG, "q_sf must be 4-byte and kv_sf 16-byte aligned");
+        // the copies that spread packed E2M1 codes over shared memory read
+        // from 32-byte aligned rows
+        if (fp4 && (!aligned(q, 32) || (S_kv > 0 && !aligned(kv, 32))))
+            return fail(MQA_ERR_INVALID_ARG, "MXFP4 q and kv must be 32-byte aligned");
     }
     if (!q || !weights || !k_start || !k_end || !logits ||
         (S_kv > 0 && (!kv || (!mx && !kv_scale))))
@@ -533,10 +540,16 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     const int tok = (mx ? kMxN : kMaxN) / H;
     const int N = tok * H;
     const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if ((s = make_map_2d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (unsigned long long)S_q * H, D,
-                         N, D, swz, "q")) != MQA_OK ||
-        (s = make_map_2d(&a.tm_kv, kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, S_kv, D, kBlockKV, D, swz,
-                         "kv")) != MQA_OK ||
+    // MXFP4: the copy spreads each 8 bytes of packed E2M1 codes (16 elements)
+    // over 16 bytes of shared memory, so a row lands as 128 bytes laid out
+    // like an E4M3 row, in the form the block-scaled MMA reads 4-bit operands
+    const CUtensorMapDataType edt =
+        fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const unsigned long long row_bytes = fp4 ? (unsigned long long)D / 2 : 0;
+    if ((s = make_map_2d(&a.tm_q, q, edt, 1, (unsigned long long)S_q * H, D, N, D, swz, "q",
+                         row_bytes)) != MQA_OK ||
+        (s = make_map_2d(&a.tm_kv, kv, edt, 1, S_kv, D, kBlockKV, D, swz, "kv", row_bytes)) !=
+            MQA_OK ||
         // MX: a valid map over the key scales, never used for copies
         (s = make_map_vec_f32(&a.tm_scale, mx ? (const void*)kv_sf : (const void*)kv_scale, S_kv,
                               kBlockKV, "kv_scale")) != MQA_OK ||
@@ -555,6 +568,7 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     p.schedule_meta = schedule_meta;
     p.q_sf = q_sf;
     p.kv_sf = kv_sf;
+    p.mx_fmt = fp4 ? kFmtE2M1 : kFmtE4M3;
     p.width = S_kv;
     p.width_i = S_kv;
     p.tok = tok;
@@ -600,12 +614,11 @@ mqa_status mqa_logits_mx(const void* q, const uint32_t* q_sf, const void* kv, co
                          void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                          unsigned flags, mqa_stream_t stream)
 {
-    if (flags & MQA_MXFP4)
-        return fail(MQA_ERR_UNSUPPORTED, "MXFP4 elements are not supported by this library yet");
     if (!q_sf || !kv_sf)
         return fail(MQA_ERR_INVALID_ARG, "null scale pointer");
     return dense_call(q, kv, nullptr, weights, k_start, k_end, nullptr, 0, logits, S_q, S_kv, H, D,
-                      ldo, flags, (cudaStream_t)stream, q_sf, kv_sf);
+                      ldo, flags & ~(unsigned)MQA_MXFP4, (cudaStream_t)stream, q_sf, kv_sf,
+                      (flags & MQA_MXFP4) != 0);
 }
 
 mqa_status mqa_logits_metadata(const int32_t* k_start, const int32_t* k_end, int S_q, int S_kv,

@@ -112,6 +112,7 @@ struct Params {
     // elements [32 b, 32 b + 32) of a row
     const uint32_t* q_sf;    // [S_q * H]
     const uint32_t* kv_sf;   // [S_kv]
+    uint32_t mx_fmt;         // element format of q and kv: kFmtE4M3 or kFmtE2M1
     long long wait_limit;
     unsigned* status;
 };
@@ -760,6 +761,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pages wbase+L (win0) and wbase+32+L (win1, prefetched).
         int wbase = 0, win0 = -1, win1 = -1, npages = 0;
         const int ppt = PAGED ? kBlockKV / p.block_kv : 1;
+        // bytes a copy of one D-element row counts on its barrier: MXFP4 rows
+        // count their packed global bytes (D / 2), though each lands as D
+        // bytes of shared memory
+        auto elem_bytes = [&](int d) -> int { return MX && p.mx_fmt == kFmtE2M1 ? d / 2 : d; };
         auto page_id = [&](int pg) -> int {
             return (pg >= 0 && pg < npages)
                        ? __ldg(p.block_table + (long long)b * p.max_blocks + pg)
@@ -816,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     const uint32_t bar = smem_u32(&sm.q_full[qb]);
-                    mbar_arrive_expect_tx(bar, (uint32_t)(N * D + p.tok * H * 4));
+                    mbar_arrive_expect_tx(bar, (uint32_t)(N * elem_bytes(D) + p.tok * H * 4));
                     // the block's first query row (token b * blk_stride + tok0)
                     const int row0 = b * p.blk_stride + p.tok0;
                     tma_load_2d(smem_u32(sm.q[qb]), &tm_q, bar, 0, row0 * H);
@@ -891,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         sm.info[stage] = info;
                         const uint32_t bar = smem_u32(&sm.full[stage]);
-                        mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * D));
+                        mbar_arrive_expect_tx(bar, (uint32_t)(kBlockKV * elem_bytes(D)));
                         tma_load_2d(smem_u32(sm.kv[stage]), &tm_kv, bar, 0, t * kBlockKV);
                     }
                 } else {
@@ -986,8 +991,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < D / 32; ++k)
                         mma_mxf8f6f4(d_tmem, da + 2 * k, db + 2 * k,
-                                     idesc_mx_e4m3_f32(kBlockKV, (uint32_t)N, (uint32_t)k), sfa_t, sfb_t,
-                                     k > 0 ? 1u : 0u);
+                                     idesc_mx_f32(kBlockKV, (uint32_t)N, (uint32_t)k, p.mx_fmt), sfa_t,
+                                     sfb_t, k > 0 ? 1u : 0u);
                 } else {
 #pragma unroll
                     for (int k = 0; k < D / 32; ++k)

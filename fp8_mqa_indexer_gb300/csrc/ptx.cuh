@@ -277,7 +277,7 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
 // The scale factors are read from TMEM: for row m of A (M = 128), lane m,
 // column sfa + m / 32; for row n of B, lane n % 32 of every lane quadrant,
 // column sfb + n / 32; in either cell the byte given by the instruction
-// descriptor's scale-factor ids (idesc_mx_e4m3_f32).  This placement was read
+// descriptor's scale-factor ids (idesc_mx_f32).  This placement was read
 // off the hardware with all-ones operands and coded scale bytes.
 __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
@@ -347,13 +347,19 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N)
            | ((M >> 4) << 24);       // M / 16
 }
 
-// Instruction descriptor of the block-scaled MMA (kind::mxf8f6f4): E4M3 x
-// E4M3 -> F32, K-major, M x N, UE8M0 scales; scale-factor id `sf` (the byte
-// of each scale cell) for both operands: the K-block of this MMA.
-__host__ __device__ constexpr uint32_t idesc_mx_e4m3_f32(uint32_t M, uint32_t N, uint32_t sf)
+// Element formats of kind::f8f6f4 / kind::mxf8f6f4 operands (the A and B
+// format fields of the instruction descriptor).
+enum : uint32_t { kFmtE4M3 = 0u, kFmtE2M1 = 5u };
+
+// Instruction descriptor of the block-scaled MMA (kind::mxf8f6f4): `fmt` x
+// `fmt` -> F32 (E4M3, or E2M1 held one element per byte of shared memory),
+// K-major, M x N, UE8M0 scales; scale-factor id `sf` (the byte of each scale
+// cell) for both operands: the K-block of this MMA.
+__host__ __device__ constexpr uint32_t idesc_mx_f32(uint32_t M, uint32_t N, uint32_t sf,
+                                                    uint32_t fmt)
 {
     return (sf << 4)                 // B scale-factor id
-           | (0u << 7) | (0u << 10)  // A, B format: E4M3
+           | (fmt << 7) | (fmt << 10)  // A, B format
            | ((N >> 3) << 17)        // N / 8
            | (1u << 23)              // scale type: UE8M0
            | ((M >> 4) << 24)        // M / 16

@@ -382,16 +382,18 @@ def mx_dense_case(S_q: int, S_kv: int, H: int, *, seed: int, fp4: bool = False,
     return MxDenseCase(name, q, q_sf, kv, kv_sf, weights, ks.contiguous(), ke.contiguous(), fp4, S_kv)
 
 
-def mx_zero_case(S_q: int, S_kv: int, H: int, *, name: str = "mx_zeros") -> MxDenseCase:
-    """The PR #435 reproducer's MXFP8 input: all-zero q, k and weights, every
-    scale byte 127 (0x7f7f7f7f: one), rows [0, S_kv - S_q + i)."""
-    D = 128
+def mx_zero_case(S_q: int, S_kv: int, H: int, *, fp4: bool = False,
+                 name: str = "mx_zeros") -> MxDenseCase:
+    """The PR #435 reproducer's MX input: all-zero q, k and weights (E4M3, or
+    packed E2M1 with 64 bytes per row), every scale byte 127 (0x7f7f7f7f:
+    one), rows [0, S_kv - S_q + i)."""
+    nb = 64 if fp4 else 128
     i = torch.arange(S_q, dtype=torch.int32)
     one = torch.tensor(0x7F7F7F7F, dtype=torch.int32)
-    return MxDenseCase(name, torch.zeros((S_q, H, D), dtype=torch.uint8),
-                       one.repeat(S_q * H).reshape(S_q, H), torch.zeros((S_kv, D), dtype=torch.uint8),
+    return MxDenseCase(name, torch.zeros((S_q, H, nb), dtype=torch.uint8),
+                       one.repeat(S_q * H).reshape(S_q, H), torch.zeros((S_kv, nb), dtype=torch.uint8),
                        one.repeat(S_kv), torch.zeros((S_q, H)), torch.zeros_like(i),
-                       (S_kv - S_q + i).contiguous(), False, S_kv)
+                       (S_kv - S_q + i).contiguous(), fp4, S_kv)
 
 
 # The MXFP8 timing shapes of "[PR #435] ...", section "Performance" (seeded
@@ -401,11 +403,15 @@ MX_CONFIGS = {
     "mx_8k_64k_h64_d128": dict(S_q=8192, S_kv=65536, H=64, seed=1011),
     "mx_2k_32k_h64_d128_zeros": dict(S_q=2048, S_kv=32768, H=64, zeros=True),
     "mx_8k_64k_h64_d128_zeros": dict(S_q=8192, S_kv=65536, H=64, zeros=True),
+    "mx4_2k_32k_h64_d128": dict(S_q=2048, S_kv=32768, H=64, seed=1012, fp4=True),
+    "mx4_2k_32k_h64_d128_zeros": dict(S_q=2048, S_kv=32768, H=64, zeros=True, fp4=True),
+    "mx4_8k_64k_h64_d128_zeros": dict(S_q=8192, S_kv=65536, H=64, zeros=True, fp4=True),
 }
 
 
 def mx_config(name: str) -> MxDenseCase:
     kw = dict(MX_CONFIGS[name])
+    fp4 = kw.pop("fp4", False)
     if kw.pop("zeros", False):
-        return mx_zero_case(kw["S_q"], kw["S_kv"], kw["H"], name=name)
-    return mx_dense_case(kw["S_q"], kw["S_kv"], kw["H"], seed=kw["seed"], name=name)
+        return mx_zero_case(kw["S_q"], kw["S_kv"], kw["H"], fp4=fp4, name=name)
+    return mx_dense_case(kw["S_q"], kw["S_kv"], kw["H"], seed=kw["seed"], fp4=fp4, name=name)

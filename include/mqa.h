@@ -103,25 +103,31 @@ MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_sca
                       int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
 
 /*
- * Dense MQA logits with MXFP8 inputs ("[PR #435] Improve SM100 MX MQA logits
- * clean-output performance": sections "Performance" (MXFP8 timings at H=64,
- * D=128) and "Standalone performance reproducer" (q [S_q, H, D] with q_sf
- * [S_q, H] int32, k [S_kv, D] with ks [S_kv] int32, 0x7f7f7f7f = unit scales)).
+ * Dense MQA logits with MX inputs: MXFP8 (E4M3 elements) or, with the flag
+ * MQA_MXFP4, MXFP4 (E2M1 elements) ("[PR #435] Improve SM100 MX MQA logits
+ * clean-output performance": sections "Performance" (MXFP8 and MXFP4 timings
+ * at H=64, D=128) and "Standalone performance reproducer" (q [S_q, H, D] with
+ * q_sf [S_q, H] int32, k [S_kv, D] with ks [S_kv] int32, 0x7f7f7f7f = unit
+ * scales; MXFP4 elements packed two per byte, D / 2 bytes per row)).
  *
  *   logits[i, j] = sum_h w[i,h] * ReLU(x),  x = sum_b 2^(eq_b - 127) * 2^(ek_b - 127)
  *                                              * sum_{d in block b} q[i,h,d] * kv[j,d]
  *
- *   q        [S_q, H, 128] E4M3 bytes, 16-byte aligned
+ *   q        [S_q, H, 128] E4M3 bytes, 16-byte aligned; MXFP4: [S_q, H, 64]
+ *            bytes, two E2M1 codes per byte, 32-byte aligned
  *   q_sf     [S_q, H] uint32: byte b (b = 0..3, little end first) is the UE8M0
  *            scale eq_b of elements [32 b, 32 b + 32) of q[i,h,:]; 4-byte aligned
- *   kv       [S_kv, 128] E4M3 bytes, 16-byte aligned
+ *   kv       [S_kv, 128] E4M3 bytes, 16-byte aligned; MXFP4: [S_kv, 64] bytes,
+ *            32-byte aligned
  *   kv_sf    [S_kv] uint32, the same for kv[j,:]; 16-byte aligned
- *   weights, k_start, k_end, logits, ldo, flags: as mqa_logits.
- *   D must be 128; H in {8, 32, 64}.  A scale byte of 255 (not a number in
- *   UE8M0) is not allowed.  flags may not hold MQA_MXFP4 (MXFP4 elements: not
- *   supported yet, MQA_ERR_UNSUPPORTED).
+ *   weights, k_start, k_end, logits, ldo: as mqa_logits.
+ *   D is the element count and must be 128; H in {8, 32, 64}.  A scale byte of
+ *   255 (not a number in UE8M0) is not allowed.  Which nibble of a byte holds
+ *   the lower-indexed element does not change any logit: a 32-element block
+ *   is 16 whole bytes, and q and kv pair the same positions.
+ *   flags    MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16 | MQA_MXFP4
  */
-enum { MQA_MXFP4 = 8u };   /* flag of mqa_logits_mx */
+enum { MQA_MXFP4 = 8u };   /* flag of mqa_logits_mx: E2M1 elements */
 MQA_API mqa_status mqa_logits_mx(const void *q, const uint32_t *q_sf, const void *kv,
                                  const uint32_t *kv_sf, const float *weights,
                                  const int32_t *k_start, const int32_t *k_end, void *logits,
