@@ -31,6 +31,7 @@ MQA_COMPRESSED = 2
 MQA_CHECK_BOUNDS = 4
 MQA_MXFP4 = 8
 MQA_OUT_BF16 = 16
+MQA_WEIGHTS_BF16 = 32
 
 STATUS_NAMES = {0: "MQA_OK", 1: "MQA_ERR_INVALID_ARG", 2: "MQA_ERR_UNSUPPORTED", 3: "MQA_ERR_CUDA",
                 4: "MQA_ERR_TIMEOUT", 5: "MQA_ERR_BAD_INPUT"}
@@ -155,7 +156,8 @@ def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: 
     ``schedule_meta`` from ``mqa_logits_metadata`` is given).
 
     q [S_q, H, D] and kv [S_kv, D] are E4M3 (float8_e4m3fn or raw uint8 bytes),
-    kv_scale [S_kv] and weights [S_q, H] float32, k_start / k_end [S_q] int32.
+    kv_scale [S_kv] float32, weights [S_q, H] float32 or bfloat16 (the flag
+    MQA_WEIGHTS_BF16 follows its dtype), k_start / k_end [S_q] int32.
     Returns ``logits`` [S_q, ldo] float32, or bfloat16 with ``out_dtype``
     (allocated when not given; ``ldo`` defaults to S_kv and must be given for
     compressed output).
@@ -165,7 +167,7 @@ def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: 
     _dev(q, "q", f8)
     _dev(kv, "kv", f8)
     _dev(kv_scale, "kv_scale", (torch.float32,))
-    _dev(weights, "weights", (torch.float32,))
+    _dev(weights, "weights", (torch.float32, torch.bfloat16))
     _dev(k_start, "k_start", (torch.int32,))
     _dev(k_end, "k_end", (torch.int32,))
     S_q, H, D = q.shape
@@ -176,7 +178,7 @@ def mqa_logits(q, kv, kv_scale, weights, k_start, k_end, logits=None, *, clean: 
         raise ValueError("shape mismatch in kv_scale / k_start / k_end")
     logits, ldo, fo = _dense_out(logits, S_q, ldo, compressed, S_kv, out_dtype, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_COMPRESSED if compressed else 0) | \
-            (MQA_CHECK_BOUNDS if check_bounds else 0) | fo
+            (MQA_CHECK_BOUNDS if check_bounds else 0) | fo | _weights_flag(weights)
     with torch.cuda.device(q.device):
         if schedule_meta is None:
             _check(load_library().mqa_logits(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights),
@@ -210,7 +212,7 @@ def mqa_logits_mx(q, q_sf, kv, kv_sf, weights, k_start, k_end, logits=None, *, c
     _dev(kv, "kv", f8)
     _dev(q_sf, "q_sf", (torch.int32,))
     _dev(kv_sf, "kv_sf", (torch.int32,))
-    _dev(weights, "weights", (torch.float32,))
+    _dev(weights, "weights", (torch.float32, torch.bfloat16))
     _dev(k_start, "k_start", (torch.int32,))
     _dev(k_end, "k_end", (torch.int32,))
     if q.dim() != 3 or kv.dim() != 2:
@@ -224,7 +226,8 @@ def mqa_logits_mx(q, q_sf, kv, kv_sf, weights, k_start, k_end, logits=None, *, c
     D = 2 * Db if fp4 else Db   # elements per row
     logits, ldo, fo = _dense_out(logits, S_q, ldo, compressed, S_kv, out_dtype, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_COMPRESSED if compressed else 0) | \
-            (MQA_CHECK_BOUNDS if check_bounds else 0) | (MQA_MXFP4 if fp4 else 0) | fo
+            (MQA_CHECK_BOUNDS if check_bounds else 0) | (MQA_MXFP4 if fp4 else 0) | fo | \
+            _weights_flag(weights)
     with torch.cuda.device(q.device):
         _check(load_library().mqa_logits_mx(_ptr(q), _ptr(q_sf), _ptr(kv), _ptr(kv_sf), _ptr(weights),
                                             _ptr(k_start), _ptr(k_end), _ptr(logits), S_q, S_kv, H,
@@ -283,6 +286,12 @@ def paged_mqa_logits_metadata(context_lens, *, next_n: int, block_kv: int,
     return out
 
 
+def _weights_flag(weights) -> int:
+    """MQA_WEIGHTS_BF16 for bf16 weights (fp32 otherwise)."""
+    import torch
+    return MQA_WEIGHTS_BF16 if weights.dtype == torch.bfloat16 else 0
+
+
 def _paged_inputs(q, kv_cache, kv_scales, weights, context_lens, block_table, next_n):
     """Type and shape checks shared by the two paged calls; returns
     (R, H, D, B, next_n, num_blocks, block_kv, max_blocks)."""
@@ -291,7 +300,7 @@ def _paged_inputs(q, kv_cache, kv_scales, weights, context_lens, block_table, ne
     _dev(q, "q", f8)
     _dev(kv_cache, "kv_cache", f8)
     _dev(kv_scales, "kv_scales", (torch.float32,))
-    _dev(weights, "weights", (torch.float32,))
+    _dev(weights, "weights", (torch.float32, torch.bfloat16))
     _dev(context_lens, "context_lens", (torch.int32,))
     _dev(block_table, "block_table", (torch.int32,))
     return paged_shapes(tuple(q.shape), tuple(kv_cache.shape), tuple(kv_scales.shape),
@@ -363,7 +372,7 @@ def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
     num_sms = schedule_meta.shape[0] - 1
     logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device, out_dtype)
     flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0) | \
-        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0)
+        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0) | _weights_flag(weights)
     with torch.cuda.device(q.device):
         _check(load_library().paged_mqa_logits(_ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights),
                                                _ptr(context_lens), _ptr(block_table), max_blocks,
@@ -387,7 +396,7 @@ def paged_mqa_logits_noalloc(q, kv_cache, kv_scales, weights, context_lens, bloc
         raise ValueError("paged_mqa_logits_noalloc needs a caller-provided logits buffer")
     logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0) | \
-        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0)
+        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0) | _weights_flag(weights)
     with torch.cuda.device(q.device):
         _check(load_library().paged_mqa_logits_noalloc(
             _ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights), _ptr(context_lens),

@@ -429,7 +429,7 @@ namespace {
 // from mqa_logits_metadata) or null for the in-kernel split.
 // MX calls pass q_sf and kv_sf (UE8M0 block scales) and no kv_scale; fp4:
 // MXFP4 elements (two E2M1 codes per byte, D / 2 bytes per row).
-mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, const float* weights,
+mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, const void* weights,
                       const int32_t* k_start, const int32_t* k_end, const int32_t* schedule_meta,
                       int sched_sms, void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                       unsigned flags, cudaStream_t stream, const uint32_t* q_sf = nullptr,
@@ -439,7 +439,9 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     const bool compressed = (flags & MQA_COMPRESSED) != 0;
     const bool clean = (flags & MQA_CLEAN) != 0;
     const bool bf16 = (flags & MQA_OUT_BF16) != 0;
-    if (flags & ~(unsigned)(MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16))
+    const bool wbf16 = (flags & MQA_WEIGHTS_BF16) != 0;
+    if (flags & ~(unsigned)(MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16 |
+                            MQA_WEIGHTS_BF16))
         return fail(MQA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
     if (S_q < 0 || S_kv < 0)
         return fail(MQA_ERR_INVALID_ARG, "S_q and S_kv must be >= 0");
@@ -553,8 +555,10 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
         // MX: a valid map over the key scales, never used for copies
         (s = make_map_vec_f32(&a.tm_scale, mx ? (const void*)kv_sf : (const void*)kv_scale, S_kv,
                               kBlockKV, "kv_scale")) != MQA_OK ||
-        (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, S_q, H, tok, H,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, "weights")) != MQA_OK)
+        (s = make_map_2d(&a.tm_w, weights,
+                         wbf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         wbf16 ? 2 : 4, S_q, H, tok, H, CU_TENSOR_MAP_SWIZZLE_NONE, "weights")) !=
+            MQA_OK)
         return s;
     Params& p = a.p;
     p.logits = logits;
@@ -569,6 +573,7 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     p.q_sf = q_sf;
     p.kv_sf = kv_sf;
     p.mx_fmt = fp4 ? kFmtE2M1 : kFmtE4M3;
+    p.w_bf16 = wbf16 ? 1 : 0;
     p.width = S_kv;
     p.width_i = S_kv;
     p.tok = tok;
@@ -589,7 +594,7 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
 }
 }  // namespace
 
-mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, const float* weights,
+mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, const void* weights,
                       const int32_t* k_start, const int32_t* k_end, void* logits, int S_q,
                       int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream)
 {
@@ -598,7 +603,7 @@ mqa_status mqa_logits(const void* q, const void* kv, const float* kv_scale, cons
 }
 
 mqa_status mqa_logits_scheduled(const void* q, const void* kv, const float* kv_scale,
-                                const float* weights, const int32_t* k_start,
+                                const void* weights, const int32_t* k_start,
                                 const int32_t* k_end, const int32_t* schedule_meta, int num_sms,
                                 void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                                 unsigned flags, mqa_stream_t stream)
@@ -610,7 +615,7 @@ mqa_status mqa_logits_scheduled(const void* q, const void* kv, const float* kv_s
 }
 
 mqa_status mqa_logits_mx(const void* q, const uint32_t* q_sf, const void* kv, const uint32_t* kv_sf,
-                         const float* weights, const int32_t* k_start, const int32_t* k_end,
+                         const void* weights, const int32_t* k_start, const int32_t* k_end,
                          void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                          unsigned flags, mqa_stream_t stream)
 {
@@ -657,7 +662,7 @@ namespace {
 // paged_mqa_logits_noalloc (which runs them before it writes its schedule).
 // Sets *nothing_to_do for B == 0.
 mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_scales,
-                          const float* weights, const int32_t* context_lens,
+                          const void* weights, const int32_t* context_lens,
                           const int32_t* block_table, int max_blocks_per_seq,
                           const int32_t* schedule_meta, const void* logits, int B, int next_n,
                           int H, int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
@@ -670,10 +675,10 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_s
         num_sms = 1;
     }
     *nothing_to_do = false;
-    if (flags & ~(unsigned)(MQA_CLEAN | MQA_CHECK_BOUNDS | MQA_OUT_BF16))
+    if (flags & ~(unsigned)(MQA_CLEAN | MQA_CHECK_BOUNDS | MQA_OUT_BF16 | MQA_WEIGHTS_BF16))
         return fail((flags & MQA_COMPRESSED) ? MQA_ERR_UNSUPPORTED : MQA_ERR_INVALID_ARG,
-                    "paged logits take only MQA_CLEAN, MQA_CHECK_BOUNDS and MQA_OUT_BF16 "
-                    "(flags 0x%x)", flags);
+                    "paged logits take only MQA_CLEAN, MQA_CHECK_BOUNDS, MQA_OUT_BF16 and "
+                    "MQA_WEIGHTS_BF16 (flags 0x%x)", flags);
     if (B < 0 || next_n < 1 || num_blocks < 1 || max_blocks_per_seq < 1 || num_sms < 1)
         return fail(MQA_ERR_INVALID_ARG,
                     "need B >= 0, next_n >= 1, num_blocks >= 1, max_blocks_per_seq >= 1, num_sms >= 1");
@@ -711,7 +716,7 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_s
 }  // namespace
 
 mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv_scales,
-                            const float* weights, const int32_t* context_lens,
+                            const void* weights, const int32_t* context_lens,
                             const int32_t* block_table, int max_blocks_per_seq,
                             const int32_t* schedule_meta, void* logits, int B, int next_n, int H,
                             int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
@@ -778,6 +783,7 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     p.blk_stride = next_n;
     p.num_q_blocks = B;
     p.rows = B * next_n;
+    p.w_bf16 = (flags & MQA_WEIGHTS_BF16) ? 1 : 0;
     p.wait_limit = (long long)g_wait_limit.load();
     p.status = st;
     a.grid = num_sms;
@@ -791,9 +797,11 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
         if ((s = make_map_2d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
                              (unsigned long long)B * next_n * H, D, (unsigned)(tok * H), D, swz,
                              "q")) != MQA_OK ||
-            (s = make_map_2d(&a.tm_w, weights, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
-                             (unsigned long long)B * next_n, H, (unsigned)tok, H,
-                             CU_TENSOR_MAP_SWIZZLE_NONE, "weights")) != MQA_OK)
+            (s = make_map_2d(&a.tm_w, weights,
+                             (flags & MQA_WEIGHTS_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                             (flags & MQA_WEIGHTS_BF16) ? 2 : 4, (unsigned long long)B * next_n, H,
+                             (unsigned)tok, H, CU_TENSOR_MAP_SWIZZLE_NONE, "weights")) != MQA_OK)
             return s;
         p.tok = tok;
         p.tok0 = t0;
@@ -818,7 +826,7 @@ int32_t* g_noalloc_ptr[kMaxDevices];
 }  // namespace
 
 mqa_status paged_mqa_logits_noalloc(const void* q, const void* kv_cache, const float* kv_scales,
-                                    const float* weights, const int32_t* context_lens,
+                                    const void* weights, const int32_t* context_lens,
                                     const int32_t* block_table, int max_blocks_per_seq,
                                     void* logits, int B, int next_n, int H, int D, int block_kv,
                                     int num_blocks, int64_t ldo, unsigned flags,

@@ -113,6 +113,7 @@ struct Params {
     const uint32_t* q_sf;    // [S_q * H]
     const uint32_t* kv_sf;   // [S_kv]
     uint32_t mx_fmt;         // element format of q and kv: kFmtE4M3 or kFmtE2M1
+    int w_bf16;              // weights are bf16 (else fp32)
     long long wait_limit;
     unsigned* status;
 };
@@ -332,12 +333,27 @@ struct Epilogue {
 
     __device__ __forceinline__ void enter_block(const UnitInfo& info)
     {
-        const float4* w4 = reinterpret_cast<const float4*>(&sm.w[info.qbuf][col0]);
+        if (p.w_bf16) {
+            // bf16 weights, widened exactly: a bf16 is the top half of an fp32
+            const uint4* w8 = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const uint16_t*>(&sm.w[info.qbuf][0]) + col0);
 #pragma unroll
-        for (int i = 0; i < kEpiCols / 4; ++i) {
-            const float4 v = w4[i];
-            w2[2 * i] = make_float2(v.x, v.y);
-            w2[2 * i + 1] = make_float2(v.z, v.w);
+            for (int i = 0; i < kEpiCols / 8; ++i) {
+                const uint4 v = w8[i];
+                const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    w2[4 * i + j] = make_float2(__uint_as_float(x[j] << 16),
+                                                __uint_as_float(x[j] & 0xffff0000u));
+            }
+        } else {
+            const float4* w4 = reinterpret_cast<const float4*>(&sm.w[info.qbuf][col0]);
+#pragma unroll
+            for (int i = 0; i < kEpiCols / 4; ++i) {
+                const float4 v = w4[i];
+                w2[2 * i] = make_float2(v.x, v.y);
+                w2[2 * i + 1] = make_float2(v.z, v.w);
+            }
         }
         const int a = threadIdx.x & 31;
         __syncwarp();
@@ -821,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     const uint32_t bar = smem_u32(&sm.q_full[qb]);
-                    mbar_arrive_expect_tx(bar, (uint32_t)(N * elem_bytes(D) + p.tok * H * 4));
+                    mbar_arrive_expect_tx(bar, (uint32_t)(N * elem_bytes(D) + p.tok * H * (p.w_bf16 ? 2 : 4)));
                     // the block's first query row (token b * blk_stride + tok0)
                     const int row0 = b * p.blk_stride + p.tok0;
                     tma_load_2d(smem_u32(sm.q[qb]), &tm_q, bar, 0, row0 * H);

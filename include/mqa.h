@@ -78,7 +78,13 @@ enum {
      * elements.  For mqa_logits, mqa_logits_scheduled, mqa_logits_mx and the
      * paged calls ("[PR #435] ...", section "Validation": FP32/BF16 output).
      * The top-k calls read fp32 logits only. */
-    MQA_OUT_BF16 = 16u
+    MQA_OUT_BF16 = 16u,
+    /* Weights as bf16 ([rows, H] 2-byte elements, 16-byte aligned): each is
+     * widened exactly to fp32 and the logits are computed as with fp32
+     * weights of the same values.  For mqa_logits, mqa_logits_scheduled,
+     * mqa_logits_mx and the paged calls ("[PR #435] ...", section
+     * "Validation": FP32/BF16 weights). */
+    MQA_WEIGHTS_BF16 = 32u
 };
 
 /*
@@ -89,16 +95,18 @@ enum {
  *   q         [S_q, H, D]  FP8 E4M3 bytes, row-major, 16-byte aligned
  *   kv        [S_kv, D]    FP8 E4M3 bytes (one KV head), 16-byte aligned
  *   kv_scale  [S_kv]       fp32 per-key scale, 16-byte aligned
- *   weights   [S_q, H]     fp32 per-(token, head) weight, 16-byte aligned
+ *   weights   [S_q, H]     fp32 per-(token, head) weight (bf16 with
+ *                          MQA_WEIGHTS_BF16), 16-byte aligned
  *   k_start, k_end [S_q]   int32 half-open key range of each query row
  *   logits    [S_q, ldo]   fp32 output, 4-byte aligned (bf16, 2-byte aligned,
  *             with MQA_OUT_BF16).  Uncompressed: row i
  *             has S_kv columns and ldo >= S_kv (columns [S_kv, ldo) are never
  *             written).  Compressed: ldo >= every row's range length.
  *   H in {8, 32, 64}, D in {64, 128}; S_q, S_kv >= 0; S_q * H < 2^31.
- *   flags     MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16
+ *   flags     MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16 |
+ *             MQA_WEIGHTS_BF16
  */
-MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_scale, const float *weights,
+MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_scale, const void *weights,
                       const int32_t *k_start, const int32_t *k_end, void *logits, int S_q,
                       int S_kv, int H, int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
 
@@ -125,11 +133,12 @@ MQA_API mqa_status mqa_logits(const void *q, const void *kv, const float *kv_sca
  *   255 (not a number in UE8M0) is not allowed.  Which nibble of a byte holds
  *   the lower-indexed element does not change any logit: a 32-element block
  *   is 16 whole bytes, and q and kv pair the same positions.
- *   flags    MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16 | MQA_MXFP4
+ *   flags    MQA_CLEAN | MQA_COMPRESSED | MQA_CHECK_BOUNDS | MQA_OUT_BF16 |
+ *            MQA_WEIGHTS_BF16 | MQA_MXFP4
  */
 enum { MQA_MXFP4 = 8u };   /* flag of mqa_logits_mx: E2M1 elements */
 MQA_API mqa_status mqa_logits_mx(const void *q, const uint32_t *q_sf, const void *kv,
-                                 const uint32_t *kv_sf, const float *weights,
+                                 const uint32_t *kv_sf, const void *weights,
                                  const int32_t *k_start, const int32_t *k_end, void *logits,
                                  int S_q, int S_kv, int H, int D, int64_t ldo, unsigned flags,
                                  mqa_stream_t stream);
@@ -171,7 +180,7 @@ MQA_API mqa_status mqa_logits_metadata(const int32_t *k_start, const int32_t *k_
  * Other arguments and errors: as mqa_logits.
  */
 MQA_API mqa_status mqa_logits_scheduled(const void *q, const void *kv, const float *kv_scale,
-                                        const float *weights, const int32_t *k_start,
+                                        const void *weights, const int32_t *k_start,
                                         const int32_t *k_end, const int32_t *schedule_meta,
                                         int num_sms, void *logits, int S_q, int S_kv, int H,
                                         int D, int64_t ldo, unsigned flags, mqa_stream_t stream);
@@ -203,7 +212,8 @@ MQA_API mqa_status paged_mqa_logits_metadata(const int32_t *context_lens, int B,
  *                r = b * next_n + t is query t of sequence b
  *   kv_cache     [num_blocks, block_kv, D] FP8 E4M3 bytes, 16-byte aligned
  *   kv_scales    [num_blocks, block_kv] fp32, 16-byte aligned
- *   weights      [B * next_n, H] fp32, 16-byte aligned
+ *   weights      [B * next_n, H] fp32 (bf16 with MQA_WEIGHTS_BF16), 16-byte
+ *                aligned
  *   context_lens [B] int32
  *   block_table  [B, max_blocks_per_seq] int32: logical page p of sequence b
  *                lives in physical block block_table[b, p]
@@ -221,10 +231,11 @@ MQA_API mqa_status paged_mqa_logits_metadata(const int32_t *context_lens, int B,
  *   num_sms      the number of schedule_meta entries minus one (the schedule's
  *                length; the kernel runs one CTA per entry).  Not in the pages'
  *                call, where the schedule tensor carries its own shape.
- *   flags        MQA_CLEAN | MQA_CHECK_BOUNDS (MQA_COMPRESSED is rejected)
+ *   flags        MQA_CLEAN | MQA_CHECK_BOUNDS | MQA_OUT_BF16 | MQA_WEIGHTS_BF16
+ *                (MQA_COMPRESSED is rejected)
  */
 MQA_API mqa_status paged_mqa_logits(const void *q, const void *kv_cache, const float *kv_scales,
-                            const float *weights, const int32_t *context_lens,
+                            const void *weights, const int32_t *context_lens,
                             const int32_t *block_table, int max_blocks_per_seq,
                             const int32_t *schedule_meta, void *logits, int B, int next_n, int H,
                             int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
@@ -256,7 +267,7 @@ MQA_API mqa_status paged_mqa_logits(const void *q, const void *kv_cache, const f
  */
 #define MQA_NOALLOC_MAX_SMS 1024
 MQA_API mqa_status paged_mqa_logits_noalloc(const void *q, const void *kv_cache,
-                                            const float *kv_scales, const float *weights,
+                                            const float *kv_scales, const void *weights,
                                             const int32_t *context_lens,
                                             const int32_t *block_table, int max_blocks_per_seq,
                                             void *logits, int B, int next_n, int H, int D,

@@ -66,7 +66,8 @@ def call_dense(lib, **kw):
     (dict(S_q=-1), 1), (dict(S_kv=-5), 1), (dict(ldo=255), 1), (dict(flags=64), 1),
     (dict(flags=3, ldo=0), 1), (dict(q=None), 1), (dict(logits=None), 1),
     (dict(q=F + 8), 1), (dict(kv_scale=F + 4), 1), (dict(logits=F + 2), 1),
-    (dict(logits=F + 1, flags=1 | 16), 1), (dict(flags=32), 1),
+    (dict(logits=F + 1, flags=1 | 16), 1), (dict(flags=128), 1), (dict(flags=256), 1),
+    (dict(weights=F + 8, flags=1 | 32), 1),
 ])
 def test_dense_rejects_invalid_arguments(lib, kw, status):
     assert call_dense(lib, **kw) == status
