@@ -206,14 +206,16 @@ __device__ __forceinline__ void select_bin(TopkSmem& sm, unsigned need, int& buf
     const unsigned before = block_exclusive_sum(s, sm.warp_sum[buf], total);
     buf ^= 1;
     unsigned acc = total - before - s;   // elements in the bins of higher threads
+    if (acc < need && acc + s >= need) {  // the one thread whose bins hold it
 #pragma unroll
-    for (int q = kB - 1; q >= 0; --q) {
-        if (acc < need && acc + h[q] >= need) {
-            sm.sel_bin = (unsigned)(b0 + q);
-            sm.sel_above = acc;
-            sm.sel_count = h[q];
+        for (int q = kB - 1; q >= 0; --q) {
+            if (acc < need && acc + h[q] >= need) {
+                sm.sel_bin = (unsigned)(b0 + q);
+                sm.sel_above = acc;
+                sm.sel_count = h[q];
+            }
+            acc += h[q];
         }
-        acc += h[q];
     }
     __syncthreads();
     bin = sm.sel_bin;
@@ -459,6 +461,83 @@ __device__ __forceinline__ unsigned compact_row(TopkSmem& sm, const RowView& r,
     return run;
 }
 
+// Element e (0..15) of v, by a four-level select on the bits of e (no local
+// memory for a dynamic register index).
+__device__ __forceinline__ float pick16(const float (&v)[16], unsigned e)
+{
+    float a[8], b[4], c[2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        a[i] = (e & 1u) ? v[2 * i + 1] : v[2 * i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        b[i] = (e & 2u) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        c[i] = (e & 4u) ? b[2 * i + 1] : b[2 * i];
+    return (e & 8u) ? c[1] : c[0];
+}
+
+// Ordered compaction of the row's keys >= thr into the shared list (the one-
+// pass case): each thread owns 16 consecutive columns of a block-wide step
+// (four 16-byte loads), so the order of the list is the thread order and one
+// 32-bit block scan per step places every thread's keys.  For thr at or above
+// the key of +0, key(v) >= thr is a signed compare of v's raw bits with thr's
+// magnitude bits (negative values fail; non-negative ones order as their
+// bits); keys are formed only for the elements taken.  Returns the number of
+// keys found (entries past kCap are counted, not written).
+__device__ __forceinline__ unsigned compact_row_owned(TopkSmem& sm, const RowView& r, unsigned thr,
+                                                      int& buf)
+{
+    const bool fast = thr >= 0x80000000u;
+    const int ithr = (int)(thr & 0x7fffffffu);
+    unsigned run = 0;
+    for (long long base = r.c_start; base < r.c_hi; base += kStep) {
+        const long long c0 = base + 16 * (long long)threadIdx.x;
+        float v[16];
+        unsigned fm = 0;
+        if (c0 >= r.c_lo && c0 + 16 <= r.c_hi) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 x = load4(r.ptr + c0 + 4 * q);
+                v[4 * q] = x.x, v[4 * q + 1] = x.y, v[4 * q + 2] = x.z, v[4 * q + 3] = x.w;
+            }
+            if (fast) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    fm |= (unsigned)((int)__float_as_uint(v[e]) >= ithr) << e;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    fm |= (unsigned)(order_key(v[e]) >= thr) << e;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const bool ok = c0 + e >= r.c_lo && c0 + e < r.c_hi;
+                v[e] = ok ? __ldg(r.ptr + c0 + e) : 0.f;
+                fm |= (unsigned)(ok && order_key(v[e]) >= thr) << e;
+            }
+        }
+        unsigned total;
+        unsigned pos = run + block_exclusive_sum(__popc(fm), sm.warp_sum[buf], total);
+        buf ^= 1;
+        const int idx0 = (int)c0 + r.key_of_col0;
+        while (fm) {
+            const unsigned e = __ffs(fm) - 1;
+            fm &= fm - 1;
+            if (pos < (unsigned)kCap) {
+                sm.cand_key[pos] = order_key(pick16(v, e));
+                sm.cand_idx[pos] = idx0 + (int)e;
+            }
+            ++pos;
+        }
+        run += total;
+    }
+    __syncthreads();
+    return run;
+}
+
 // Threshold key t0 from a sample of the row (one aligned float4 in every
 // `stride` elements, 1/16 of the keys for rows up to 65536): the lower edge of
 // the 24-bit key prefix holding the sample's need-th largest key, with need
@@ -617,7 +696,7 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
             unsigned t0;
             if (2u * k <= (unsigned)kCap && n >= 8192u && n >= 4u * k &&
                 sample_threshold(sm, r, n, k, buf, t0)) {
-                const unsigned m = compact_row<false>(sm, r, 0ull, t0, buf);
+                const unsigned m = compact_row_owned(sm, r, t0, buf);
                 if (m >= k && m <= (unsigned)kCap) {
                     if (!select_from_list_rel(sm, m, k, t0, out, buf))
                         select_from_list(sm, m, k, out, buf);
