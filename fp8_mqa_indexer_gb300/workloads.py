@@ -415,3 +415,73 @@ def mx_config(name: str) -> MxDenseCase:
     if kw.pop("zeros", False):
         return mx_zero_case(kw["S_q"], kw["S_kv"], kw["H"], fp4=fp4, name=name)
     return mx_dense_case(kw["S_q"], kw["S_kv"], kw["H"], seed=kw["seed"], fp4=fp4, name=name)
+
+
+@dataclass
+class PagedMxCase:
+    """Paged decode input with MX (block-scaled) elements: E4M3 or packed E2M1
+    keys in pages, one int32 of four UE8M0 scales per key slot and per
+    (query row, head)."""
+    name: str
+    q: torch.Tensor            # [B*next_n, H, 128] uint8 (E4M3) or [.., 64] (E2M1 pairs)
+    q_sf: torch.Tensor         # [B*next_n, H] int32
+    kv_cache: torch.Tensor     # [num_blocks, block_kv, 128] or [.., 64] uint8
+    kv_sf: torch.Tensor        # [num_blocks, block_kv] int32
+    weights: torch.Tensor      # [B*next_n, H] float32
+    context_lens: torch.Tensor  # [B] int32
+    block_table: torch.Tensor  # [B, max_blocks_per_seq] int32
+    next_n: int
+    ldo: int
+    fp4: bool
+    D = 128
+    clean = True
+
+    @property
+    def B(self):
+        return self.context_lens.shape[0]
+
+    @property
+    def H(self):
+        return self.q.shape[1]
+
+    @property
+    def block_kv(self):
+        return self.kv_cache.shape[1]
+
+    @property
+    def num_blocks(self):
+        return self.kv_cache.shape[0]
+
+    @property
+    def max_blocks_per_seq(self):
+        return self.block_table.shape[1]
+
+
+def paged_mx_case(B: int, next_n: int, H: int, *, seed: int, context_lens, block_kv: int = 64,
+                  num_blocks: Optional[int] = None, fp4: bool = False, sf_lo: int = 124,
+                  sf_hi: int = 130, name: str = "paged_mx") -> PagedMxCase:
+    """Paged MX case: the given context lengths, pages handed out by a random
+    permutation of the blocks, elements as ``mx_dense_case``."""
+    g = _gen(seed)
+    ctx = torch.as_tensor(context_lens, dtype=torch.int64)
+    pages = (ctx.clamp(min=0) + block_kv - 1) // block_kv
+    max_blocks = max(1, int(pages.max()))
+    if num_blocks is None:
+        num_blocks = int(pages.sum()) + 3
+    perm = torch.randperm(num_blocks, generator=g).to(torch.int32)
+    table = torch.full((B, max_blocks), -1, dtype=torch.int32)
+    off = 0
+    for b in range(B):
+        n = int(pages[b])
+        table[b, :n] = perm[off:off + n]
+        off += n
+    D = 128
+    if fp4:
+        q, kv = e2m1_pairs((B * next_n, H, D // 2), g), e2m1_pairs((num_blocks, block_kv, D // 2), g)
+    else:
+        q, kv = e4m3_normal((B * next_n, H, D), g), e4m3_normal((num_blocks, block_kv, D), g)
+    q_sf = packed_scales((B * next_n, H), sf_lo, sf_hi, g)
+    kv_sf = packed_scales((num_blocks, block_kv), sf_lo, sf_hi, g)
+    weights = torch.randn((B * next_n, H), generator=g)
+    return PagedMxCase(name, q, q_sf, kv, kv_sf, weights, ctx.to(torch.int32), table, next_n,
+                       max_blocks * block_kv, fp4)

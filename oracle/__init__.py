@@ -62,10 +62,13 @@ def _load():
             lib.oracle_e2m1_table.argtypes = [P]
             lib.oracle_mx_mqa_logits.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i64,
                                                  u32, i32, i32, P, P]
+            lib.oracle_paged_mx_mqa_logits.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                       i32, i32, i32, i32, i64, u32, i32, i32, P, P]
             for f in (lib.oracle_e4m3_table, lib.oracle_mqa_logits, lib.oracle_paged_mqa_logits,
                       lib.oracle_paged_mqa_logits_metadata, lib.oracle_mqa_logits_metadata,
                       lib.oracle_topk_indices,
-                      lib.oracle_e2m1_table, lib.oracle_mx_mqa_logits):
+                      lib.oracle_e2m1_table, lib.oracle_mx_mqa_logits,
+                      lib.oracle_paged_mx_mqa_logits):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -222,6 +225,44 @@ def mx_mqa_logits(q, q_sf, kv, kv_sf, weights, k_start, k_end, *, fp4: bool = Fa
                                       _flags(clean, compressed), r0, r1, _ptr(out), _ptr(tol))
     if rc != 0:
         raise ValueError("oracle_mx_mqa_logits: invalid arguments")
+    return (out, tol) if with_tol else out
+
+
+def paged_mx_mqa_logits(q, q_sf, kv_cache, kv_sf, weights, context_lens, block_table, *,
+                        next_n: int, fp4: bool = False, ldo: Optional[int] = None,
+                        clean: bool = True, rows: Optional[tuple] = None,
+                        out: Optional[np.ndarray] = None, with_tol: bool = False):
+    """Paged MX logits for rows [r0, r1); see ``mqa_oracle.c``.
+
+    q: [B*next_n, H, 128] E4M3 or [.., 64] packed E2M1 bytes (``fp4``); q_sf
+    [B*next_n, H]; kv_cache [num_blocks, block_kv, 128] or [.., 64]; kv_sf
+    [num_blocks, block_kv]; weights [B*next_n, H] f32.
+    """
+    qn, kvc = _np(q, np.uint8), _np(kv_cache, np.uint8)
+    R, H, qb = qn.shape
+    num_blocks, block_kv, kb = kvc.shape
+    assert kb == qb
+    D = 2 * qb if fp4 else qb
+    bt = _np(block_table, np.int32)
+    B, max_blocks = bt.shape
+    assert R == B * next_n
+    width = max_blocks * block_kv
+    if ldo is None:
+        ldo = width
+    r0, r1 = rows if rows is not None else (0, R)
+    if out is None:
+        out = np.full((r1 - r0, ldo), np.nan, np.float32)
+    tol = np.zeros((r1 - r0, ldo), np.float64) if with_tol else None
+    qs = np.ascontiguousarray(_np(q_sf, np.int64).astype(np.uint32))
+    ks_ = np.ascontiguousarray(_np(kv_sf, np.int64).astype(np.uint32))
+    w = _np(weights, np.float32)
+    cl = _np(context_lens, np.int32)
+    rc = _load().oracle_paged_mx_mqa_logits(_ptr(qn), _ptr(qs), _ptr(kvc), _ptr(ks_), _ptr(w),
+                                            _ptr(cl), _ptr(bt), max_blocks, B, next_n, H, D,
+                                            1 if fp4 else 0, block_kv, num_blocks, ldo,
+                                            _flags(clean, False), r0, r1, _ptr(out), _ptr(tol))
+    if rc != 0:
+        raise ValueError("oracle_paged_mx_mqa_logits: invalid arguments")
     return (out, tol) if with_tol else out
 
 

@@ -617,3 +617,70 @@ int oracle_mx_mqa_logits(const uint8_t *q, const uint32_t *q_sf, const uint8_t *
     }
     return 0;
 }
+
+/*
+ * Paged MX logits for rows [row_begin, row_end): the paged decode of
+ * oracle_paged_mqa_logits with the block-scaled scores of oracle_mx_mqa_logits
+ * ("[PR #314] fix: SM90 paged MQA logits IMA on next_n=4", section "Testing":
+ * the paged MQA logits are tested with FP4 keys on GB200; the element and
+ * scale encoding is the one read above for the dense MX call).  Reading taken:
+ * the per-key UE8M0 scale word sits beside its key in the paged layout, one
+ * uint32 per slot of a block, as the per-key fp32 scale does for FP8 keys.
+ *   q         [B * next_n, H, D] E4M3 bytes, or [.., D/2] packed E2M1 when fp4
+ *   q_sf      [B * next_n, H] uint32, four UE8M0 block scales each
+ *   kv_cache  [num_blocks, block_kv, D] E4M3 bytes, or [.., D/2] packed E2M1
+ *   kv_sf     [num_blocks, block_kv] uint32
+ * Row r = b * next_n + t scores key positions [0, ctx_b - next_n + t + 1);
+ * position j is slot j % block_kv of block block_table[b, j / block_kv].
+ * D must be 128.  tol receives 1e-3 * sum_h |w x| + 1e-5.
+ */
+int oracle_paged_mx_mqa_logits(const uint8_t *q, const uint32_t *q_sf, const uint8_t *kv_cache,
+                               const uint32_t *kv_sf, const float *weights,
+                               const int32_t *context_lens, const int32_t *block_table,
+                               int max_blocks_per_seq, int B, int next_n, int H, int D, int fp4,
+                               int block_kv, int num_blocks, int64_t ldo, unsigned flags,
+                               int row_begin, int row_end, float *logits, double *tol)
+{
+    int clean = (flags & ORACLE_CLEAN) != 0;
+    int64_t width = (int64_t)max_blocks_per_seq * block_kv;
+    if (B < 0 || next_n <= 0 || H <= 0 || D != 128 || block_kv <= 0 || num_blocks < 0 ||
+        max_blocks_per_seq < 0 || ldo < width || row_begin < 0 || row_end > B * next_n ||
+        row_begin > row_end || (flags & ORACLE_COMPRESSED))
+        return -1;
+    const size_t row_bytes = (size_t)(fp4 ? D / 2 : D);
+    for (int r = row_begin; r < row_end; ++r) {
+        int b = r / next_n, t = r % next_n;
+        int ctx = context_lens[b];
+        if (ctx < 0 || (int64_t)ctx > width)
+            return -1;
+        int end = ctx - next_n + t + 1;
+        if (end < 0)
+            end = 0;
+        float *out = logits + (size_t)(r - row_begin) * (size_t)ldo;
+        double *tout = tol ? tol + (size_t)(r - row_begin) * (size_t)ldo : NULL;
+        for (int64_t j = 0; j < width; ++j) {
+            if (j < end) {
+                int32_t blk = block_table[(size_t)b * max_blocks_per_seq + j / block_kv];
+                if (blk < 0 || blk >= num_blocks)
+                    return -1;
+                size_t slot = (size_t)blk * block_kv + (size_t)(j % block_kv);
+                double sum = 0.0, asum = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    double x = mx_dot(q + ((size_t)r * H + h) * row_bytes, q_sf[(size_t)r * H + h],
+                                      kv_cache + slot * row_bytes, kv_sf[slot], D, fp4);
+                    double w = (double)weights[(size_t)r * H + h];
+                    sum += w * (x > 0.0 ? x : 0.0);
+                    asum += fabs(w * x);
+                }
+                out[j] = (float)sum;
+                if (tout)
+                    tout[j] = 1e-3 * asum + 1e-5;
+            } else if (clean) {
+                out[j] = -INFINITY;
+                if (tout)
+                    tout[j] = 0.0;
+            }
+        }
+    }
+    return 0;
+}

@@ -8,7 +8,10 @@ eight magnitudes written as literals; the reproducer's all-zero check (exact
 zeros in range, -inf outside); unit scales reducing MXFP8 to the pinned FP8
 logits with kv_scale = 1; one head with unit weights reducing to torch.matmul
 in float64 on decoded, scaled values; exact power-of-two scaling per block;
-hand-derived block-to-byte cases; the nibble order being unobservable.
+hand-derived block-to-byte cases; the nibble order being unobservable.  The
+paged MX oracle is pinned bit for bit to the dense one over keys gathered
+through the block table by tensor indexing, to the paged FP8 oracle by unit
+scales, and by a hand case.
 """
 import numpy as np
 import pytest
@@ -192,3 +195,71 @@ def test_invalid_arguments(oracle_mod):
     with pytest.raises(ValueError):   # D must be 128
         oracle_mod.mx_mqa_logits(case.q[:, :, :64], case.q_sf, case.kv[:, :64], case.kv_sf,
                                  case.weights, case.k_start, case.k_end)
+
+
+# ------------------------------------------------------------- paged MX
+# The paged MX oracle is pinned to the dense MX oracle above by gathering each
+# sequence's keys through its block table with plain tensor indexing, and to
+# the paged FP8 oracle by unit scales.
+
+def gather_dense(case, b):
+    """Keys and scales of sequence b in position order (torch indexing)."""
+    n = int((case.block_table[b] >= 0).sum())
+    blocks = case.block_table[b, :n].long()
+    kv = case.kv_cache[blocks].reshape(n * case.block_kv, case.kv_cache.shape[2])
+    ks = case.kv_sf[blocks].reshape(n * case.block_kv)
+    return kv, ks
+
+
+@pytest.mark.parametrize("fp4,next_n,block_kv", [(False, 2, 64), (True, 3, 32), (False, 1, 128)])
+def test_paged_mx_equals_dense_mx_of_the_gathered_keys(oracle_mod, fp4, next_n, block_kv):
+    ctx = [1, 70, 129, 0, 200]
+    case = wl.paged_mx_case(5, next_n, 8, seed=48 + next_n, context_lens=ctx, block_kv=block_kv,
+                            fp4=fp4)
+    got = oracle_mod.paged_mx_mqa_logits(case.q, case.q_sf, case.kv_cache, case.kv_sf,
+                                         case.weights, case.context_lens, case.block_table,
+                                         next_n=next_n, fp4=fp4)
+    width = case.ldo
+    for b, c in enumerate(ctx):
+        kv, ks = gather_dense(case, b)
+        rows = slice(b * next_n, (b + 1) * next_n)
+        t = torch.arange(next_n, dtype=torch.int32)
+        ends = (c - next_n + t + 1).clamp(min=0)
+        want = oracle_mod.mx_mqa_logits(case.q[rows], case.q_sf[rows], kv, ks, case.weights[rows],
+                                        torch.zeros(next_n, dtype=torch.int32), ends, fp4=fp4,
+                                        ldo=max(kv.shape[0], 1)) if kv.shape[0] else None
+        g = got[rows]
+        for i in range(next_n):
+            e = int(ends[i])
+            assert np.isneginf(g[i, e:]).all()
+            if e:
+                assert np.array_equal(g[i, :e].view(np.uint32), want[i, :e].view(np.uint32))
+        assert g.shape[1] == width
+
+
+def test_paged_mx_unit_scales_equal_paged_fp8(oracle_mod):
+    ctx = [90, 3, 257]
+    case = wl.paged_mx_case(3, 2, 16, seed=52, context_lens=ctx, block_kv=64, sf_lo=127, sf_hi=127)
+    a = oracle_mod.paged_mx_mqa_logits(case.q, case.q_sf, case.kv_cache, case.kv_sf, case.weights,
+                                       case.context_lens, case.block_table, next_n=2)
+    ones = torch.ones(case.kv_sf.shape, dtype=torch.float32)
+    b = oracle_mod.paged_mqa_logits(case.q, case.kv_cache, ones, case.weights, case.context_lens,
+                                    case.block_table, next_n=2)
+    assert np.array_equal(np.isneginf(a), np.isneginf(b))
+    fin = np.isfinite(b)
+    assert np.allclose(a[fin], b[fin], rtol=1e-6, atol=1e-6)
+
+
+def test_paged_mx_hand_case(oracle_mod):
+    # one sequence of 3 keys in block 1 (block 0 unused), one head, E2M1 code
+    # 2 (1.0) in all 128 elements of q and of key 1; key 2's block 3 scale is
+    # 2^1: x = 4 blocks x 32 = 128 for key 1, 3 x 32 + 64 = 160 for key 2
+    q = torch.full((1, 1, 64), 0x22, dtype=torch.uint8)
+    kv = torch.zeros((2, 4, 64), dtype=torch.uint8)
+    kv[1, 1], kv[1, 2] = 0x22, 0x22
+    ksf = torch.full((2, 4), ONE, dtype=torch.int32)
+    ksf[1, 2] = sf(127, 127, 127, 128)
+    out = oracle_mod.paged_mx_mqa_logits(q, torch.tensor([[ONE]], dtype=torch.int32), kv, ksf,
+                                         torch.tensor([[0.5]]), torch.tensor([3], dtype=torch.int32),
+                                         torch.tensor([[1]], dtype=torch.int32), next_n=1, fp4=True)
+    assert out[0].tolist() == [0.0, 64.0, 80.0, float("-inf")]
