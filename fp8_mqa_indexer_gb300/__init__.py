@@ -21,7 +21,7 @@ from typing import Optional
 
 __all__ = [
     "MQAError", "mqa_logits", "mqa_logits_metadata", "mqa_logits_mx", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
-    "paged_mqa_logits_noalloc", "mqa_topk_indices", "paged_mqa_topk_indices",
+    "paged_mqa_logits_noalloc", "paged_mqa_logits_mx", "mqa_topk_indices", "paged_mqa_topk_indices",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
     "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS", "MQA_OUT_BF16",
 ]
@@ -75,6 +75,8 @@ def load_library() -> ctypes.CDLL:
             "paged_mqa_logits_metadata": ([P, I, I, I, I, P, P], I),
             "paged_mqa_logits": ([P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I64, U, P], I),
             "paged_mqa_logits_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I64, U, P], I),
+            "paged_mqa_logits_mx": ([P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I64, U, P],
+                                    I),
             "mqa_topk_indices": ([P, P, P, P, I, I, I64, I, U, P], I),
             "paged_mqa_topk_indices": ([P, P, P, I, I, I, I64, I, P], I),
             "mqa_get_num_sms": ([I], I),
@@ -379,6 +381,48 @@ def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
                                                _ptr(schedule_meta), _ptr(logits), B, next_n, H, D,
                                                block_kv, num_blocks, num_sms, logits.stride(0), flags,
                                                _stream_handle(stream)))
+    return logits
+
+
+def paged_mqa_logits_mx(q, q_sf, kv_cache, kv_sf, weights, context_lens, block_table,
+                        schedule_meta, logits=None, *, next_n: Optional[int] = None,
+                        clean: bool = True, check_bounds: bool = False, out_dtype=None,
+                        fp4: bool = False, stream=None):
+    """Paged decode MQA logits with MX inputs (C ABI ``paged_mqa_logits_mx``).
+
+    MXFP8: q [B*next_n, H, 128] and kv_cache [num_blocks, block_kv, 128] E4M3;
+    ``fp4``: MXFP4, q [B*next_n, H, 64] and kv_cache [.., 64] bytes (uint8 or
+    int8) of two E2M1 codes.  q_sf [B*next_n, H] and kv_sf [num_blocks,
+    block_kv] int32: four UE8M0 scales each.  The rest as ``paged_mqa_logits``.
+    """
+    import torch
+    f8 = (torch.uint8, torch.int8) if fp4 else _fp8_types()
+    _dev(q, "q", f8)
+    _dev(kv_cache, "kv_cache", f8)
+    _dev(q_sf, "q_sf", (torch.int32,))
+    _dev(kv_sf, "kv_sf", (torch.int32,))
+    _dev(weights, "weights", (torch.float32, torch.bfloat16))
+    _dev(context_lens, "context_lens", (torch.int32,))
+    _dev(block_table, "block_table", (torch.int32,))
+    R, H, Db, B, next_n, num_blocks, block_kv, max_blocks = paged_shapes(
+        tuple(q.shape), tuple(kv_cache.shape), tuple(kv_sf.shape), tuple(weights.shape),
+        tuple(context_lens.shape), tuple(block_table.shape), next_n)
+    if tuple(q_sf.shape) != (R, H):
+        raise ValueError("q_sf must be [B*next_n, H]")
+    D = 2 * Db if fp4 else Db   # elements per row
+    _dev(schedule_meta, "schedule_meta", (torch.int32,))
+    if schedule_meta.dim() != 2 or schedule_meta.shape[1] != 2:
+        raise ValueError("schedule_meta must be an int32 [num_sms + 1, 2] tensor")
+    logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device, out_dtype)
+    flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0) | \
+        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0) | _weights_flag(weights) | \
+        (MQA_MXFP4 if fp4 else 0)
+    with torch.cuda.device(q.device):
+        _check(load_library().paged_mqa_logits_mx(
+            _ptr(q), _ptr(q_sf), _ptr(kv_cache), _ptr(kv_sf), _ptr(weights), _ptr(context_lens),
+            _ptr(block_table), max_blocks, _ptr(schedule_meta), _ptr(logits), B, next_n, H, D,
+            block_kv, num_blocks, schedule_meta.shape[0] - 1, logits.stride(0), flags,
+            _stream_handle(stream)))
     return logits
 
 

@@ -24,6 +24,7 @@ struct LaunchArgs {
 // bf16: __nv_bfloat16 logits instead of float.
 cudaError_t launch_dense(int H, int D, bool bf16, const LaunchArgs& a);
 cudaError_t launch_paged(int H, int D, bool bf16, const LaunchArgs& a);
+cudaError_t launch_paged_mx(int H, bool bf16, const LaunchArgs& a);
 cudaError_t launch_dense_mx(int H, bool bf16, const LaunchArgs& a);
 cudaError_t launch_dense_bf16(int H, int D, const LaunchArgs& a);
 cudaError_t launch_paged_bf16(int H, int D, const LaunchArgs& a);

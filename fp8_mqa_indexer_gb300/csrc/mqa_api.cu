@@ -661,7 +661,7 @@ namespace {
 // Host-side checks of a paged call, shared by paged_mqa_logits and
 // paged_mqa_logits_noalloc (which runs them before it writes its schedule).
 // Sets *nothing_to_do for B == 0.
-mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_scales,
+mqa_status validate_paged(const void* q, const void* kv_cache, const void* kv_scales,
                           const void* weights, const int32_t* context_lens,
                           const int32_t* block_table, int max_blocks_per_seq,
                           const int32_t* schedule_meta, const void* logits, int B, int next_n,
@@ -715,20 +715,34 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const float* kv_s
 }
 }  // namespace
 
-mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv_scales,
-                            const void* weights, const int32_t* context_lens,
-                            const int32_t* block_table, int max_blocks_per_seq,
-                            const int32_t* schedule_meta, void* logits, int B, int next_n, int H,
-                            int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
-                            unsigned flags, mqa_stream_t stream_)
+namespace {
+// paged_mqa_logits and paged_mqa_logits_mx.  MX calls pass q_sf and kv_sf
+// (UE8M0 block scales, one word per query row and head, one per key slot) in
+// place of kv_scales; fp4: MXFP4 elements (two E2M1 codes per byte).
+mqa_status paged_call(const void* q, const void* kv_cache, const float* kv_scales,
+                      const void* weights, const int32_t* context_lens, const int32_t* block_table,
+                      int max_blocks_per_seq, const int32_t* schedule_meta, void* logits, int B,
+                      int next_n, int H, int D, int block_kv, int num_blocks, int num_sms,
+                      int64_t ldo, unsigned flags, cudaStream_t stream,
+                      const uint32_t* q_sf = nullptr, const uint32_t* kv_sf = nullptr,
+                      bool fp4 = false)
 {
-    cudaStream_t stream = (cudaStream_t)stream_;
+    const bool mx = kv_sf != nullptr;
     bool nothing = false;
-    mqa_status v0 = validate_paged(q, kv_cache, kv_scales, weights, context_lens, block_table,
-                                   max_blocks_per_seq, schedule_meta, logits, B, next_n, H, D,
-                                   block_kv, num_blocks, num_sms, ldo, flags, false, &nothing);
+    mqa_status v0 = validate_paged(q, kv_cache, mx ? (const void*)kv_sf : (const void*)kv_scales,
+                                   weights, context_lens, block_table, max_blocks_per_seq,
+                                   schedule_meta, logits, B, next_n, H, D, block_kv, num_blocks,
+                                   num_sms, ldo, flags, false, &nothing);
     if (v0 != MQA_OK || nothing)
         return v0;
+    if (mx) {
+        if (D != 128)
+            return fail(MQA_ERR_UNSUPPORTED, "MX calls need D = 128 (four 32-element blocks)");
+        if (!q_sf || !aligned(q_sf, 4))
+            return fail(MQA_ERR_INVALID_ARG, "q_sf must be non-null and 4-byte aligned");
+        if (fp4 && (!aligned(q, 32) || !aligned(kv_cache, 32)))
+            return fail(MQA_ERR_INVALID_ARG, "MXFP4 q and kv_cache must be 32-byte aligned");
+    }
     const long long width = (long long)max_blocks_per_seq * block_kv;
 
     int dev;
@@ -761,11 +775,16 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     LaunchArgs a;
     memset(&a, 0, sizeof(a));
     const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if ((s = make_map_2d(&a.tm_kv, kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                         (unsigned long long)num_blocks * block_kv, D, block_kv, D, swz,
-                         "kv_cache")) != MQA_OK ||
-        (s = make_map_vec_f32(&a.tm_scale, kv_scales, (unsigned long long)num_blocks * block_kv,
-                              block_kv, "kv_scales")) != MQA_OK)
+    // MXFP4: packed E2M1 rows land as 128-byte rows (see dense_call)
+    const CUtensorMapDataType edt =
+        fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const unsigned long long row_bytes = fp4 ? (unsigned long long)D / 2 : 0;
+    if ((s = make_map_2d(&a.tm_kv, kv_cache, edt, 1, (unsigned long long)num_blocks * block_kv, D,
+                         block_kv, D, swz, "kv_cache", row_bytes)) != MQA_OK ||
+        // MX: a valid map over the key scale words, never used for copies
+        (s = make_map_vec_f32(&a.tm_scale, mx ? (const void*)kv_sf : (const void*)kv_scales,
+                              (unsigned long long)num_blocks * block_kv, block_kv, "kv_scales")) !=
+            MQA_OK)
         return s;
     Params& p = a.p;
     p.logits = logits;
@@ -778,25 +797,29 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
     p.next_n = next_n;
     p.block_kv = block_kv;
     p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
     p.width = width;
     p.width_i = (int)width;
     p.blk_stride = next_n;
     p.num_q_blocks = B;
     p.rows = B * next_n;
     p.w_bf16 = (flags & MQA_WEIGHTS_BF16) ? 1 : 0;
+    p.q_sf = q_sf;
+    p.kv_sf = kv_sf;
+    p.mx_fmt = fp4 ? kFmtE2M1 : kFmtE4M3;
     p.wait_limit = (long long)g_wait_limit.load();
     p.status = st;
     a.grid = num_sms;
     a.stream = stream;
     // A sequence's next_n query tokens are split into query atoms of at most
     // kMaxN / H tokens (one accumulator of kMaxN columns holds an atom's
-    // tokens x heads); each atom is one launch over the same schedule.
-    const int atom = kMaxN / H;
+    // tokens x heads; kMxN for MX calls, whose scale factors share TMEM); each
+    // atom is one launch over the same schedule.
+    const int atom = (mx ? kMxN : kMaxN) / H;
     for (int t0 = 0; t0 < next_n; t0 += atom) {
         const int tok = next_n - t0 < atom ? next_n - t0 : atom;
-        if ((s = make_map_2d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                             (unsigned long long)B * next_n * H, D, (unsigned)(tok * H), D, swz,
-                             "q")) != MQA_OK ||
+        if ((s = make_map_2d(&a.tm_q, q, edt, 1, (unsigned long long)B * next_n * H, D,
+                             (unsigned)(tok * H), D, swz, "q", row_bytes)) != MQA_OK ||
             (s = make_map_2d(&a.tm_w, weights,
                              (flags & MQA_WEIGHTS_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
@@ -805,13 +828,42 @@ mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv
             return s;
         p.tok = tok;
         p.tok0 = t0;
-        cudaError_t e = launch_paged(H, D, (flags & MQA_OUT_BF16) != 0, a);
+        cudaError_t e = mx ? launch_paged_mx(H, (flags & MQA_OUT_BF16) != 0, a)
+                           : launch_paged(H, D, (flags & MQA_OUT_BF16) != 0, a);
         if (e == cudaErrorNotSupported)
             return fail(MQA_ERR_UNSUPPORTED, "no paged kernel for H=%d D=%d", H, D);
         if (e != cudaSuccess)
             return cuda_fail(e, "paged kernel launch");
     }
     return MQA_OK;
+}
+}  // namespace
+
+mqa_status paged_mqa_logits(const void* q, const void* kv_cache, const float* kv_scales,
+                            const void* weights, const int32_t* context_lens,
+                            const int32_t* block_table, int max_blocks_per_seq,
+                            const int32_t* schedule_meta, void* logits, int B, int next_n, int H,
+                            int D, int block_kv, int num_blocks, int num_sms, int64_t ldo,
+                            unsigned flags, mqa_stream_t stream)
+{
+    return paged_call(q, kv_cache, kv_scales, weights, context_lens, block_table,
+                      max_blocks_per_seq, schedule_meta, logits, B, next_n, H, D, block_kv,
+                      num_blocks, num_sms, ldo, flags, (cudaStream_t)stream);
+}
+
+mqa_status paged_mqa_logits_mx(const void* q, const uint32_t* q_sf, const void* kv_cache,
+                               const uint32_t* kv_sf, const void* weights,
+                               const int32_t* context_lens, const int32_t* block_table,
+                               int max_blocks_per_seq, const int32_t* schedule_meta, void* logits,
+                               int B, int next_n, int H, int D, int block_kv, int num_blocks,
+                               int num_sms, int64_t ldo, unsigned flags, mqa_stream_t stream)
+{
+    if (!kv_sf || !q_sf)
+        return fail(MQA_ERR_INVALID_ARG, "null scale pointer");
+    return paged_call(q, kv_cache, nullptr, weights, context_lens, block_table, max_blocks_per_seq,
+                      schedule_meta, logits, B, next_n, H, D, block_kv, num_blocks, num_sms, ldo,
+                      flags & ~(unsigned)MQA_MXFP4, (cudaStream_t)stream, q_sf, kv_sf,
+                      (flags & MQA_MXFP4) != 0);
 }
 
 // ------------------------------------------------ no-allocation paged call

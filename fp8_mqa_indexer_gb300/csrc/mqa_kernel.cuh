@@ -100,6 +100,7 @@ struct Params {
     int next_n;
     int block_kv;
     int max_blocks;
+    int num_blocks;          // physical blocks of the pool (bounds the scale-word loads)
     // shared
     long long width;     // logical columns of an uncompressed row
     int width_i;         // the same, as an int (below 2^31 - 256)
@@ -574,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     Smem<D, MX>& sm = *reinterpret_cast<Smem<D, MX>*>(smem_raw + pad);
-    static_assert(!MX || (!PAGED && D == 128), "MX calls are dense with D = 128");
+    static_assert(!MX || D == 128, "MX calls have D = 128");
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -820,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the block's B-operand scales, transposed for tcgen05.cp:
                     // half c, row r, word j <- column n = 128 c + 32 j + r
                     const long long r0 = (long long)(b * p.blk_stride + p.tok0) * H;
-                    const long long nq = (long long)p.S_q * H;
+                    const long long nq = (long long)p.rows * H;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         uint32_t v[4];
@@ -848,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int stage = u % S;
             uint32_t ksf[4];
             if (mine) {
-                if constexpr (MX) {
+                if constexpr (MX && !PAGED) {
                     // the tile's key scales, loaded before the wait for the stage
                     // (the wait hides their latency): word j <- key 32 j + lane
 #pragma unroll
@@ -857,16 +858,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ksf[j] = key < p.S_kv ? __ldg(p.kv_sf + key) : 0x7f7f7f7fu;
                     }
                 }
-                if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx, kProducerSleepNs))
-                    break;
-                const bool last = (u + 1 == n_units) || (t + 1 >= thi);
-                const UnitInfo info{b, t, k_block & 1,
-                                    (first ? kFirstOfBlock : 0) | (last ? kLastOfBlock : 0)};
-                if (PAGED) {
-                    // gather the pages of tile t through the block table
-                    const long long keys = min((long long)ctx, p.width);
-                    int ids[4];
-                    uint32_t bytes = 0;
+                // paged: the physical blocks of tile t's pages (-1: none)
+                const long long keys = PAGED ? min((long long)ctx, p.width) : 0;
+                int ids[4];
+                uint32_t bytes = 0;
+                auto page_ids = [&]() {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         ids[k] = -1;
@@ -880,9 +876,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int id = __shfl_sync(0xffffffffu, win0, pg - wbase);
                             if ((long long)pg * p.block_kv < keys && pg < p.max_blocks) {
                                 ids[k] = id;
-                                bytes += (uint32_t)(p.block_kv * (D + 4));
+                                bytes += (uint32_t)(p.block_kv * (MX ? elem_bytes(D) : D + 4));
                             }
                         }
+                    }
+                };
+                if constexpr (PAGED && MX) {
+                    // the block table first, then the scale word of each key
+                    // slot of the tile (word j <- key 32 j + lane, whose page is
+                    // 32 j / block_kv), loaded before the wait hides their latency
+                    page_ids();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int kk = 32 * j + lane;
+                        const int pi = (32 * j) / p.block_kv;
+                        const int id = pi == 0 ? ids[0] : pi == 1 ? ids[1] : pi == 2 ? ids[2] : ids[3];
+                        ksf[j] = (id >= 0 && id < p.num_blocks && (long long)t * kBlockKV + kk < keys)
+                                     ? __ldg(p.kv_sf + (long long)id * p.block_kv + (kk % p.block_kv))
+                                     : 0x7f7f7f7fu;
+                    }
+                }
+                if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx, kProducerSleepNs))
+                    break;
+                const bool last = (u + 1 == n_units) || (t + 1 >= thi);
+                const UnitInfo info{b, t, k_block & 1,
+                                    (first ? kFirstOfBlock : 0) | (last ? kLastOfBlock : 0)};
+                if (PAGED) {
+                    // gather the pages of tile t through the block table
+                    if constexpr (!MX)
+                        page_ids();
+                    if constexpr (MX) {
+                        *reinterpret_cast<uint4*>(&sm.sfa[stage][lane][0]) =
+                            make_uint4(ksf[0], ksf[1], ksf[2], ksf[3]);
+                        fence_proxy_async_smem();   // read by tcgen05.cp (async proxy)
+                        __syncwarp();
                     }
                     if (lane == 0) {
                         sm.info[stage] = info;
@@ -893,8 +920,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (k < ppt && ids[k] >= 0) {
                                 tma_load_2d(smem_u32(sm.kv[stage]) + k * p.block_kv * D, &tm_kv, bar, 0,
                                             ids[k] * p.block_kv);
-                                tma_load_2d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale, bar,
-                                            ids[k] * p.block_kv, 0);
+                                if constexpr (!MX)
+                                    tma_load_2d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale,
+                                                bar, ids[k] * p.block_kv, 0);
                             }
                         }
                     }

@@ -242,6 +242,36 @@ MQA_API mqa_status paged_mqa_logits(const void *q, const void *kv_cache, const f
                             unsigned flags, mqa_stream_t stream);
 
 /*
+ * Paged decode MQA logits with MX keys and queries: MXFP8 (E4M3) or, with the
+ * flag MQA_MXFP4, MXFP4 (E2M1, two codes per byte) elements and UE8M0 block
+ * scales ("[PR #314] fix: SM90 paged MQA logits IMA on next_n=4", section
+ * "Testing": the paged logits are tested with FP4 keys on GB200; the element
+ * and scale encoding as mqa_logits_mx).  Row r = b * next_n + t scores key
+ * positions [0, context_lens[b] - next_n + t + 1) with
+ *   x = sum_b 2^(eq_b - 127) * 2^(ek_b - 127) * sum_{d in block b} q[r,h,d] * kv[j,d]
+ * in place of kv_scale * <q, kv>; everything else as paged_mqa_logits.
+ *
+ *   q         [B * next_n, H, 128] E4M3 bytes (16-byte aligned), or with
+ *             MQA_MXFP4 [B * next_n, H, 64] packed E2M1 bytes (32-byte aligned)
+ *   q_sf      [B * next_n, H] uint32, four UE8M0 scales each; 4-byte aligned
+ *   kv_cache  [num_blocks, block_kv, 128] E4M3 bytes, or [.., 64] packed E2M1
+ *             (alignment as q)
+ *   kv_sf     [num_blocks, block_kv] uint32: the scale word of each key slot,
+ *             beside its key as kv_scales is for FP8 keys; 16-byte aligned
+ *   D must be 128; H in {16, 32, 64}; query atoms of at most 192 / H tokens
+ *   (the scale factors share the accumulator memory).
+ *   flags     MQA_CLEAN | MQA_CHECK_BOUNDS | MQA_OUT_BF16 | MQA_WEIGHTS_BF16 |
+ *             MQA_MXFP4
+ */
+MQA_API mqa_status paged_mqa_logits_mx(const void *q, const uint32_t *q_sf, const void *kv_cache,
+                                       const uint32_t *kv_sf, const void *weights,
+                                       const int32_t *context_lens, const int32_t *block_table,
+                                       int max_blocks_per_seq, const int32_t *schedule_meta,
+                                       void *logits, int B, int next_n, int H, int D, int block_kv,
+                                       int num_blocks, int num_sms, int64_t ldo, unsigned flags,
+                                       mqa_stream_t stream);
+
+/*
  * Paged decode MQA logits without any caller-provided or library-allocated
  * scratch (the pages have no counterpart to this call; it is an addition of
  * this library).  Arguments are those of paged_mqa_logits minus

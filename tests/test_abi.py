@@ -102,6 +102,27 @@ def test_paged_zero_batch_is_a_no_op(lib):
     assert call_paged(lib, B=0) == 0
 
 
+def call_paged_mx(lib, **kw):
+    a = dict(q=F, q_sf=F, kv_cache=F, kv_sf=F, weights=F, context_lens=F, block_table=F,
+             max_blocks=16, meta=F, logits=F, B=2, next_n=2, H=64, D=128, block_kv=64,
+             num_blocks=40, num_sms=8, ldo=1024, flags=1)
+    a.update(kw)
+    return lib.paged_mqa_logits_mx(a["q"], a["q_sf"], a["kv_cache"], a["kv_sf"], a["weights"],
+                                   a["context_lens"], a["block_table"], a["max_blocks"], a["meta"],
+                                   a["logits"], a["B"], a["next_n"], a["H"], a["D"], a["block_kv"],
+                                   a["num_blocks"], a["num_sms"], a["ldo"], a["flags"], None)
+
+
+# flags=1 | 8: MXFP4 with the 16-byte aligned fake pointers (32 bytes needed)
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), 2), (dict(q_sf=None), 1), (dict(kv_sf=None), 1), (dict(q_sf=F + 2), 1),
+    (dict(flags=1 | 8), 1), (dict(flags=2), 2), (dict(H=8), 2), (dict(block_kv=48), 2),
+    (dict(ldo=1000), 1),
+])
+def test_paged_mx_rejects_invalid_arguments(lib, kw, status):
+    assert call_paged_mx(lib, **kw) == status
+
+
 @pytest.mark.parametrize("kw,status", [(dict(block_kv=48), 2), (dict(num_sms=0), 1),
                                        (dict(next_n=0), 1), (dict(meta=None), 1)])
 def test_metadata_rejects_invalid_arguments(lib, kw, status):
