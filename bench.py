@@ -245,17 +245,19 @@ def make_case(workload: str):
         return wl.topk_config(workload)
     if workload in wl.PAGED_CONFIGS:
         return wl.paged_config(workload)
+    if workload in wl.PAGED_MX_CONFIGS:
+        return wl.paged_mx_config(workload)
     if workload in wl.MX_CONFIGS:
         return wl.mx_config(workload)
     if workload not in wl.DENSE_CONFIGS:
         raise SystemExit(f"unknown workload {workload!r}; known: "
-                         f"{sorted(wl.DENSE_CONFIGS) + sorted(wl.PAGED_CONFIGS) + sorted(wl.TOPK_CONFIGS) + sorted(wl.MX_CONFIGS)}")
+                         f"{sorted(wl.DENSE_CONFIGS) + sorted(wl.PAGED_CONFIGS) + sorted(wl.PAGED_MX_CONFIGS) + sorted(wl.TOPK_CONFIGS) + sorted(wl.MX_CONFIGS)}")
     return wl.dense_config(workload)
 
 
 def is_paged(workload: str) -> bool:
     from fp8_mqa_indexer_gb300 import workloads as wl
-    return workload in wl.PAGED_CONFIGS
+    return workload in wl.PAGED_CONFIGS or workload in wl.PAGED_MX_CONFIGS
 
 
 def is_mx(workload: str) -> bool:
@@ -508,6 +510,11 @@ def paged_oracle_sample(case, budget_s: float):
 
         def one(seq):
             r0 = seq * case.next_n
+            if hasattr(case, "q_sf"):   # MX keys
+                return oracle.paged_mx_mqa_logits(case.q, case.q_sf, case.kv_cache, case.kv_sf,
+                                                  case.weights, case.context_lens, case.block_table,
+                                                  next_n=case.next_n, fp4=case.fp4, ldo=case.ldo,
+                                                  rows=(r0, r0 + case.next_n))
             return oracle.paged_mqa_logits(case.q, case.kv_cache, case.kv_scales, case.weights,
                                            case.context_lens, case.block_table,
                                            next_n=case.next_n, ldo=case.ldo, clean=case.clean,
@@ -530,25 +537,38 @@ def bench_paged(args, mqa, torch, dev, stream):
     R = case.B * case.next_n
     ctx = case.context_lens.to(torch.int64)
     pages = ((ctx.clamp(min=0) + case.block_kv - 1) // case.block_kv)
-    # algorithmic bytes: every key of every context (E4M3 row + fp32 scale) once,
-    # the query rows, weights, block-table entries in use, and the whole output
-    alg_bytes = (int(ctx.clamp(min=0).sum()) * (case.D + 4) + case.q.numel() + case.weights.numel() * 4
+    mx = hasattr(case, "q_sf")   # MX keys: a scale word per key slot, per query row and head
+    # algorithmic bytes: every key of every context (its row of E4M3 or packed
+    # E2M1 bytes + its fp32 scale or scale word) once, the query rows (and
+    # their scale words), weights, block-table entries in use, and the output
+    alg_bytes = (int(ctx.clamp(min=0).sum()) * (case.kv_cache.shape[2] + 4) + case.q.numel()
+                 + (case.q_sf.numel() * 4 if mx else 0) + case.weights.numel() * 4
                  + int(pages.sum()) * 4 + case.B * 4 + R * case.ldo * 4)
-    q, kvc = case.q.to(dev), case.kv_cache.to(dev)
-    sc, w = case.kv_scales.to(dev), case.weights.to(dev)
-    cl, bt = case.context_lens.to(dev), case.block_table.to(dev)
+    src = dict(q=case.q, kvc=case.kv_cache, sc=case.kv_sf if mx else case.kv_scales, w=case.weights,
+               cl=case.context_lens, bt=case.block_table)
+    if mx:
+        src["qsf"] = case.q_sf
+    dd = {k: v.to(dev) for k, v in src.items()}
+    cl = dd["cl"]
     out = torch.empty((R, case.ldo), dtype=torch.float32, device=dev)
     meta = torch.empty((mqa.get_num_sms(dev) + 1, 2), dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def step(q_, kvc_, sc_, w_, cl_, bt_):
-        mqa.paged_mqa_logits_metadata(cl_, next_n=case.next_n, block_kv=case.block_kv, out=meta)
-        mqa.paged_mqa_logits(q_, kvc_, sc_, w_, cl_, bt_, meta, out, next_n=case.next_n,
-                             clean=case.clean)
+    def logits(d, o):
+        if mx:
+            mqa.paged_mqa_logits_mx(d["q"], d["qsf"], d["kvc"], d["sc"], d["w"], d["cl"], d["bt"],
+                                    meta, o, next_n=case.next_n, fp4=case.fp4)
+        else:
+            mqa.paged_mqa_logits(d["q"], d["kvc"], d["sc"], d["w"], d["cl"], d["bt"], meta, o,
+                                 next_n=case.next_n, clean=case.clean)
+
+    def step(d):
+        mqa.paged_mqa_logits_metadata(d["cl"], next_n=case.next_n, block_kv=case.block_kv, out=meta)
+        logits(d, out)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        step(q, kvc, sc, w, cl, bt)
+        step(dd)
     torch.cuda.synchronize()
     assert mqa.device_status() == 0
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -562,7 +582,7 @@ def bench_paged(args, mqa, torch, dev, stream):
         flush.zero_()
         pre_spin(torch)
         a.record(stream)
-        step(q, kvc, sc, w, cl, bt)
+        step(dd)
         b.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -577,21 +597,19 @@ def bench_paged(args, mqa, torch, dev, stream):
         flush.zero_()
         pre_spin(torch)
         a.record(stream)
-        mqa.paged_mqa_logits(q, kvc, sc, w, cl, bt, meta, out, next_n=case.next_n, clean=case.clean)
+        logits(dd, out)
         b.record(stream)
     torch.cuda.synchronize()
     assert mqa.device_status() == 0
     kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
 
-    host = {k: v.pin_memory() for k, v in dict(q=case.q, kvc=case.kv_cache, sc=case.kv_scales,
-                                                w=case.weights, cl=case.context_lens,
-                                                bt=case.block_table).items()}
+    host = {k: v.pin_memory() for k, v in src.items()}
     host_out = torch.empty((R, case.ldo), dtype=torch.float32, pin_memory=True)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
 
     def e2e_step():
         d = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
-        step(d["q"], d["kvc"], d["sc"], d["w"], d["cl"], d["bt"])
+        step(d)
         host_out.copy_(out, non_blocking=True)
 
     e2e_step()
@@ -608,7 +626,7 @@ def bench_paged(args, mqa, torch, dev, stream):
     if not args.no_graph:
         def call(o):
             mqa.paged_mqa_logits_metadata(cl, next_n=case.next_n, block_kv=case.block_kv, out=meta)
-            mqa.paged_mqa_logits(q, kvc, sc, w, cl, bt, meta, o, next_n=case.next_n, clean=case.clean)
+            logits(dd, o)
         graph = graph_timing(torch, call, out)
         graph["gbs_at_median"] = alg_bytes / (graph["median_ms"] * 1e-3) / 1e9
     assert mqa.device_status() == 0
@@ -620,19 +638,23 @@ def bench_paged(args, mqa, torch, dev, stream):
         "value": flops / (ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
+        "dtype": (("mxfp4 (e2m1 x e2m1" if case.fp4 else "mxfp8 (e4m3 x e4m3") +
+                  ", ue8m0 block 32) -> f32") if mx else "e4m3 x e4m3 -> f32",
+        "data": "synthetic",
         "config": {"workload": args.workload, "B": case.B, "next_n": case.next_n, "H": case.H,
                    "D": case.D, "block_kv": case.block_kv, "num_blocks": case.num_blocks,
                    "ldo": case.ldo, "valid_logits": valid, "clean": case.clean,
                    "l2": "flushed (256 MiB write) before every timed step; the pool exceeds L2",
-                   "step": "paged_mqa_logits_metadata + paged_mqa_logits"},
+                   "step": "paged_mqa_logits_metadata + " +
+                           ("paged_mqa_logits_mx" if mx else "paged_mqa_logits")},
         **percentiles(times_ms),
         "graph_timing": graph,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "kernel_ms": kernel_ms,
-                     "kernel": "paged_mqa_logits alone (event mean over the timed steps, L2 "
-                               "flushed); the step's value includes the schedule kernel",
+                     "kernel": ("paged_mqa_logits_mx" if mx else "paged_mqa_logits") +
+                               " alone (event mean over the timed steps, L2 flushed); the step's "
+                               "value includes the schedule kernel",
                      "step_gbs": alg_bytes / (ms_per_step * 1e-3) / 1e9,
                      "traffic": recorded_traffic(args.workload),
                      "algorithmic_bytes": alg_bytes, "peak_source": f"{peaks_src} HBM copy"},

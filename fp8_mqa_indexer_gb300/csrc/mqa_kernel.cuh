@@ -592,7 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&sm.full[s]), 1);
+            // paged MX: the 32 lanes of the producer that copies the key
+            // scale words arrive too (cp.async completion)
+            mbar_init(smem_u32(&sm.full[s]), (PAGED && MX) ? 33 : 1);
             mbar_init(smem_u32(&sm.empty[s]), 1 + n_epi);
         }
         for (int k = 0; k < 2; ++k) {
@@ -881,21 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 };
-                if constexpr (PAGED && MX) {
-                    // the block table first, then the scale word of each key
-                    // slot of the tile (word j <- key 32 j + lane, whose page is
-                    // 32 j / block_kv), loaded before the wait hides their latency
-                    page_ids();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int kk = 32 * j + lane;
-                        const int pi = (32 * j) / p.block_kv;
-                        const int id = pi == 0 ? ids[0] : pi == 1 ? ids[1] : pi == 2 ? ids[2] : ids[3];
-                        ksf[j] = (id >= 0 && id < p.num_blocks && (long long)t * kBlockKV + kk < keys)
-                                     ? __ldg(p.kv_sf + (long long)id * p.block_kv + (kk % p.block_kv))
-                                     : 0x7f7f7f7fu;
-                    }
-                }
+                if constexpr (PAGED && MX)
+                    page_ids();   // the block-table lookups overlap the wait
                 if (!warp_wait(smem_u32(&sm.empty[stage]), ((u / S) & 1) ^ 1, wctx, kProducerSleepNs))
                     break;
                 const bool last = (u + 1 == n_units) || (t + 1 >= thi);
@@ -906,10 +895,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (!MX)
                         page_ids();
                     if constexpr (MX) {
-                        *reinterpret_cast<uint4*>(&sm.sfa[stage][lane][0]) =
-                            make_uint4(ksf[0], ksf[1], ksf[2], ksf[3]);
-                        fence_proxy_async_smem();   // read by tcgen05.cp (async proxy)
-                        __syncwarp();
+                        // the scale word of each key slot of the tile, copied by
+                        // cp.async straight into the transposed layout tcgen05.cp
+                        // reads (row lane, word j <- key 32 j + lane, whose page
+                        // is 32 j / block_kv); slots past the context copy word
+                        // 0 (their keys are masked); each lane's arrival on the
+                        // stage barrier waits for its copies
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int kk = 32 * j + lane;
+                            const int pi = (32 * j) / p.block_kv;
+                            const int id = pi == 0 ? ids[0] : pi == 1 ? ids[1] : pi == 2 ? ids[2] : ids[3];
+                            const bool ok =
+                                id >= 0 && id < p.num_blocks && (long long)t * kBlockKV + kk < keys;
+                            cp_async_4(smem_u32(&sm.sfa[stage][lane][j]),
+                                       p.kv_sf + (ok ? (long long)id * p.block_kv + (kk % p.block_kv) : 0));
+                        }
+                        cp_async_mbar_arrive_noinc(smem_u32(&sm.full[stage]));
                     }
                     if (lane == 0) {
                         sm.info[stage] = info;
@@ -1025,6 +1027,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // scale factors into TMEM (in issue order before the MMAs
                     // that read them): the key tile's into the slot of this
                     // unit's parity, the query block's at its first unit
+                    if constexpr (PAGED)
+                        fence_proxy_async_smem();   // cp.async-written scale words -> tcgen05.cp
                     const uint32_t sfa_t = tmem_base + kMxSfaCol + (uint32_t)((u & 1) * 4);
                     const uint32_t sfb_t = tmem_base + kMxSfbCol + (uint32_t)(info.qbuf * 8);
                     tmem_cp_32x128b_x4(sfa_t, sf_desc(smem_u32(&sm.sfa[stage][0][0])));

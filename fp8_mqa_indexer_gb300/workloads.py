@@ -456,16 +456,22 @@ class PagedMxCase:
     def max_blocks_per_seq(self):
         return self.block_table.shape[1]
 
+    def valid_counts(self) -> torch.Tensor:
+        ctx = self.context_lens.to(torch.int64).repeat_interleave(self.next_n)
+        t = torch.arange(self.next_n, dtype=torch.int64).repeat(self.B)
+        return (ctx - self.next_n + t + 1).clamp(min=0)
+
 
 def paged_mx_case(B: int, next_n: int, H: int, *, seed: int, context_lens, block_kv: int = 64,
                   num_blocks: Optional[int] = None, fp4: bool = False, sf_lo: int = 124,
-                  sf_hi: int = 130, name: str = "paged_mx") -> PagedMxCase:
+                  sf_hi: int = 130, max_blocks_per_seq: Optional[int] = None,
+                  name: str = "paged_mx") -> PagedMxCase:
     """Paged MX case: the given context lengths, pages handed out by a random
     permutation of the blocks, elements as ``mx_dense_case``."""
     g = _gen(seed)
     ctx = torch.as_tensor(context_lens, dtype=torch.int64)
     pages = (ctx.clamp(min=0) + block_kv - 1) // block_kv
-    max_blocks = max(1, int(pages.max()))
+    max_blocks = max_blocks_per_seq or max(1, int(pages.max()))
     if num_blocks is None:
         num_blocks = int(pages.sum()) + 3
     perm = torch.randperm(num_blocks, generator=g).to(torch.int32)
@@ -485,3 +491,20 @@ def paged_mx_case(B: int, next_n: int, H: int, *, seed: int, context_lens, block
     weights = torch.randn((B * next_n, H), generator=g)
     return PagedMxCase(name, q, q_sf, kv, kv_sf, weights, ctx.to(torch.int32), table, next_n,
                        max_blocks * block_kv, fp4)
+
+
+# The paged decode shape with MX keys (MXFP8, and MXFP4: the FP4 keys of the
+# "[PR #314] ..." page's paged test matrix): 64 sequences, next_n = 2, H = 64,
+# contexts uniform in [4096, 65536], 64-key pages over a 70000-block pool.
+PAGED_MX_CONFIGS = {
+    "paged_mx_b64_n2_h64_d128": dict(fp4=False, seed=1013),
+    "paged_mx4_b64_n2_h64_d128": dict(fp4=True, seed=1014),
+}
+
+
+def paged_mx_config(name: str) -> PagedMxCase:
+    kw = PAGED_MX_CONFIGS[name]
+    g = _gen(kw["seed"])
+    ctx = torch.randint(4096, 65536 + 1, (64,), generator=g, dtype=torch.int64)
+    return paged_mx_case(64, 2, 64, seed=kw["seed"] + 100, context_lens=ctx.tolist(), block_kv=64,
+                         num_blocks=70000, fp4=kw["fp4"], max_blocks_per_seq=65536 // 64, name=name)
