@@ -592,9 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            // paged MX: the 32 lanes of the producer that copies the key
-            // scale words arrive too (cp.async completion)
-            mbar_init(smem_u32(&sm.full[s]), (PAGED && MX) ? 33 : 1);
+            mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1 + n_epi);
         }
         for (int k = 0; k < 2; ++k) {
@@ -878,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int id = __shfl_sync(0xffffffffu, win0, pg - wbase);
                             if ((long long)pg * p.block_kv < keys && pg < p.max_blocks) {
                                 ids[k] = id;
-                                bytes += (uint32_t)(p.block_kv * (MX ? elem_bytes(D) : D + 4));
+                                bytes += (uint32_t)(p.block_kv * (elem_bytes(D) + 4));
                             }
                         }
                     }
@@ -894,25 +892,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // gather the pages of tile t through the block table
                     if constexpr (!MX)
                         page_ids();
-                    if constexpr (MX) {
-                        // the scale word of each key slot of the tile, copied by
-                        // cp.async straight into the transposed layout tcgen05.cp
-                        // reads (row lane, word j <- key 32 j + lane, whose page
-                        // is 32 j / block_kv); slots past the context copy word
-                        // 0 (their keys are masked); each lane's arrival on the
-                        // stage barrier waits for its copies
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int kk = 32 * j + lane;
-                            const int pi = (32 * j) / p.block_kv;
-                            const int id = pi == 0 ? ids[0] : pi == 1 ? ids[1] : pi == 2 ? ids[2] : ids[3];
-                            const bool ok =
-                                id >= 0 && id < p.num_blocks && (long long)t * kBlockKV + kk < keys;
-                            cp_async_4(smem_u32(&sm.sfa[stage][lane][j]),
-                                       p.kv_sf + (ok ? (long long)id * p.block_kv + (kk % p.block_kv) : 0));
-                        }
-                        cp_async_mbar_arrive_noinc(smem_u32(&sm.full[stage]));
-                    }
                     if (lane == 0) {
                         sm.info[stage] = info;
                         const uint32_t bar = smem_u32(&sm.full[stage]);
@@ -922,9 +901,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (k < ppt && ids[k] >= 0) {
                                 tma_load_2d(smem_u32(sm.kv[stage]) + k * p.block_kv * D, &tm_kv, bar, 0,
                                             ids[k] * p.block_kv);
-                                if constexpr (!MX)
-                                    tma_load_2d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale,
-                                                bar, ids[k] * p.block_kv, 0);
+                                // the slots' fp32 scales, or (MX) their scale words
+                                tma_load_2d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale, bar,
+                                            ids[k] * p.block_kv, 0);
                             }
                         }
                     }
@@ -998,25 +977,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================================================= MMA issuer
         regs_dec<kRegsCtl>();
-        if (lane == 0) {
+        // Paged MX: the whole warp runs the loop, to put each tile's scale
+        // words (copied by TMA in key order) into the transposed rows
+        // tcgen05.cp reads; otherwise lane 0 alone.
+        constexpr bool kWarpMma = PAGED && MX;
+        auto wait = [&](uint32_t bar, uint32_t parity, unsigned sleep) -> bool {
+            return kWarpMma ? warp_wait(bar, parity, wctx, sleep) : wait_bounded(bar, parity, wctx, sleep);
+        };
+        if (kWarpMma || lane == 0) {
             const uint32_t idesc = idesc_e4m3_f32(kBlockKV, (uint32_t)N);
             const uint64_t desc_kv0 = smem_desc(smem_u32(sm.kv[0]), D);
             const uint64_t desc_q0 = smem_desc(smem_u32(sm.q[0]), D);
             int k_block = -1;
             for (int u = 0; u < n_units; ++u) {
                 const int stage = u % S;
-                if (!wait_bounded(smem_u32(&sm.full[stage]), (u / S) & 1, wctx, kMmaSleepNs))
+                if (!wait(smem_u32(&sm.full[stage]), (u / S) & 1, kMmaSleepNs))
                     break;
                 const UnitInfo info = sm.info[stage];
                 if (info.flags & kFirstOfBlock) {
                     ++k_block;
-                    if (!wait_bounded(smem_u32(&sm.q_full[info.qbuf]), (k_block >> 1) & 1, wctx))
+                    if (!wait(smem_u32(&sm.q_full[info.qbuf]), (k_block >> 1) & 1, 0))
                         break;
                 }
                 const int buf = u & 1;
-                if (!wait_bounded(smem_u32(&sm.acc_empty[buf]), ((u >> 1) & 1) ^ 1, wctx,
-                                  kMmaSleepNs))
+                if (!wait(smem_u32(&sm.acc_empty[buf]), ((u >> 1) & 1) ^ 1, kMmaSleepNs))
                     break;
+                if constexpr (kWarpMma) {
+                    // row lane, word j <- the scale word of key 32 j + lane
+                    const uint32_t* lin = reinterpret_cast<const uint32_t*>(sm.scale[stage]);
+                    *reinterpret_cast<uint4*>(&sm.sfa[stage][lane][0]) =
+                        make_uint4(lin[lane], lin[32 + lane], lin[64 + lane], lin[96 + lane]);
+                    fence_proxy_async_smem();   // read by tcgen05.cp (async proxy)
+                    __syncwarp();
+                    if (lane != 0)
+                        continue;
+                }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kMaxN);
                 // descriptors advance by address / 16: one stage, one query
@@ -1027,8 +1022,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // scale factors into TMEM (in issue order before the MMAs
                     // that read them): the key tile's into the slot of this
                     // unit's parity, the query block's at its first unit
-                    if constexpr (PAGED)
-                        fence_proxy_async_smem();   // cp.async-written scale words -> tcgen05.cp
                     const uint32_t sfa_t = tmem_base + kMxSfaCol + (uint32_t)((u & 1) * 4);
                     const uint32_t sfb_t = tmem_base + kMxSfbCol + (uint32_t)(info.qbuf * 8);
                     tmem_cp_32x128b_x4(sfa_t, sf_desc(smem_u32(&sm.sfa[stage][0][0])));
@@ -1053,8 +1046,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // every MMA issued above has completed once this barrier flips;
             // waited for even after an abort, before TMEM is freed
-            mma_commit(smem_u32(&sm.mma_done));
-            wait_drain(smem_u32(&sm.mma_done), 0, wctx);
+            if (lane == 0) {
+                mma_commit(smem_u32(&sm.mma_done));
+                wait_drain(smem_u32(&sm.mma_done), 0, wctx);
+            }
         }
         __syncwarp();
     } else if (warp < kEpiWarp0) {
