@@ -229,22 +229,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// 4-byte asynchronous copy global -> shared (cp.async); its completion is
-// reported to an mbarrier by cp_async_mbar_arrive_noinc.
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src))
-                 : "memory");
-}
-
-// Arrive on `bar` once every cp.async this thread issued before has landed
-// (an arrival the barrier's count must include: noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // ------------------------------------------------------------------ tcgen05
 // TMEM allocation: executed by one whole warp.  The allocated base address is
 // written to shared memory at `slot`.
