@@ -57,6 +57,29 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+FP8_PEAK_FILE = os.path.join(ROOT, "profiles", "fp8_peak.json")
+
+
+def committed_fp8_peak():
+    """The FP8 GEMM peak a default benchmark run measured on this machine's GB300
+    (profiles/fp8_peak.json), for lines run without their own measurement."""
+    if not os.path.exists(FP8_PEAK_FILE):
+        return None
+    with open(FP8_PEAK_FILE) as f:
+        return json.load(f)
+
+
+def fp8_roofline_peak(fp8, nominal_peak, peaks_src):
+    """(peak, source): the live FP8 measurement, else the committed one, else
+    the bf16 burst x 2."""
+    if fp8:
+        return fp8["burst_tflops"], "measured fp8 (cuBLAS e4m3 GEMM burst on this GPU)"
+    rec = committed_fp8_peak()
+    if rec:
+        return rec["burst_tflops"], "measured fp8 (cuBLAS e4m3 GEMM burst, profiles/fp8_peak.json)"
+    return nominal_peak, f"{peaks_src} bf16 burst x {FP8_PER_BF16} (nominal fp8:bf16)"
+
+
 def recorded_traffic(workload: str, sources=KERNEL_SOURCES):
     """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged."""
     if not os.path.exists(TRAFFIC_FILE):
@@ -340,7 +363,7 @@ def bench_mx(args, mqa, torch, dev, stream):
     peaks, peaks_src = load_peaks()
     nominal_peak = peaks["bf16_tflops"] * FP8_PER_BF16
     fp8 = None if args.no_fp8_peak else measure_fp8_peak(torch, dev)
-    peak = fp8["burst_tflops"] if fp8 else nominal_peak
+    peak, peak_source = fp8_roofline_peak(fp8, nominal_peak, peaks_src)
     published = MX_PUBLISHED_US.get(args.workload)
     pub_tflops = flops / (published * 1e-6) / 1e12 if published else None
     if graph and pub_tflops:
@@ -362,8 +385,7 @@ def bench_mx(args, mqa, torch, dev, stream):
         "graph_timing": graph,
         "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / peak, "traffic": recorded_traffic(args.workload),
-                     "peak_source": ("measured fp8 (cuBLAS e4m3 GEMM burst on this GPU)" if fp8 else
-                                     f"{peaks_src} bf16 burst x {FP8_PER_BF16} (nominal fp8:bf16)"),
+                     "peak_source": peak_source,
                      "peak_bf16x2": nominal_peak, "frac_bf16x2": value / nominal_peak},
         "fp8_peak": fp8,
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -967,7 +989,7 @@ def main():
     peaks, peaks_src = load_peaks()
     nominal_peak = peaks["bf16_tflops"] * FP8_PER_BF16
     fp8 = None if args.no_fp8_peak else measure_fp8_peak(torch, dev)
-    peak = fp8["burst_tflops"] if fp8 else nominal_peak
+    peak, peak_source = fp8_roofline_peak(fp8, nominal_peak, peaks_src)
     achieved = flops / (ms_per_step * 1e-3) / 1e12
     traffic = recorded_traffic(args.workload)
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -989,8 +1011,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes": case_bytes(case),
-                     "peak_source": ("measured fp8 (cuBLAS e4m3 GEMM burst on this GPU)" if fp8 else
-                                     f"{peaks_src} bf16 burst x {FP8_PER_BF16} (nominal fp8:bf16)"),
+                     "peak_source": peak_source,
                      "peak_bf16x2": nominal_peak, "frac_bf16x2": achieved / nominal_peak,
                      "peak_at_kernel_clock": at_clock,
                      "frac_at_kernel_clock": achieved / at_clock if at_clock else None,
