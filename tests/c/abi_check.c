@@ -54,6 +54,30 @@ int main(void)
     expect("topk k=0", mqa_topk_indices(f, i, i, i, 4, 256, 256, 0, 0, NULL), MQA_ERR_INVALID_ARG);
     expect("paged topk width", paged_mqa_topk_indices(f, i, i, 2, 2, 1024, 1000, 16, NULL),
            MQA_ERR_INVALID_ARG);
+    {
+        const uint32_t *u = (const uint32_t *)buf;
+        expect("mx D=64", mqa_logits_mx(p, u, p, u, f, i, i, f, 4, 256, 64, 64, 256, MQA_CLEAN, NULL),
+               MQA_ERR_UNSUPPORTED);
+        expect("mxfp4 alignment", mqa_logits_mx(p, u, p, u, f, i, i, f, 4, 256, 64, 128, 256,
+                                                MQA_CLEAN | MQA_MXFP4, NULL),
+               MQA_ERR_INVALID_ARG);
+        expect("paged mx D=64", paged_mqa_logits_mx(p, u, p, u, f, i, i, 16, i, f, 2, 2, 64, 64, 64,
+                                                    40, 8, 1024, MQA_CLEAN, NULL),
+               MQA_ERR_UNSUPPORTED);
+        expect("paged mx null q_sf", paged_mqa_logits_mx(p, NULL, p, u, f, i, i, 16, i, f, 2, 2, 64,
+                                                         128, 64, 40, 8, 1024, MQA_CLEAN, NULL),
+               MQA_ERR_INVALID_ARG);
+        expect("scheduled null meta", mqa_logits_scheduled(p, p, f, f, i, i, NULL, 8, f, 4, 256, 64,
+                                                           128, 256, MQA_CLEAN, NULL),
+               MQA_ERR_INVALID_ARG);
+        expect("dense metadata H=16", mqa_logits_metadata(i, i, 4, 256, 16, 8, i, NULL),
+               MQA_ERR_UNSUPPORTED);
+        expect("dense unknown flag", mqa_logits(p, p, f, f, i, i, f, 4, 256, 64, 128, 256, 128u, NULL),
+               MQA_ERR_INVALID_ARG);
+        expect("bf16 weights misaligned", mqa_logits(p, p, f, (const char *)buf + 8, i, i, f, 4, 256,
+                                                     64, 128, 256, MQA_CLEAN | MQA_WEIGHTS_BF16, NULL),
+               MQA_ERR_INVALID_ARG);
+    }
     expect("wait limit", mqa_set_wait_limit(0), MQA_OK);
     if (failures == 0)
         printf("abi_check: ok\n");

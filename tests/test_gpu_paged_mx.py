@@ -108,3 +108,30 @@ def test_paged_mx_long_contexts_sampled(dev, fp4):
     assert_logits_match(out[rows].cpu().numpy(), ref, tol, what=f"paged mx long fp4={fp4}")
     again = gpu_call(case, upload(case, dev), dev)
     assert torch.equal(again.view(torch.int32), out.view(torch.int32))
+
+
+@pytest.mark.parametrize("bad", ["block_id", "context", "schedule"])
+def test_paged_mx_check_bounds_rejects(dev, bad):
+    """MQA_CHECK_BOUNDS: a block id past the pool, a context longer than the
+    table's width or a schedule entry out of order is reported as
+    MQA_ERR_BAD_INPUT before any logits kernel runs."""
+    case = wl.paged_mx_case(4, 2, 64, seed=860, context_lens=[100, 300, 520, 64], fp4=True)
+    d = upload(case, dev)
+    meta = mqa.paged_mqa_logits_metadata(d[5], next_n=2, block_kv=case.block_kv)
+    if bad == "block_id":
+        d[6][1, 0] = case.num_blocks
+    elif bad == "context":
+        d[5][2] = case.max_blocks_per_seq * case.block_kv + 1
+    else:
+        meta[1, 1] += 1
+    with pytest.raises(mqa.MQAError) as e:
+        mqa.paged_mqa_logits_mx(*d, meta, next_n=2, fp4=True, check_bounds=True)
+    assert e.value.status == 5
+    assert mqa.device_status() == 0
+    # and a valid call with the check on computes as without it
+    good = upload(case, dev)
+    meta = mqa.paged_mqa_logits_metadata(good[5], next_n=2, block_kv=case.block_kv)
+    a = mqa.paged_mqa_logits_mx(*good, meta, next_n=2, fp4=True, check_bounds=True)
+    b = mqa.paged_mqa_logits_mx(*good, meta, next_n=2, fp4=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
