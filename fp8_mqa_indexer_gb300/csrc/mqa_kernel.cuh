@@ -4,9 +4,12 @@
 // Computation with DeepGEMM", section "Core Architecture Components"): for
 // query token i and key j in its range,
 //     logits[i, j] = sum_h w[i,h] * ReLU(s[j] * <q[i,h,:], kv[j,:]>)
-// with E4M3 q/kv, fp32 per-key scale s and per-head weight w, fp32 output, and
-// -inf outside the range in clean mode ("[PR #435] Improve SM100 MX MQA logits
-// clean-output performance", section "Standalone performance reproducer").
+// with E4M3 q/kv, fp32 per-key scale s and per-head weight w (fp32 or bf16),
+// fp32 or bf16 output, and -inf outside the range in clean mode ("[PR #435]
+// Improve SM100 MX MQA logits clean-output performance", section "Standalone
+// performance reproducer").  MX instances take MXFP8 or MXFP4 q/kv with UE8M0
+// block scales in place of s (same page, sections "Performance" and
+// "Validation").
 //
 // Design (this library's own, for GB300):
 //  * Keys sit on the MMA M dimension: one 128-key tile of kv is the A operand
@@ -27,7 +30,13 @@
 //    paged_mqa_logits_metadata.
 //  * Warp roles (640 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 //    owner, warps 2-3 write -inf into the columns no tile covers (clean mode),
-//    warps 4-19 are four epilogue warp groups of 64 columns each.
+//    warps 4-19 are four epilogue warp groups of 64 columns each (groups
+//    without columns in a launch leave at once).  Paged calls: warps 0 and 2
+//    produce alternate units (page-id lookups and gathers), warp 3 alone fills.
+//  * MX: the block scales go into TMEM with tcgen05.cp beside the two
+//    accumulators (units of 192 columns) and the MMA is the block-scaled
+//    kind::mxf8f6f4; dense calls transpose the key scales in the producer,
+//    paged calls copy them by TMA with the pages and the MMA warp transposes.
 //  * Pipelines: a ring of key tiles (+ their scales and a small work record),
 //    two query-block buffers (+ weights and per-token ranges) and two TMEM
 //    accumulators of 256 columns; every hand-off is an mbarrier, every wait is
