@@ -22,6 +22,7 @@ from typing import Optional
 __all__ = [
     "MQAError", "mqa_logits", "mqa_logits_metadata", "mqa_logits_mx", "paged_mqa_logits", "paged_mqa_logits_metadata", "get_num_sms",
     "paged_mqa_logits_noalloc", "paged_mqa_logits_mx", "mqa_topk_indices", "paged_mqa_topk_indices",
+    "mqa_logits_topk", "mqa_logits_topk_workspace_size",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
     "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS", "MQA_OUT_BF16",
 ]
@@ -79,6 +80,8 @@ def load_library() -> ctypes.CDLL:
                                     I),
             "mqa_topk_indices": ([P, P, P, P, I, I, I64, I, U, P], I),
             "paged_mqa_topk_indices": ([P, P, P, I, I, I, I64, I, P], I),
+            "mqa_logits_topk_workspace_size": ([I, I], ctypes.c_size_t),
+            "mqa_logits_topk": ([P, P, P, P, P, P, P, P, ctypes.c_size_t, I, I, I, I, I, U, P], I),
             "mqa_get_num_sms": ([I], I),
             "mqa_device_status": ([P], I),
             "mqa_set_wait_limit": ([ULL], I),
@@ -493,6 +496,48 @@ def mqa_topk_indices(logits, k_start, k_end, topk: int, indices=None, *, S_kv: O
     with torch.cuda.device(logits.device):
         _check(load_library().mqa_topk_indices(_ptr(logits), _ptr(k_start), _ptr(k_end), _ptr(indices),
                                                S_q, S_kv, ldo, topk, flags, _stream_handle(stream)))
+    return indices
+
+
+def mqa_logits_topk_workspace_size(S_q: int, S_kv: int) -> int:
+    """Bytes of device workspace ``mqa_logits_topk`` needs for S_q rows of S_kv keys."""
+    return int(load_library().mqa_logits_topk_workspace_size(S_q, S_kv))
+
+
+def mqa_logits_topk(q, kv, kv_scale, weights, k_start, k_end, topk: int, indices=None, *,
+                    workspace=None, stream=None):
+    """Fused dense logits + top-k (C ABI ``mqa_logits_topk``): the result of
+    ``mqa_topk_indices`` over the logits ``mqa_logits`` would compute, without
+    writing those logits.  Inputs as ``mqa_logits``; returns int32 [S_q, topk].
+    ``workspace``: a CUDA uint8 tensor of at least
+    ``mqa_logits_topk_workspace_size(S_q, S_kv)`` bytes (allocated when None).
+    """
+    import torch
+    f8 = _fp8_types()
+    _dev(q, "q", f8)
+    _dev(kv, "kv", f8)
+    _dev(kv_scale, "kv_scale", (torch.float32,))
+    _dev(weights, "weights", (torch.float32, torch.bfloat16))
+    _dev(k_start, "k_start", (torch.int32,))
+    _dev(k_end, "k_end", (torch.int32,))
+    S_q, H, D = q.shape
+    S_kv = kv.shape[0]
+    if kv.dim() != 2 or kv.shape[1] != D or weights.shape != (S_q, H):
+        raise ValueError("shape mismatch between q, kv and weights")
+    if kv_scale.shape != (S_kv,) or k_start.shape != (S_q,) or k_end.shape != (S_q,):
+        raise ValueError("shape mismatch in kv_scale / k_start / k_end")
+    need = mqa_logits_topk_workspace_size(S_q, S_kv)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    elif not (isinstance(workspace, torch.Tensor) and workspace.is_cuda
+              and workspace.dtype == torch.uint8 and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    indices = _indices_out(indices, S_q, topk, q.device)
+    with torch.cuda.device(q.device):
+        _check(load_library().mqa_logits_topk(
+            _ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights), _ptr(k_start), _ptr(k_end),
+            _ptr(indices), _ptr(workspace), workspace.numel(), S_q, S_kv, H, D, topk,
+            _weights_flag(weights), _stream_handle(stream)))
     return indices
 
 

@@ -22,8 +22,8 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmqa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-UNITS = ["mqa_api.cu", "mqa_dense.cu", "mqa_dense_bf16.cu", "mqa_dense_mx.cu", "mqa_paged.cu",
-         "mqa_paged_bf16.cu", "mqa_paged_mx.cu", "mqa_topk.cu"]
+UNITS = ["mqa_api.cu", "mqa_dense.cu", "mqa_dense_bf16.cu", "mqa_dense_cand.cu", "mqa_dense_mx.cu",
+         "mqa_paged.cu", "mqa_paged_bf16.cu", "mqa_paged_mx.cu", "mqa_topk.cu"]
 
 
 def nvcc() -> str:

@@ -28,6 +28,8 @@ cudaError_t launch_paged_mx(int H, bool bf16, const LaunchArgs& a);
 cudaError_t launch_dense_mx(int H, bool bf16, const LaunchArgs& a);
 cudaError_t launch_dense_bf16(int H, int D, const LaunchArgs& a);
 cudaError_t launch_paged_bf16(int H, int D, const LaunchArgs& a);
+// candidate instances (CandOut) of the fused logits + top-k call
+cudaError_t launch_dense_cand(int H, int D, const LaunchArgs& a);
 
 template <int H, int D, bool PAGED, bool MX = false, typename OutT = float>
 cudaError_t launch_instance(const LaunchArgs& a)

@@ -428,12 +428,15 @@ namespace {
 // mqa_logits and mqa_logits_scheduled: `schedule_meta` (num_sms + 1 entries
 // from mqa_logits_metadata) or null for the in-kernel split.
 // MX calls pass q_sf and kv_sf (UE8M0 block scales) and no kv_scale; fp4:
-// MXFP4 elements (two E2M1 codes per byte, D / 2 bytes per row).
+// MXFP4 elements (two E2M1 codes per byte, D / 2 bytes per row).  cand_mask:
+// the candidate instances of the fused logits + top-k call (logits is then
+// the candidate values, cand_thr the per-row threshold keys or null).
 mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, const void* weights,
                       const int32_t* k_start, const int32_t* k_end, const int32_t* schedule_meta,
                       int sched_sms, void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                       unsigned flags, cudaStream_t stream, const uint32_t* q_sf = nullptr,
-                      const uint32_t* kv_sf = nullptr, bool fp4 = false)
+                      const uint32_t* kv_sf = nullptr, bool fp4 = false,
+                      unsigned* cand_mask = nullptr, const unsigned* cand_thr = nullptr)
 {
     const bool mx = q_sf != nullptr || kv_sf != nullptr;
     const bool compressed = (flags & MQA_COMPRESSED) != 0;
@@ -574,6 +577,8 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     p.kv_sf = kv_sf;
     p.mx_fmt = fp4 ? kFmtE2M1 : kFmtE4M3;
     p.w_bf16 = wbf16 ? 1 : 0;
+    p.cand_mask = cand_mask;
+    p.cand_thr = cand_thr;
     p.width = S_kv;
     p.width_i = S_kv;
     p.tok = tok;
@@ -585,7 +590,9 @@ mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, cons
     p.status = st;
     a.grid = num_sms;
     a.stream = stream;
-    cudaError_t e = mx ? launch_dense_mx(H, bf16, a) : launch_dense(H, D, bf16, a);
+    cudaError_t e = mx          ? launch_dense_mx(H, bf16, a)
+                    : cand_mask ? launch_dense_cand(H, D, a)
+                                : launch_dense(H, D, bf16, a);
     if (e == cudaErrorNotSupported)
         return fail(MQA_ERR_UNSUPPORTED, "no dense kernel for H=%d D=%d", H, D);
     if (e != cudaSuccess)
@@ -998,6 +1005,120 @@ mqa_status paged_mqa_topk_indices(const float* logits, const int32_t* context_le
     p.topk = topk;
     p.indices = indices;
     return launch_topk_checked(p, (cudaStream_t)stream);
+}
+
+
+// ------------------------------------------------ fused logits + top-k
+namespace {
+struct CandLayout {
+    long long ldo;   // candidate row stride (floats), a multiple of 32
+    size_t vals, mask, ranges, thr, total;   // byte offsets into the workspace
+};
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+CandLayout cand_layout(int S_q, int S_kv)
+{
+    CandLayout l;
+    l.ldo = ((long long)(S_kv > 0 ? S_kv : 1) + 31) & ~31ll;
+    const size_t rows = (size_t)(S_q > 0 ? S_q : 0);
+    l.vals = 0;
+    l.mask = round256(rows * (size_t)l.ldo * sizeof(float));
+    l.ranges = l.mask + round256(rows * (size_t)(l.ldo / 32) * sizeof(unsigned));
+    l.thr = l.ranges + round256(4 * rows * sizeof(int));
+    l.total = l.thr + round256(rows * sizeof(unsigned));
+    return l;
+}
+}  // namespace
+
+size_t mqa_logits_topk_workspace_size(int S_q, int S_kv)
+{
+    if (S_q < 0 || S_kv < 0)
+        return 0;
+    return cand_layout(S_q, S_kv).total;
+}
+
+mqa_status mqa_logits_topk(const void* q, const void* kv, const float* kv_scale,
+                           const void* weights, const int32_t* k_start, const int32_t* k_end,
+                           int32_t* indices, void* workspace, size_t workspace_bytes, int S_q,
+                           int S_kv, int H, int D, int topk, unsigned flags, mqa_stream_t stream)
+{
+    if (flags & ~(unsigned)MQA_WEIGHTS_BF16)
+        return fail(MQA_ERR_INVALID_ARG, "unknown or unsupported flag bits 0x%x", flags);
+    if (S_q < 0 || S_kv < 0 || topk < 1)
+        return fail(MQA_ERR_INVALID_ARG, "need S_q >= 0, S_kv >= 0, topk >= 1");
+    if (D != 64 && D != 128)
+        return fail(MQA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", D);
+    if (H != 8 && H != 32 && H != 64)
+        return fail(MQA_ERR_UNSUPPORTED, "H must be 8, 32 or 64 (got %d)", H);
+    if ((long long)S_q * H >= INT_MAX || S_kv > INT_MAX - 256)
+        return fail(MQA_ERR_INVALID_ARG, "S_q * H or S_kv too large");
+    if (S_q == 0)
+        return MQA_OK;
+    if (!indices || !workspace || !k_start || !k_end || !q || !weights ||
+        (S_kv > 0 && (!kv || !kv_scale)))
+        return fail(MQA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(q, 16) || !aligned(weights, 16) ||
+        (S_kv > 0 && (!aligned(kv, 16) || !aligned(kv_scale, 16))))
+        return fail(MQA_ERR_INVALID_ARG, "q, kv, kv_scale and weights must be 16-byte aligned");
+    if (!aligned(indices, 4) || !aligned(workspace, 256) || !aligned(k_start, 4) ||
+        !aligned(k_end, 4))
+        return fail(MQA_ERR_INVALID_ARG,
+                    "indices, k_start, k_end must be 4-byte and workspace 256-byte aligned");
+    const CandLayout l = cand_layout(S_q, S_kv);
+    if (workspace_bytes < l.total)
+        return fail(MQA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    l.total);
+    if ((long long)S_q * l.ldo >= (1ll << 62) / 4)
+        return fail(MQA_ERR_INVALID_ARG, "S_q * S_kv too large");
+    int dev;
+    unsigned* st;
+    mqa_status s = device_state(&dev, &st);
+    if (s != MQA_OK)
+        return s;
+    char* ws = static_cast<char*>(workspace);
+    CandTopkParams cp;
+    memset(&cp, 0, sizeof(cp));
+    cp.k_start = k_start;
+    cp.k_end = k_end;
+    cp.rows = S_q;
+    cp.n_cols = S_kv;
+    cp.topk = topk;
+    cp.ldo = l.ldo;
+    cp.vals = reinterpret_cast<const float*>(ws + l.vals);
+    cp.mask = reinterpret_cast<const unsigned*>(ws + l.mask);
+    int* ranges = reinterpret_cast<int*>(ws + l.ranges);
+    cp.pre_lo = ranges;
+    cp.pre_hi = ranges + S_q;
+    cp.rem_lo = ranges + 2 * (size_t)S_q;
+    cp.rem_hi = ranges + 3 * (size_t)S_q;
+    cp.thr = reinterpret_cast<unsigned*>(ws + l.thr);
+    cp.indices = indices;
+    cudaStream_t strm = (cudaStream_t)stream;
+    float* vals = reinterpret_cast<float*>(ws + l.vals);
+    unsigned* mask = reinterpret_cast<unsigned*>(ws + l.mask);
+    const int grid = kTopkCtasPerSm * g_num_sms[dev];
+    const int sel_grid = S_q < grid ? S_q : grid;
+    cudaError_t e = launch_cand_split(cp, strm);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "split kernel launch");
+    // prefix: every logit is a candidate
+    s = dense_call(q, kv, kv_scale, weights, cp.pre_lo, cp.pre_hi, nullptr, 0, vals, S_q, S_kv,
+                   H, D, l.ldo, flags, strm, nullptr, nullptr, false, mask, nullptr);
+    if (s != MQA_OK)
+        return s;
+    if (S_kv > 0) {
+        if ((e = launch_cand_threshold(cp, sel_grid, strm)) != cudaSuccess)
+            return cuda_fail(e, "threshold kernel launch");
+        // remainder: the logits at or above the prefix's topk-th largest
+        s = dense_call(q, kv, kv_scale, weights, cp.rem_lo, cp.rem_hi, nullptr, 0, vals, S_q,
+                       S_kv, H, D, l.ldo, flags, strm, nullptr, nullptr, false, mask, cp.thr);
+        if (s != MQA_OK)
+            return s;
+    }
+    if ((e = launch_cand_select(cp, sel_grid, strm)) != cudaSuccess)
+        return cuda_fail(e, "select kernel launch");
+    return MQA_OK;
 }
 
 }  // extern "C"

@@ -37,6 +37,11 @@
 //    accumulators (units of 192 columns) and the MMA is the block-scaled
 //    kind::mxf8f6f4; dense calls transpose the key scales in the producer,
 //    paged calls copy them by TMA with the pages and the MMA warp transposes.
+//  * Candidate instances (output type CandOut) serve the fused logits + top-k
+//    call: a logit of a row's range is kept only when its order key is at or
+//    above the row's threshold, and the kept logits of each 32-key line are
+//    written packed to the front of that line with a 32-bit mask of their
+//    keys; nothing else is written (no -inf fill).
 //  * Pipelines: a ring of key tiles (+ their scales and a small work record),
 //    two query-block buffers (+ weights and per-token ranges) and two TMEM
 //    accumulators of 256 columns; every hand-off is an mbarrier, every wait is
@@ -46,6 +51,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -88,11 +94,15 @@ struct __align__(16) TokRow {
     int slo, shi;    // keys stored
     int vlo, vhi;    // keys with a value
     long long off;   // offset of key 0 of the row in the logits
-    long long pad;
+    long long pad;   // candidate instances: the row's threshold key (low 32 bits)
 };
 
+// Output type of the candidate instances: per 32-key line, the kept fp32
+// logits packed to the front of the line and a mask of their keys.
+struct CandOut {};
+
 struct Params {
-    void* logits;            // float, or __nv_bfloat16 (bf16 instances)
+    void* logits;            // float, or __nv_bfloat16 (bf16 instances); candidates: float
     long long ldo;
     unsigned flags;
     // dense
@@ -124,6 +134,11 @@ struct Params {
     const uint32_t* kv_sf;   // [S_kv]
     uint32_t mx_fmt;         // element format of q and kv: kFmtE4M3 or kFmtE2M1
     int w_bf16;              // weights are bf16 (else fp32)
+    // candidate instances: row r, line L (keys [32 L, 32 L + 32)) has its mask
+    // at cand_mask[r * ldo / 32 + L]; a logit is kept when its order key is
+    // >= cand_thr[r] (all of them when cand_thr is null)
+    unsigned* cand_mask;
+    const unsigned* cand_thr;
     long long wait_limit;
     unsigned* status;
 };
@@ -246,6 +261,15 @@ __device__ __forceinline__ long long block_units(const Params& p, bool paged, in
     return thi - tlo;
 }
 
+// Unsigned key whose order is the IEEE-754 totalOrder of v (negative values
+// have every bit flipped, non-negative ones only the sign bit): the order in
+// which the top-k selection ranks logits.
+__device__ __forceinline__ unsigned logit_order_key(float v)
+{
+    const unsigned u = __float_as_uint(v);
+    return u ^ ((unsigned)((int)u >> 31) | 0x80000000u);
+}
+
 // -------------------------------------------------------- -inf fill of rows
 // -inf of the output element type (fp32 0xff800000, bf16 0xff80).
 template <typename OutT> __device__ __forceinline__ OutT neg_inf();
@@ -321,6 +345,7 @@ struct Epilogue {
     using C = Cfg<D>;
     static constexpr int S = C::kStages;
     static constexpr int kTokW = kEpiCols / H;   // tokens in a warp's columns
+    static constexpr bool kCand = std::is_same<OutT, CandOut>::value;
     static_assert(kTokW <= kMaxTokW, "token rows do not fit the shared table");
 
     struct Unit {
@@ -376,6 +401,8 @@ struct Epilogue {
             t.pad = 0;
             if (a < ntok && r < p.rows) {
                 t.off = (long long)r * p.ldo;
+                if (kCand && p.cand_thr)
+                    t.pad = (long long)__ldg(p.cand_thr + r);
                 t.slo = t.vlo = rg.x;
                 t.shi = t.vhi = rg.y;
                 if (p.flags & kFlagCompressed) {   // column j - lo, below ldo
@@ -436,10 +463,23 @@ struct Epilogue {
     {
         // key index; the host keeps widths below 2^31 - 256 so this fits an int
         const int j = st.info.t * kBlockKV + row;
-        // one predicated store: the logit, -inf (clean) or nothing
-        if (j >= t.slo && j < t.shi)
-            static_cast<OutT*>(p.logits)[t.off + j] =
-                (j >= t.vlo && j < t.vhi) ? to_out<OutT>(v) : neg_inf<OutT>();
+        if constexpr (kCand) {
+            // the warp's 32 lanes are the 32 keys of one line (row = 32 quad + lane)
+            const bool take =
+                j >= t.vlo && j < t.vhi && logit_order_key(v) >= (unsigned)t.pad;
+            const unsigned m = __ballot_sync(0xffffffffu, take);
+            const int lane = row & 31;
+            const int l0 = j - lane;   // first key of the line
+            if (take)
+                static_cast<float*>(p.logits)[t.off + l0 + __popc(m & ((1u << lane) - 1u))] = v;
+            if (lane == 0 && l0 < t.vhi && l0 + 32 > t.vlo)
+                p.cand_mask[(t.off >> 5) + (l0 >> 5)] = m;
+        } else {
+            // one predicated store: the logit, -inf (clean) or nothing
+            if (j >= t.slo && j < t.shi)
+                static_cast<OutT*>(p.logits)[t.off + j] =
+                    (j >= t.vlo && j < t.vhi) ? to_out<OutT>(v) : neg_inf<OutT>();
+        }
     }
 
     // Columns [c0, c0 + P) of the warp's slice, already in x.
@@ -1064,7 +1104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < kEpiWarp0) {
         // ================================================= -inf fill
         regs_dec<kRegsCtl>();
-        if (p.flags & kFlagClean) {
+        if (!std::is_same<OutT, CandOut>::value && (p.flags & kFlagClean)) {
             // fill warps: 2 and 3 (dense); 3 alone (paged: warp 2 produces)
             constexpr int nfw = PAGED ? 1 : 2;
             const int fw = warp - (kEpiWarp0 - nfw);
@@ -1072,7 +1112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nrows = PAGED ? p.B * p.tok : p.rows;
             for (int rr = cta + fw * G; rr < nrows; rr += nfw * G) {
                 const int r = PAGED ? (rr / p.tok) * p.next_n + p.tok0 + rr % p.tok : rr;
-                OutT* row = static_cast<OutT*>(p.logits) + (long long)r * p.ldo;
+                // (candidate instances never fill: the host sets no clean flag)
+                using FillT = std::conditional_t<std::is_same<OutT, CandOut>::value, float, OutT>;
+                FillT* row = static_cast<FillT*>(p.logits) + (long long)r * p.ldo;
                 if (PAGED) {
                     const int c = max(__ldg(p.context_lens + r / p.next_n), 0);
                     const long long covered = min((long long)paged_tiles(c) * kBlockKV, p.width);

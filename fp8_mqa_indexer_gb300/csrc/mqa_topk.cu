@@ -413,14 +413,13 @@ __device__ __forceinline__ void write_selected(TopkSmem& sm, Walk&& each, unsign
     });
 }
 
-// Ordered compaction of the row's elements with key >= thr into the shared
+// Ordered compaction of the walk's elements with key >= thr into the shared
 // list (the first kCap of them, in key order); returns how many there are.
-template <bool HINT>
-__device__ __forceinline__ unsigned compact_row(TopkSmem& sm, const RowView& r,
-                                                unsigned long long pol, unsigned thr, int& buf)
+template <class Walk>
+__device__ __forceinline__ unsigned compact_walk(TopkSmem& sm, Walk&& each, unsigned thr, int& buf)
 {
     unsigned run = 0;
-    for_row<HINT>(r, pol, [&](const unsigned(&key)[kPer], unsigned okm, RowIdx idx) {
+    each([&](const unsigned(&key)[kPer], unsigned okm, auto idx) {
         unsigned fm = 0;
 #pragma unroll
         for (int e = 0; e < kPer; ++e)
@@ -459,6 +458,14 @@ __device__ __forceinline__ unsigned compact_row(TopkSmem& sm, const RowView& r,
     });
     __syncthreads();
     return run;
+}
+
+template <bool HINT>
+__device__ __forceinline__ unsigned compact_row(TopkSmem& sm, const RowView& r,
+                                                unsigned long long pol, unsigned thr, int& buf)
+{
+    return compact_walk(
+        sm, [&](auto&& f) { for_row<HINT>(r, pol, f); }, thr, buf);
 }
 
 // Element e (0..15) of v, by a four-level select on the bits of e (no local
@@ -733,6 +740,223 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
     }
 }
 
+// ------------------------------------------------ fused logits + top-k
+// The candidate form of a row: line L (keys [32 L, 32 L + 32)) holds, packed
+// at its front in key order, the logits of the keys whose bits are set in the
+// line's mask.  Keys whose order key is below thr are not taken.
+struct CandView {
+    const float* vals;      // the row's candidate values
+    const unsigned* mask;   // the row's line masks
+    long long c_lo, c_hi;   // the row's key range
+    unsigned thr;
+};
+
+// f(key[16], okmask, idx) over the candidate row, element 4 g + j of thread t
+// being key base + g * kTile + 4 t + j as in for_row (a run of four keys never
+// crosses a line).  Keys without a candidate are not ok.
+template <class F>
+__device__ __forceinline__ void for_cand_row(const CandView& r, F&& f)
+{
+    for (long long base = r.c_lo & ~31ll; base < r.c_hi; base += kStep) {
+        const long long c0 = base + 4 * threadIdx.x;
+        unsigned key[kPer], okm = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const long long c = c0 + g * kTile;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                key[4 * g + j] = 0u;
+            if (c + 4 > r.c_lo && c < r.c_hi) {
+                const unsigned m = __ldg(r.mask + (c >> 5));
+                const int pos = (int)(c & 31);
+                const float* line = r.vals + (c & ~31ll);
+                unsigned rank = __popc(m & ((1u << pos) - 1u));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if ((m >> (pos + j)) & 1u) {
+                        const unsigned kk = order_key(__ldg(line + rank));
+                        ++rank;
+                        key[4 * g + j] = kk;
+                        okm |= (unsigned)(c + j >= r.c_lo && c + j < r.c_hi && kk >= r.thr)
+                               << (4 * g + j);
+                    }
+                }
+            }
+        }
+        f(key, okm, RowIdx{(int)c0});
+    }
+}
+
+// Row i's key range, clamped to [0, n_cols] as the top-k kernel clamps it.
+__device__ __forceinline__ void cand_range(const CandTopkParams& p, int i, int& lo, int& hi)
+{
+    long long a = __ldg(p.k_start + i), b = __ldg(p.k_end + i);
+    a = a < 0 ? 0 : (a > p.n_cols ? p.n_cols : a);
+    b = b > p.n_cols ? p.n_cols : b;
+    b = b < a ? a : b;
+    lo = (int)a;
+    hi = (int)b;
+}
+
+// Prefix and remainder of each row.  The prefix holds at least
+// max(2 topk, sqrt(n topk)) keys: about the length that minimises the
+// candidates written (all of the prefix, plus about topk / prefix of the
+// remainder for logits in random order).
+__global__ void cand_split_kernel(CandTopkParams p)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.rows)
+        return;
+    int lo, hi;
+    cand_range(p, i, lo, hi);
+    const long long n = (long long)hi - lo, k = p.topk;
+    int pre_lo = lo, pre_hi = lo, rem_hi = lo;
+    if (n > k) {
+        long long len = (long long)ceil(sqrt((double)n * (double)k));
+        len = len < 2 * k ? 2 * k : len;
+        len = (len + 127) & ~127ll;
+        const long long s = ((long long)hi - len) & ~127ll;   // rounds toward -inf
+        pre_lo = s > lo ? (int)s : lo;
+        pre_hi = hi;
+        rem_hi = pre_lo;
+    }
+    p.pre_lo[i] = pre_lo;
+    p.pre_hi[i] = pre_hi;
+    p.rem_lo[i] = lo;
+    p.rem_hi[i] = rem_hi;
+    p.thr[i] = 0u;
+}
+
+// thr[i] = order key of the topk-th largest logit of row i's prefix, for rows
+// with a remainder (the prefix then holds more than topk keys, every one of
+// them written, so its candidates are its plain logits at their own columns).
+// Digits 1 to 3 of the radix select, each over the prefix.
+__global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_threshold_kernel(CandTopkParams p)
+{
+    extern __shared__ __align__(16) unsigned char topk_smem_raw[];
+    TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
+    int buf = 0;
+    const unsigned k = (unsigned)p.topk;
+    for (int i = blockIdx.x; i < p.rows; i += gridDim.x) {
+        const int lo = __ldg(p.rem_lo + i), s = __ldg(p.rem_hi + i);
+        if (s <= lo)
+            continue;   // the same for every thread of the block
+        __syncthreads();   // the previous row's shared state is no longer read
+        RowView r;
+        r.ptr = p.vals + (long long)i * p.ldo;
+        r.c_lo = s;
+        r.c_hi = __ldg(p.pre_hi + i);
+        r.key_of_col0 = 0;
+        r.c_start = r.c_lo - (long long)((reinterpret_cast<unsigned long long>(r.ptr + r.c_lo) >> 2) & 3);
+        auto each = [&](auto&& f) { for_row<false>(r, 0ull, f); };
+        clear_hist<kBins12>(sm);
+        each([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                if ((okm >> e) & 1u)
+                    atomicAdd(&sm.hist[key[e] >> 20], 1u);
+        });
+        __syncthreads();
+        unsigned b1, above1, n1;
+        select_bin<kBins12>(sm, k, buf, b1, above1, n1);
+        clear_hist<kBins12>(sm);
+        each([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                if (((okm >> e) & 1u) && (key[e] >> 20) == b1)
+                    atomicAdd(&sm.hist[(key[e] >> 8) & 0xfffu], 1u);
+        });
+        __syncthreads();
+        unsigned b2, above2, n2;
+        select_bin<kBins12>(sm, k - above1, buf, b2, above2, n2);
+        const unsigned prefix = (b1 << 12) | b2;
+        clear_hist<kBins8>(sm);
+        each([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                if (((okm >> e) & 1u) && (key[e] >> 8) == prefix)
+                    atomicAdd(&sm.hist[key[e] & 0xffu], 1u);
+        });
+        __syncthreads();
+        unsigned b3, above3, n3;
+        select_bin<kBins8>(sm, k - above1 - above2, buf, b3, above3, n3);
+        if (threadIdx.x == 0)
+            p.thr[i] = (prefix << 8) | b3;
+    }
+}
+
+// The topk largest candidates of each row, in ascending key order, -1 padded.
+// Every logit of the row with order key >= thr[i] is a candidate (the whole
+// prefix was written, and the remainder's logits at or above thr[i]), and at
+// least topk of them exist, so the selection over the candidates is the
+// selection over the row.
+__global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_select_kernel(CandTopkParams p)
+{
+    extern __shared__ __align__(16) unsigned char topk_smem_raw[];
+    TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
+    int buf = 0;
+    const unsigned k = (unsigned)p.topk;
+    for (int i = blockIdx.x; i < p.rows; i += gridDim.x) {
+        int lo, hi;
+        cand_range(p, i, lo, hi);
+        const unsigned n = (unsigned)(hi - lo);
+        int* out = p.indices + (long long)i * p.topk;
+        const unsigned taken = n < k ? n : k;
+        __syncthreads();   // the previous row's shared state is no longer read
+        if (n <= k) {
+            for (unsigned c = threadIdx.x; c < n; c += kNT)
+                out[c] = lo + (int)c;
+        } else {
+            CandView cv;
+            cv.vals = p.vals + (long long)i * p.ldo;
+            cv.mask = p.mask + (long long)i * (p.ldo >> 5);
+            cv.c_lo = lo;
+            cv.c_hi = hi;
+            cv.thr = __ldg(p.thr + i);
+            auto walk = [&](auto&& f) { for_cand_row(cv, f); };
+            clear_hist<kBins12>(sm);
+            walk([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
+#pragma unroll
+                for (int e = 0; e < kPer; ++e)
+                    if ((okm >> e) & 1u)
+                        atomicAdd(&sm.hist[key[e] >> 20], 1u);
+            });
+            __syncthreads();
+            unsigned b1, above1, n1;
+            select_bin<kBins12>(sm, k, buf, b1, above1, n1);
+            if (above1 + n1 <= (unsigned)kCap) {
+                const unsigned mm = compact_walk(sm, walk, b1 << 20, buf);
+                finish_row(
+                    sm, [&](auto&& f) { for_cand(sm, mm < (unsigned)kCap ? mm : (unsigned)kCap, f); },
+                    b1, above1, k, out, buf);
+            } else {
+                finish_row(sm, walk, b1, above1, k, out, buf);
+            }
+        }
+        for (unsigned c = taken + threadIdx.x; c < k; c += kNT)
+            out[c] = -1;
+    }
+}
+
+// Sets the shared-memory limit of a selection kernel once per device.
+template <class K>
+cudaError_t set_topk_smem(K kern, std::atomic<unsigned long long>& attr_set)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (!(attr_set.load() & bit) || !bit) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(TopkSmem));
+        if (e != cudaSuccess)
+            return e;
+        attr_set.fetch_or(bit);
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t stream)
@@ -752,6 +976,32 @@ cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t stream)
         attr_set.fetch_or(bit);
     }
     topk_kernel<<<grid, kNT, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cand_split(const CandTopkParams& p, cudaStream_t stream)
+{
+    cand_split_kernel<<<(p.rows + 255) / 256, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cand_threshold(const CandTopkParams& p, int grid, cudaStream_t stream)
+{
+    static std::atomic<unsigned long long> attr_set{0};
+    cudaError_t e = set_topk_smem(cand_threshold_kernel, attr_set);
+    if (e != cudaSuccess)
+        return e;
+    cand_threshold_kernel<<<grid, kNT, sizeof(TopkSmem), stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cand_select(const CandTopkParams& p, int grid, cudaStream_t stream)
+{
+    static std::atomic<unsigned long long> attr_set{0};
+    cudaError_t e = set_topk_smem(cand_select_kernel, attr_set);
+    if (e != cudaSuccess)
+        return e;
+    cand_select_kernel<<<grid, kNT, sizeof(TopkSmem), stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -23,4 +23,33 @@ constexpr int kTopkCtasPerSm = 4;
 
 cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t stream);
 
+// The fused logits + top-k call (mqa_logits_topk).  Row i's range [lo, hi)
+// (k_start / k_end clamped to [0, n_cols]) is split at a 128-key boundary s
+// into a prefix [s, hi) of at least max(2 topk, sqrt(n topk)) keys and a
+// remainder [lo, s).  The logits kernel writes every logit of the prefix as a
+// candidate; the threshold kernel sets thr[i] to the order key of the prefix's
+// topk-th largest logit; the logits kernel then writes the remainder's
+// logits with keys >= thr[i]; the select kernel takes the topk largest of the
+// candidates.  Rows with at most topk keys have empty prefix and remainder.
+struct CandTopkParams {
+    const int* k_start;       // [rows] the call's key ranges
+    const int* k_end;
+    int rows;
+    int n_cols;               // keys (S_kv)
+    int topk;
+    long long ldo;            // candidate row stride in floats, a multiple of 32
+    const float* vals;        // [rows, ldo] candidates: line L packs its kept logits at 32 L
+    const unsigned* mask;     // [rows, ldo / 32] keys kept in each line
+    int* pre_lo;              // [rows] prefix ranges
+    int* pre_hi;
+    int* rem_lo;              // [rows] remainder ranges
+    int* rem_hi;
+    unsigned* thr;            // [rows] threshold keys
+    int* indices;             // [rows, topk] int32 output
+};
+
+cudaError_t launch_cand_split(const CandTopkParams& p, cudaStream_t stream);
+cudaError_t launch_cand_threshold(const CandTopkParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_cand_select(const CandTopkParams& p, int grid, cudaStream_t stream);
+
 }  // namespace mqa

@@ -37,6 +37,7 @@
 #ifndef MQA_H
 #define MQA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -343,6 +344,38 @@ MQA_API mqa_status mqa_topk_indices(const float *logits, const int32_t *k_start,
 MQA_API mqa_status paged_mqa_topk_indices(const float *logits, const int32_t *context_lens,
                                           int32_t *indices, int B, int next_n, int width,
                                           int64_t ldo, int topk, mqa_stream_t stream);
+
+/*
+ * Fused logits + top-k over dense KV: the `indices` of mqa_topk_indices for
+ * the logits mqa_logits would compute (non-clean, uncompressed), without
+ * writing those logits.  The top-k follows the MQA logits directly in the
+ * indexer: "FlashMLA", parameters of flash_mla_with_kvcache (indices of shape
+ * (batch, seq_len_q, topk), -1 for invalid entries), over the logits of "How
+ * to Implement MQA (Multi-Query Attention) Logits Computation with DeepGEMM",
+ * section "Core Architecture Components".
+ *
+ *   q, kv, kv_scale, weights, k_start, k_end, S_q, S_kv, H, D: as mqa_logits
+ *            (ranges are clamped to [0, S_kv] as mqa_topk_indices clamps them)
+ *   indices  [S_q, topk] int32 output, 4-byte aligned
+ *   topk >= 1
+ *   workspace  device memory of at least mqa_logits_topk_workspace_size(S_q,
+ *            S_kv) bytes, 256-byte aligned, owned by the caller; its contents
+ *            on entry do not matter and on return are unspecified.  It holds
+ *            one fp32 slot per logit, but only the candidates are written:
+ *            for each row the logits of a tail of its range (max(2 topk,
+ *            sqrt(len topk)) keys, at a 128-key boundary) and those of the
+ *            rest at or above the topk-th largest logit of that tail.
+ *   flags: MQA_WEIGHTS_BF16 or 0 (others are rejected).
+ * The result equals mqa_topk_indices applied to the mqa_logits output for the
+ * same inputs, bit for bit (both compute each logit with the same
+ * arithmetic).  Five kernels on `stream`; no host synchronisation.
+ */
+MQA_API size_t mqa_logits_topk_workspace_size(int S_q, int S_kv);
+MQA_API mqa_status mqa_logits_topk(const void *q, const void *kv, const float *kv_scale,
+                                   const void *weights, const int32_t *k_start,
+                                   const int32_t *k_end, int32_t *indices, void *workspace,
+                                   size_t workspace_bytes, int S_q, int S_kv, int H, int D,
+                                   int topk, unsigned flags, mqa_stream_t stream);
 
 /* Number of SMs of `device` (cached), or -1 on error. */
 MQA_API int mqa_get_num_sms(int device);

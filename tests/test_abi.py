@@ -270,3 +270,40 @@ def test_mx_rejects_invalid_arguments(lib, kw, status):
     a.update(kw)
     assert lib.mqa_logits_mx(a["q"], a["q_sf"], a["kv"], a["kv_sf"], F, F, F, F, 4, 256, a["H"],
                              a["D"], a["ldo"], a["flags"], None) == status
+
+
+def call_fused(lib, **kw):
+    a = dict(q=F, kv=F, kv_scale=F, weights=F, k_start=F, k_end=F, indices=F, ws=256, ws_bytes=1 << 40,
+             S_q=4, S_kv=256, H=64, D=128, topk=16, flags=0)
+    a.update(kw)
+    return lib.mqa_logits_topk(a["q"], a["kv"], a["kv_scale"], a["weights"], a["k_start"], a["k_end"],
+                               a["indices"], a["ws"], a["ws_bytes"], a["S_q"], a["S_kv"], a["H"],
+                               a["D"], a["topk"], a["flags"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(topk=0), 1), (dict(S_q=-1), 1), (dict(S_kv=-1), 1), (dict(D=96), 2), (dict(H=16), 2),
+    (dict(flags=1), 1), (dict(flags=2), 1), (dict(flags=4), 1), (dict(flags=16), 1),
+    (dict(q=None), 1), (dict(indices=None), 1), (dict(ws=None), 1), (dict(k_end=None), 1),
+    (dict(ws=F), 1), (dict(ws=256 + 64), 1), (dict(indices=F + 2), 1), (dict(q=F + 8), 1),
+    (dict(ws_bytes=1000), 1),
+])
+def test_fused_topk_rejects_invalid_arguments(lib, kw, status):
+    assert call_fused(lib, **kw) == status
+    assert lib.mqa_last_error_message().decode()
+
+
+def test_fused_topk_zero_rows_is_a_no_op(lib):
+    assert call_fused(lib, S_q=0, q=None, indices=None, ws=None) == 0
+
+
+def test_fused_topk_workspace_size(lib):
+    # one fp32 slot per key (rows padded to 32 keys), one mask word per 32
+    # keys, four range words and a threshold per row, each part 256-aligned
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for S_q, S_kv in ((1, 1), (4, 256), (2048, 32768), (17, 3001), (3, 0)):
+        ldo = max((max(S_kv, 1) + 31) // 32 * 32, 32)
+        want = r256(S_q * ldo * 4) + r256(S_q * ldo // 32 * 4) + r256(16 * S_q) + r256(4 * S_q)
+        assert mqa.mqa_logits_topk_workspace_size(S_q, S_kv) == want
+    assert lib.mqa_logits_topk_workspace_size(-1, 5) == 0
