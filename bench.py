@@ -266,6 +266,8 @@ def make_case(workload: str):
     from fp8_mqa_indexer_gb300 import workloads as wl
     if workload in wl.TOPK_CONFIGS:
         return wl.topk_config(workload)
+    if workload in wl.FUSED_CONFIGS:
+        return wl.fused_config(workload)[0]
     if workload in wl.PAGED_CONFIGS:
         return wl.paged_config(workload)
     if workload in wl.PAGED_MX_CONFIGS:
@@ -517,6 +519,147 @@ def bench_topk(args, mqa, torch, dev, stream):
     return 0
 
 
+def is_fused(workload: str) -> bool:
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    return workload in wl.FUSED_CONFIGS
+
+
+def fused_oracle_sample(case, topk: int, budget_s: float):
+    """Time the oracle's logits and top-k, row by row, on evenly spread rows."""
+    import oracle
+    import numpy as np
+    oracle.build()
+    cores = max(1, len(os.sched_getaffinity(0)))
+    order = list(range(0, case.S_q, max(1, case.S_q // 256)))
+    order += [r for r in range(case.S_q) if r not in set(order)]
+
+    def one(r):
+        L = oracle.mqa_logits(case.q, case.kv, case.kv_scale, case.weights, case.k_start,
+                              case.k_end, clean=False, rows=(r, r + 1))
+        return oracle.topk_indices(L, case.k_start[r:r + 1], case.k_end[r:r + 1], topk=topk,
+                                   n_cols=case.S_kv)
+
+    done, t0, k = 0, time.perf_counter(), 0
+    while k < len(order):
+        batch = order[k:k + cores]
+        k += len(batch)
+        oracle.run_rows_parallel(one, batch, threads=cores)
+        done += len(batch)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    wall = time.perf_counter() - t0
+    return {"rows_per_s": done / wall, "cores": cores, "rows": done, "wall_s": wall}
+
+
+def bench_fused(args, mqa, torch, dev, stream):
+    """Fused logits + top-k (mqa_logits_topk) on the dense workload's inputs,
+    with the unfused pipeline (mqa_logits, then mqa_topk_indices) timed beside
+    it.  The roofline is the logits contraction over the whole call."""
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    case, topk = wl.fused_config(args.workload)
+    R = case.S_q
+    valid = int(case.valid_counts().sum())
+    flops = valid * 2.0 * case.H * case.D
+    d = dict(q=case.q, kv=case.kv, s=case.kv_scale, w=case.weights, ks=case.k_start,
+             ke=case.k_end)
+    dd = {k: v.to(dev) for k, v in d.items()}
+    out = torch.empty((R, topk), dtype=torch.int32, device=dev)
+    ws = torch.empty(mqa.mqa_logits_topk_workspace_size(R, case.S_kv), dtype=torch.uint8,
+                     device=dev)
+    L = torch.empty((R, case.S_kv), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(x):
+        mqa.mqa_logits_topk(x["q"], x["kv"], x["s"], x["w"], x["ks"], x["ke"], topk, out,
+                            workspace=ws)
+
+    def unfused(x):
+        mqa.mqa_logits(x["q"], x["kv"], x["s"], x["w"], x["ks"], x["ke"], L, clean=False)
+        mqa.mqa_topk_indices(L, x["ks"], x["ke"], topk, out)
+
+    def timed(fn, n):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            fn(dd)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            flush.zero_()
+            pre_spin(torch)
+            a.record(stream)
+            fn(dd)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[0].strip() if vis else "0")
+    sampler.start()
+    time.sleep(0.3)
+    times_ms = timed(step, args.steps)
+    clocks = sampler.stop()
+    ms_per_step = sum(times_ms) / args.steps
+    unfused_ms = sorted(timed(unfused, max(5, args.steps // 2)))
+    unfused_med = unfused_ms[len(unfused_ms) // 2]
+
+    host = {k: (v.view(torch.uint8) if v.dtype == torch.float8_e4m3fn else v).pin_memory()
+            for k, v in d.items()}
+    host_out = torch.empty((R, topk), dtype=torch.int32, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+
+    def e2e_step():
+        x = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+        step(x)
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+
+    peaks, peaks_src = load_peaks()
+    fp8 = None if args.no_fp8_peak else measure_fp8_peak(torch, dev)
+    peak, peak_src = fp8_roofline_peak(fp8, peaks["bf16_tflops"] * 2.0, peaks_src)
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": "fused logits + top-k rows/s",
+        "value": R / (ms_per_step * 1e-3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 -> i32", "data": "synthetic",
+        "config": {"workload": args.workload, "S_q": R, "S_kv": case.S_kv, "H": case.H,
+                   "D": case.D, "topk": topk, "valid_logits": valid,
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "step": "mqa_logits_topk (split, candidate logits of each row's tail, "
+                           "threshold, candidate logits of the rest, selection)"},
+        **percentiles(times_ms),
+        "unfused_ms": unfused_med,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_flops": flops,
+                     "scope": "the whole call (five kernels), not one kernel",
+                     "peak_source": peak_src},
+        "e2e": {"value": R / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": host_out.numel() * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        info = fused_oracle_sample(case, topk, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": info["rows_per_s"], "unit": "rows/s", "cores": info["cores"],
+                                "kind": "oracle",
+                                "sample": f"{info['rows']} of {R} rows ({info['wall_s']:.1f} s of "
+                                          f"oracle time), throughput extrapolated"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def paged_oracle_sample(case, budget_s: float):
     """Time the oracle on whole sequences (both of their rows) for ~budget_s."""
     import oracle
@@ -735,6 +878,8 @@ def run_reference(args, rank, world):
         return 0
     if is_topk(args.workload):
         return run_reference_topk(args)
+    if is_fused(args.workload):
+        return run_reference_fused(args)
     case = make_case(args.workload)
     valid = int(case.valid_counts().sum())
     flops_full = valid * 2.0 * case.H * case.D
@@ -766,6 +911,33 @@ def run_reference(args, rank, world):
                          "sample": f"{info['rows']} of {case.B * case.next_n if paged else case.S_q} rows per step, "
                                    f"extrapolated to the full workload ({info['wall_s']:.1f} s)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_fused(args):
+    from fp8_mqa_indexer_gb300 import workloads as wl
+    case, topk = wl.fused_config(args.workload)
+    for _ in range(args.warmup):
+        fused_oracle_sample(case, topk, budget_s=0.3)
+    budget = args.ref_budget or max(1.0, min(6.0, 90.0 / max(1, args.steps)))
+    per_step, info = [], None
+    for _ in range(args.steps):
+        info = fused_oracle_sample(case, topk, budget_s=budget)
+        per_step.append(info["rows_per_s"])
+    value = statistics.median(per_step)
+    line = {
+        "impl": "reference", "metric": "fused logits + top-k rows/s", "value": value,
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": case.S_q / value * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (exact e4m3 decode) -> i32", "data": "synthetic",
+        "config": {"workload": args.workload, "S_q": case.S_q, "S_kv": case.S_kv, "H": case.H,
+                   "D": case.D, "topk": topk},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": info["cores"], "kind": "oracle",
+                         "sample": f"{info['rows']} of {case.S_q} rows per step, extrapolated to "
+                                   f"the full workload ({info['wall_s']:.1f} s)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -903,6 +1075,10 @@ def main():
     if pg:
         pg.barrier()
     mqa.load_library()
+    if is_fused(args.workload):
+        if world > 1:
+            raise SystemExit("the fused workloads are measured on one GPU")
+        return bench_fused(args, mqa, torch, dev, torch.cuda.current_stream())
     if is_topk(args.workload):
         if world > 1:
             raise SystemExit("the top-k workload is measured on one GPU")

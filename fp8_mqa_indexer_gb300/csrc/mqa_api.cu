@@ -430,13 +430,13 @@ namespace {
 // MX calls pass q_sf and kv_sf (UE8M0 block scales) and no kv_scale; fp4:
 // MXFP4 elements (two E2M1 codes per byte, D / 2 bytes per row).  cand_mask:
 // the candidate instances of the fused logits + top-k call (logits is then
-// the candidate values, cand_thr the per-row threshold keys or null).
+// the candidate values, cand_thr the per-row thresholds or null).
 mqa_status dense_call(const void* q, const void* kv, const float* kv_scale, const void* weights,
                       const int32_t* k_start, const int32_t* k_end, const int32_t* schedule_meta,
                       int sched_sms, void* logits, int S_q, int S_kv, int H, int D, int64_t ldo,
                       unsigned flags, cudaStream_t stream, const uint32_t* q_sf = nullptr,
                       const uint32_t* kv_sf = nullptr, bool fp4 = false,
-                      unsigned* cand_mask = nullptr, const unsigned* cand_thr = nullptr)
+                      unsigned* cand_mask = nullptr, const float* cand_thr = nullptr)
 {
     const bool mx = q_sf != nullptr || kv_sf != nullptr;
     const bool compressed = (flags & MQA_COMPRESSED) != 0;
@@ -1011,8 +1011,8 @@ mqa_status paged_mqa_topk_indices(const float* logits, const int32_t* context_le
 // ------------------------------------------------ fused logits + top-k
 namespace {
 struct CandLayout {
-    long long ldo;   // candidate row stride (floats), a multiple of 32
-    size_t vals, mask, ranges, thr, total;   // byte offsets into the workspace
+    long long ldo;   // candidate row stride (floats), a multiple of 128
+    size_t vals, mask, ranges, thr, thr_f, total;   // byte offsets into the workspace
 };
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1020,13 +1020,17 @@ size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 CandLayout cand_layout(int S_q, int S_kv)
 {
     CandLayout l;
-    l.ldo = ((long long)(S_kv > 0 ? S_kv : 1) + 31) & ~31ll;
+    // a whole 128-key tile of every row fits its stride, so the candidate
+    // kernel writes the mask of each line of a tile without a bounds test
+    l.ldo = ((long long)(S_kv > 0 ? S_kv : 1) + 127) & ~127ll;
     const size_t rows = (size_t)(S_q > 0 ? S_q : 0);
     l.vals = 0;
     l.mask = round256(rows * (size_t)l.ldo * sizeof(float));
-    l.ranges = l.mask + round256(rows * (size_t)(l.ldo / 32) * sizeof(unsigned));
+    // one scratch row of masks for the absent rows of a last query block
+    l.ranges = l.mask + round256((rows + 1) * (size_t)(l.ldo / 32) * sizeof(unsigned));
     l.thr = l.ranges + round256(4 * rows * sizeof(int));
-    l.total = l.thr + round256(rows * sizeof(unsigned));
+    l.thr_f = l.thr + round256(rows * sizeof(unsigned));
+    l.total = l.thr_f + round256(rows * sizeof(float));
     return l;
 }
 }  // namespace
@@ -1085,14 +1089,15 @@ mqa_status mqa_logits_topk(const void* q, const void* kv, const float* kv_scale,
     cp.n_cols = S_kv;
     cp.topk = topk;
     cp.ldo = l.ldo;
-    cp.vals = reinterpret_cast<const float*>(ws + l.vals);
-    cp.mask = reinterpret_cast<const unsigned*>(ws + l.mask);
+    cp.vals = reinterpret_cast<float*>(ws + l.vals);
+    cp.mask = reinterpret_cast<unsigned*>(ws + l.mask);
     int* ranges = reinterpret_cast<int*>(ws + l.ranges);
     cp.pre_lo = ranges;
     cp.pre_hi = ranges + S_q;
     cp.rem_lo = ranges + 2 * (size_t)S_q;
     cp.rem_hi = ranges + 3 * (size_t)S_q;
     cp.thr = reinterpret_cast<unsigned*>(ws + l.thr);
+    cp.thr_f = reinterpret_cast<float*>(ws + l.thr_f);
     cp.indices = indices;
     cudaStream_t strm = (cudaStream_t)stream;
     float* vals = reinterpret_cast<float*>(ws + l.vals);
@@ -1102,9 +1107,9 @@ mqa_status mqa_logits_topk(const void* q, const void* kv, const float* kv_scale,
     cudaError_t e = launch_cand_split(cp, strm);
     if (e != cudaSuccess)
         return cuda_fail(e, "split kernel launch");
-    // prefix: every logit is a candidate
+    // prefix: every logit, at its own column (the plain kernel, non-clean)
     s = dense_call(q, kv, kv_scale, weights, cp.pre_lo, cp.pre_hi, nullptr, 0, vals, S_q, S_kv,
-                   H, D, l.ldo, flags, strm, nullptr, nullptr, false, mask, nullptr);
+                   H, D, l.ldo, flags, strm);
     if (s != MQA_OK)
         return s;
     if (S_kv > 0) {
@@ -1112,7 +1117,7 @@ mqa_status mqa_logits_topk(const void* q, const void* kv, const float* kv_scale,
             return cuda_fail(e, "threshold kernel launch");
         // remainder: the logits at or above the prefix's topk-th largest
         s = dense_call(q, kv, kv_scale, weights, cp.rem_lo, cp.rem_hi, nullptr, 0, vals, S_q,
-                       S_kv, H, D, l.ldo, flags, strm, nullptr, nullptr, false, mask, cp.thr);
+                       S_kv, H, D, l.ldo, flags, strm, nullptr, nullptr, false, mask, cp.thr_f);
         if (s != MQA_OK)
             return s;
     }

@@ -38,10 +38,9 @@
 //    kind::mxf8f6f4; dense calls transpose the key scales in the producer,
 //    paged calls copy them by TMA with the pages and the MMA warp transposes.
 //  * Candidate instances (output type CandOut) serve the fused logits + top-k
-//    call: a logit of a row's range is kept only when its order key is at or
-//    above the row's threshold, and the kept logits of each 32-key line are
-//    written packed to the front of that line with a 32-bit mask of their
-//    keys; nothing else is written (no -inf fill).
+//    call: a logit of a row's range is written (at its own column) only when
+//    it is not below the row's threshold, and each 32-key line gets a 32-bit
+//    mask of the keys written; nothing else is written (no -inf fill).
 //  * Pipelines: a ring of key tiles (+ their scales and a small work record),
 //    two query-block buffers (+ weights and per-token ranges) and two TMEM
 //    accumulators of 256 columns; every hand-off is an mbarrier, every wait is
@@ -94,11 +93,11 @@ struct __align__(16) TokRow {
     int slo, shi;    // keys stored
     int vlo, vhi;    // keys with a value
     long long off;   // offset of key 0 of the row in the logits
-    long long pad;   // candidate instances: the row's threshold key (low 32 bits)
+    long long pad;   // candidate instances: the row's threshold (fp32 bits, low half)
 };
 
-// Output type of the candidate instances: per 32-key line, the kept fp32
-// logits packed to the front of the line and a mask of their keys.
+// Output type of the candidate instances: the kept fp32 logits at their own
+// columns and, per 32-key line, a mask of their keys.
 struct CandOut {};
 
 struct Params {
@@ -135,10 +134,12 @@ struct Params {
     uint32_t mx_fmt;         // element format of q and kv: kFmtE4M3 or kFmtE2M1
     int w_bf16;              // weights are bf16 (else fp32)
     // candidate instances: row r, line L (keys [32 L, 32 L + 32)) has its mask
-    // at cand_mask[r * ldo / 32 + L]; a logit is kept when its order key is
-    // >= cand_thr[r] (all of them when cand_thr is null)
+    // at cand_mask[r * ldo / 32 + L] (row `rows` is scratch for the absent
+    // rows of a last query block; ldo is a multiple of 128); a logit v of the
+    // row's range is kept unless v < cand_thr[r] (all of them when cand_thr is
+    // null)
     unsigned* cand_mask;
-    const unsigned* cand_thr;
+    const float* cand_thr;
     long long wait_limit;
     unsigned* status;
 };
@@ -259,15 +260,6 @@ __device__ __forceinline__ long long block_units(const Params& p, bool paged, in
     int tlo, thi;
     dense_block_tiles(p, b, tlo, thi);
     return thi - tlo;
-}
-
-// Unsigned key whose order is the IEEE-754 totalOrder of v (negative values
-// have every bit flipped, non-negative ones only the sign bit): the order in
-// which the top-k selection ranks logits.
-__device__ __forceinline__ unsigned logit_order_key(float v)
-{
-    const unsigned u = __float_as_uint(v);
-    return u ^ ((unsigned)((int)u >> 31) | 0x80000000u);
 }
 
 // -------------------------------------------------------- -inf fill of rows
@@ -397,12 +389,13 @@ struct Epilogue {
             const int r = info.b * p.blk_stride + p.tok0 + tok0 + a;
             const int2 rg = sm.range[info.qbuf][tok0 + a];   // within [0, width)
             t.slo = t.shi = t.vlo = t.vhi = 0;
-            t.off = 0;
+            t.off = kCand ? (long long)p.rows * p.ldo : 0;   // candidates: the scratch row
             t.pad = 0;
             if (a < ntok && r < p.rows) {
                 t.off = (long long)r * p.ldo;
-                if (kCand && p.cand_thr)
-                    t.pad = (long long)__ldg(p.cand_thr + r);
+                if (kCand)
+                    t.pad = (long long)__float_as_uint(p.cand_thr ? __ldg(p.cand_thr + r)
+                                                                  : __int_as_float(0xff800000));
                 t.slo = t.vlo = rg.x;
                 t.shi = t.vhi = rg.y;
                 if (p.flags & kFlagCompressed) {   // column j - lo, below ldo
@@ -464,15 +457,18 @@ struct Epilogue {
         // key index; the host keeps widths below 2^31 - 256 so this fits an int
         const int j = st.info.t * kBlockKV + row;
         if constexpr (kCand) {
-            // the warp's 32 lanes are the 32 keys of one line (row = 32 quad + lane)
+            // The warp's 32 lanes are the 32 keys of one line (row = 32 quad +
+            // lane): one ballot gives the line's mask.  "not below" keeps NaNs: a superset of the keys at or
+            // above the threshold's order key is all the selection needs.
             const bool take =
-                j >= t.vlo && j < t.vhi && logit_order_key(v) >= (unsigned)t.pad;
+                j >= t.vlo && j < t.vhi && !(v < __uint_as_float((unsigned)t.pad));
             const unsigned m = __ballot_sync(0xffffffffu, take);
-            const int lane = row & 31;
-            const int l0 = j - lane;   // first key of the line
+            const int l0 = j - (row & 31);   // first key of the line
             if (take)
-                static_cast<float*>(p.logits)[t.off + l0 + __popc(m & ((1u << lane) - 1u))] = v;
-            if (lane == 0 && l0 < t.vhi && l0 + 32 > t.vlo)
+                static_cast<float*>(p.logits)[t.off + j] = v;
+            // every line of the tile gets a mask (a row's masks are read only
+            // over the range this launch covers for it)
+            if ((row & 31) == 0)
                 p.cand_mask[(t.off >> 5) + (l0 >> 5)] = m;
         } else {
             // one predicated store: the logit, -inf (clean) or nothing

@@ -741,24 +741,36 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
 }
 
 // ------------------------------------------------ fused logits + top-k
-// The candidate form of a row: line L (keys [32 L, 32 L + 32)) holds, packed
-// at its front in key order, the logits of the keys whose bits are set in the
-// line's mask.  Keys whose order key is below thr are not taken.
+// The candidate form of a row with range [lo, hi) split at s: keys [s, hi)
+// (the prefix) have their logits at their own columns; in [lo, s) (the
+// remainder) only the keys whose bits are set in their line's mask (line L:
+// keys [32 L, 32 L + 32)) have their logits there, the other columns hold
+// garbage.
 struct CandView {
-    const float* vals;      // the row's candidate values
+    const float* vals;      // the row's values
     const unsigned* mask;   // the row's line masks
     long long c_lo, c_hi;   // the row's key range
-    unsigned thr;
+    long long s;            // first prefix key (a multiple of 128, or c_lo)
+    unsigned thr;           // prefix keys below thr are not taken
 };
 
 // f(key[16], okmask, idx) over the candidate row, element 4 g + j of thread t
 // being key base + g * kTile + 4 t + j as in for_row (a run of four keys never
-// crosses a line).  Keys without a candidate are not ok.
+// crosses a line; it crosses s only when s = c_lo, the row having no
+// remainder).  Remainder keys without a candidate and prefix keys below thr
+// are not ok; remainder mask bits are only ever set for keys of the row's
+// range.
 template <class F>
 __device__ __forceinline__ void for_cand_row(const CandView& r, F&& f)
 {
     for (long long base = r.c_lo & ~31ll; base < r.c_hi; base += kStep) {
         const long long c0 = base + 4 * threadIdx.x;
+        unsigned m[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {   // the step's remainder masks first
+            const long long c = c0 + g * kTile;
+            m[g] = (c + 4 > r.c_lo && c + 4 <= r.s) ? __ldg(r.mask + (c >> 5)) : 0u;
+        }
         unsigned key[kPer], okm = 0;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -766,20 +778,30 @@ __device__ __forceinline__ void for_cand_row(const CandView& r, F&& f)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 key[4 * g + j] = 0u;
-            if (c + 4 > r.c_lo && c < r.c_hi) {
-                const unsigned m = __ldg(r.mask + (c >> 5));
-                const int pos = (int)(c & 31);
-                const float* line = r.vals + (c & ~31ll);
-                unsigned rank = __popc(m & ((1u << pos) - 1u));
+            if (c + 4 > r.s) {   // prefix: plain logits
+                if (c >= r.s && c + 4 <= r.c_hi) {
+                    const float4 x = load4(r.vals + c);
+                    key[4 * g] = order_key(x.x), key[4 * g + 1] = order_key(x.y);
+                    key[4 * g + 2] = order_key(x.z), key[4 * g + 3] = order_key(x.w);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if ((m >> (pos + j)) & 1u) {
-                        const unsigned kk = order_key(__ldg(line + rank));
-                        ++rank;
-                        key[4 * g + j] = kk;
-                        okm |= (unsigned)(c + j >= r.c_lo && c + j < r.c_hi && kk >= r.thr)
-                               << (4 * g + j);
+                    for (int j = 0; j < 4; ++j)
+                        okm |= (unsigned)(key[4 * g + j] >= r.thr) << (4 * g + j);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (c + j >= r.s && c + j < r.c_hi) {
+                            key[4 * g + j] = order_key(__ldg(r.vals + c + j));
+                            okm |= (unsigned)(key[4 * g + j] >= r.thr) << (4 * g + j);
+                        }
                     }
+                }
+            } else {   // remainder: candidates at their own columns
+                const unsigned bits = (m[g] >> (int)(c & 31)) & 0xfu;
+                if (bits) {
+                    const float4 x = load4(r.vals + c);
+                    key[4 * g] = order_key(x.x), key[4 * g + 1] = order_key(x.y);
+                    key[4 * g + 2] = order_key(x.z), key[4 * g + 3] = order_key(x.w);
+                    okm |= bits << (4 * g);
                 }
             }
         }
@@ -825,12 +847,13 @@ __global__ void cand_split_kernel(CandTopkParams p)
     p.rem_lo[i] = lo;
     p.rem_hi[i] = rem_hi;
     p.thr[i] = 0u;
+    p.thr_f[i] = __int_as_float(0xff800000);   // -inf
 }
 
-// thr[i] = order key of the topk-th largest logit of row i's prefix, for rows
-// with a remainder (the prefix then holds more than topk keys, every one of
-// them written, so its candidates are its plain logits at their own columns).
-// Digits 1 to 3 of the radix select, each over the prefix.
+// thr[i] = order key T of the topk-th largest logit of row i's prefix and
+// thr_f[i] = that logit, for rows with a remainder (the prefix then holds more
+// than topk keys, every one of them written at its own column): digits 1 to 3
+// of the radix select, each over the prefix.
 __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_threshold_kernel(CandTopkParams p)
 {
     extern __shared__ __align__(16) unsigned char topk_smem_raw[];
@@ -880,16 +903,20 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_threshold_kernel(Can
         __syncthreads();
         unsigned b3, above3, n3;
         select_bin<kBins8>(sm, k - above1 - above2, buf, b3, above3, n3);
-        if (threadIdx.x == 0)
-            p.thr[i] = (prefix << 8) | b3;
+        if (threadIdx.x == 0) {
+            const unsigned T = (prefix << 8) | b3;
+            p.thr[i] = T;
+            // the logit whose order key is T (order_key inverted)
+            p.thr_f[i] = __uint_as_float((T & 0x80000000u) ? (T ^ 0x80000000u) : ~T);
+        }
     }
 }
 
 // The topk largest candidates of each row, in ascending key order, -1 padded.
-// Every logit of the row with order key >= thr[i] is a candidate (the whole
-// prefix was written, and the remainder's logits at or above thr[i]), and at
-// least topk of them exist, so the selection over the candidates is the
-// selection over the row.
+// The candidates hold every logit of the row with order key >= thr[i] (the
+// prefix's, and the remainder's written ones), at least topk of them, and no
+// larger logit is missing, so the selection over them is the selection over
+// the row.
 __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_select_kernel(CandTopkParams p)
 {
     extern __shared__ __align__(16) unsigned char topk_smem_raw[];
@@ -912,6 +939,7 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_select_kernel(CandTo
             cv.mask = p.mask + (long long)i * (p.ldo >> 5);
             cv.c_lo = lo;
             cv.c_hi = hi;
+            cv.s = __ldg(p.rem_hi + i);
             cv.thr = __ldg(p.thr + i);
             auto walk = [&](auto&& f) { for_cand_row(cv, f); };
             clear_hist<kBins12>(sm);

@@ -26,25 +26,30 @@ cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t stream);
 // The fused logits + top-k call (mqa_logits_topk).  Row i's range [lo, hi)
 // (k_start / k_end clamped to [0, n_cols]) is split at a 128-key boundary s
 // into a prefix [s, hi) of at least max(2 topk, sqrt(n topk)) keys and a
-// remainder [lo, s).  The logits kernel writes every logit of the prefix as a
-// candidate; the threshold kernel sets thr[i] to the order key of the prefix's
-// topk-th largest logit; the logits kernel then writes the remainder's
-// logits with keys >= thr[i]; the select kernel takes the topk largest of the
-// candidates.  Rows with at most topk keys have empty prefix and remainder.
+// remainder [lo, s).  The plain logits kernel writes every logit of the
+// prefix at its own column; the threshold kernel sets thr[i] to the order key
+// of the prefix's topk-th largest logit (thr_f[i]: that logit); the candidate
+// logits kernel then writes the remainder's logits not below thr_f[i], at
+// their own columns, with a mask of their keys per 32-key line; the select
+// kernel takes the topk
+// largest of the prefix's logits and the remainder's candidates.  Rows with at
+// most topk keys have empty prefix and remainder.
 struct CandTopkParams {
     const int* k_start;       // [rows] the call's key ranges
     const int* k_end;
     int rows;
     int n_cols;               // keys (S_kv)
     int topk;
-    long long ldo;            // candidate row stride in floats, a multiple of 32
-    const float* vals;        // [rows, ldo] candidates: line L packs its kept logits at 32 L
-    const unsigned* mask;     // [rows, ldo / 32] keys kept in each line
+    long long ldo;            // candidate row stride in floats, a multiple of 128
+    float* vals;              // [rows, ldo] logits at their own columns (the prefix's, and
+                              // the remainder's that its masks name)
+    unsigned* mask;           // [rows + 1, ldo / 32] keys kept in each remainder line
     int* pre_lo;              // [rows] prefix ranges
     int* pre_hi;
     int* rem_lo;              // [rows] remainder ranges
     int* rem_hi;
     unsigned* thr;            // [rows] threshold keys
+    float* thr_f;             // [rows] the same thresholds as fp32 values
     int* indices;             // [rows, topk] int32 output
 };
 

@@ -305,6 +305,23 @@ def topk_config(name: str) -> TopkCase:
     return topk_case(name=name, **TOPK_CONFIGS[name])
 
 
+# Fused logits + top-k: the dense workload's inputs (non-clean, the fused call
+# writes no logits) and the number of keys kept per row.
+FUSED_CONFIGS = {
+    "fused_topk_2k_32k_h64_d128_k2048": dict(dense="dense_2k_32k_h64_d128", topk=2048),
+    "fused_topk_8k_64k_h64_d128_k2048": dict(dense="dense_8k_64k_h64_d128", topk=2048),
+}
+
+
+def fused_config(name: str):
+    """(dense case, topk) of a fused logits + top-k workload."""
+    cfg = FUSED_CONFIGS[name]
+    case = dense_config(cfg["dense"])
+    case.name = name
+    case.clean = False
+    return case, cfg["topk"]
+
+
 @dataclass
 class MxDenseCase:
     """Dense MX (block-scaled) input: E4M3 or packed E2M1 elements with four
