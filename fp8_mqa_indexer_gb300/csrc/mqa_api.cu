@@ -1012,7 +1012,7 @@ mqa_status paged_mqa_topk_indices(const float* logits, const int32_t* context_le
 namespace {
 struct CandLayout {
     long long ldo;   // candidate row stride (floats), a multiple of 128
-    size_t vals, mask, ranges, thr, thr_f, total;   // byte offsets into the workspace
+    size_t vals, mask, ranges, thr, thr_f, t0, total;   // byte offsets into the workspace
 };
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1030,7 +1030,8 @@ CandLayout cand_layout(int S_q, int S_kv)
     l.ranges = l.mask + round256((rows + 1) * (size_t)(l.ldo / 32) * sizeof(unsigned));
     l.thr = l.ranges + round256(4 * rows * sizeof(int));
     l.thr_f = l.thr + round256(rows * sizeof(unsigned));
-    l.total = l.thr_f + round256(rows * sizeof(float));
+    l.t0 = l.thr_f + round256(rows * sizeof(float));
+    l.total = l.t0 + round256(rows * sizeof(unsigned));
     return l;
 }
 }  // namespace
@@ -1098,6 +1099,7 @@ mqa_status mqa_logits_topk(const void* q, const void* kv, const float* kv_scale,
     cp.rem_hi = ranges + 3 * (size_t)S_q;
     cp.thr = reinterpret_cast<unsigned*>(ws + l.thr);
     cp.thr_f = reinterpret_cast<float*>(ws + l.thr_f);
+    cp.t0 = reinterpret_cast<unsigned*>(ws + l.t0);
     cp.indices = indices;
     cudaStream_t strm = (cudaStream_t)stream;
     float* vals = reinterpret_cast<float*>(ws + l.vals);

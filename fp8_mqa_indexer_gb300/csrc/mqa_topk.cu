@@ -181,21 +181,24 @@ __device__ __forceinline__ void tile_offsets(unsigned long long pre, unsigned lo
 
 // The bin of hist[0, NBINS) that holds the need-th largest element (1 <= need
 // <= the histogram's total): its index, the elements in higher bins and the
-// elements in the bin.  Ends with the selection visible to all threads.
+// elements in the bin.  Ends with the selection visible to all threads.  The
+// histogram is sm.hist unless `hist` names another shared array.
 template <int NBINS>
 __device__ __forceinline__ void select_bin(TopkSmem& sm, unsigned need, int& buf, unsigned& bin,
-                                           unsigned& above, unsigned& count)
+                                           unsigned& above, unsigned& count,
+                                           const unsigned* hist = nullptr)
 {
+    const unsigned* hs = hist ? hist : sm.hist;
     constexpr int kB = NBINS >= kNT ? NBINS / kNT : 1;   // bins per thread
     static_assert(kB == 1 || kB % 4 == 0, "bins are read four at a time");
     const int b0 = threadIdx.x * kB;
     unsigned h[kB], s = 0;
     if constexpr (kB == 1) {
-        h[0] = b0 < NBINS ? sm.hist[b0] : 0u;
+        h[0] = b0 < NBINS ? hs[b0] : 0u;
     } else {
 #pragma unroll
         for (int q = 0; q < kB; q += 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(&sm.hist[b0 + q]);
+            const uint4 v = *reinterpret_cast<const uint4*>(&hs[b0 + q]);
             h[q] = v.x, h[q + 1] = v.y, h[q + 2] = v.z, h[q + 3] = v.w;
         }
     }
@@ -848,16 +851,22 @@ __global__ void cand_split_kernel(CandTopkParams p)
     p.rem_hi[i] = rem_hi;
     p.thr[i] = 0u;
     p.thr_f[i] = __int_as_float(0xff800000);   // -inf
+    p.t0[i] = 0u;
 }
 
 // thr[i] = order key T of the topk-th largest logit of row i's prefix and
 // thr_f[i] = that logit, for rows with a remainder (the prefix then holds more
 // than topk keys, every one of them written at its own column): digits 1 to 3
-// of the radix select, each over the prefix.
+// of the radix select, each over the prefix.  The same histograms give t0[i],
+// the lower edge of the 24-bit key prefix holding the prefix's need-th largest
+// logit, need scaled so that about 1.4 topk keys of the whole row lie at or
+// above t0 when the prefix is typical of the row (0: no such estimate).  t0
+// only steers the selection, which checks the count it yields.
 __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_threshold_kernel(CandTopkParams p)
 {
     extern __shared__ __align__(16) unsigned char topk_smem_raw[];
     TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
+    unsigned* hist2 = sm.cand_key;   // a second 4096-bin histogram
     int buf = 0;
     const unsigned k = (unsigned)p.topk;
     for (int i = blockIdx.x; i < p.rows; i += gridDim.x) {
@@ -871,6 +880,11 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_threshold_kernel(Can
         r.c_hi = __ldg(p.pre_hi + i);
         r.key_of_col0 = 0;
         r.c_start = r.c_lo - (long long)((reinterpret_cast<unsigned long long>(r.ptr + r.c_lo) >> 2) & 3);
+        const unsigned long long pre_n = (unsigned long long)(r.c_hi - r.c_lo);
+        const unsigned long long row_n = (unsigned long long)(r.c_hi - lo);
+        const unsigned long long want = (14ull * k * pre_n + 10ull * row_n - 1) / (10ull * row_n);
+        const unsigned need = want < 1 ? 1u : (unsigned)want;
+        const bool est = need < k;
         auto each = [&](auto&& f) { for_row<false>(r, 0ull, f); };
         clear_hist<kBins12>(sm);
         each([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
@@ -880,18 +894,28 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_threshold_kernel(Can
                     atomicAdd(&sm.hist[key[e] >> 20], 1u);
         });
         __syncthreads();
-        unsigned b1, above1, n1;
+        unsigned b1, above1, n1, c1 = 0, cabove1 = 0, cn1 = 0;
         select_bin<kBins12>(sm, k, buf, b1, above1, n1);
+        if (est)
+            select_bin<kBins12>(sm, need, buf, c1, cabove1, cn1);
         clear_hist<kBins12>(sm);
+        for (int b = threadIdx.x; b < kBins12 / 4; b += kNT)
+            reinterpret_cast<uint4*>(hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
         each([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
 #pragma unroll
-            for (int e = 0; e < kPer; ++e)
+            for (int e = 0; e < kPer; ++e) {
                 if (((okm >> e) & 1u) && (key[e] >> 20) == b1)
                     atomicAdd(&sm.hist[(key[e] >> 8) & 0xfffu], 1u);
+                if (est && ((okm >> e) & 1u) && (key[e] >> 20) == c1)
+                    atomicAdd(&hist2[(key[e] >> 8) & 0xfffu], 1u);
+            }
         });
         __syncthreads();
-        unsigned b2, above2, n2;
+        unsigned b2, above2, n2, c2 = 0, cabove2 = 0, cn2 = 0;
         select_bin<kBins12>(sm, k - above1, buf, b2, above2, n2);
+        if (est)
+            select_bin<kBins12>(sm, need - cabove1, buf, c2, cabove2, cn2, hist2);
         const unsigned prefix = (b1 << 12) | b2;
         clear_hist<kBins8>(sm);
         each([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
@@ -908,6 +932,7 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_threshold_kernel(Can
             p.thr[i] = T;
             // the logit whose order key is T (order_key inverted)
             p.thr_f[i] = __uint_as_float((T & 0x80000000u) ? (T ^ 0x80000000u) : ~T);
+            p.t0[i] = est ? (c1 << 20) | (c2 << 8) : 0u;
         }
     }
 }
@@ -942,23 +967,37 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) cand_select_kernel(CandTo
             cv.s = __ldg(p.rem_hi + i);
             cv.thr = __ldg(p.thr + i);
             auto walk = [&](auto&& f) { for_cand_row(cv, f); };
-            clear_hist<kBins12>(sm);
-            walk([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
+            // common case: the estimate t0 leaves between topk and kCap
+            // candidates; one walk compacts them and the rest is in shared memory
+            const unsigned t0 = __ldg(p.t0 + i);
+            bool done = false;
+            if (t0 != 0u) {
+                const unsigned m = compact_walk(sm, walk, t0, buf);
+                if (m >= k && m <= (unsigned)kCap) {
+                    if (!select_from_list_rel(sm, m, k, t0, out, buf))
+                        select_from_list(sm, m, k, out, buf);
+                    done = true;
+                }
+            }
+            if (!done) {
+                clear_hist<kBins12>(sm);
+                walk([&](const unsigned(&key)[kPer], unsigned okm, RowIdx) {
 #pragma unroll
-                for (int e = 0; e < kPer; ++e)
-                    if ((okm >> e) & 1u)
-                        atomicAdd(&sm.hist[key[e] >> 20], 1u);
-            });
-            __syncthreads();
-            unsigned b1, above1, n1;
-            select_bin<kBins12>(sm, k, buf, b1, above1, n1);
-            if (above1 + n1 <= (unsigned)kCap) {
-                const unsigned mm = compact_walk(sm, walk, b1 << 20, buf);
-                finish_row(
-                    sm, [&](auto&& f) { for_cand(sm, mm < (unsigned)kCap ? mm : (unsigned)kCap, f); },
-                    b1, above1, k, out, buf);
-            } else {
-                finish_row(sm, walk, b1, above1, k, out, buf);
+                    for (int e = 0; e < kPer; ++e)
+                        if ((okm >> e) & 1u)
+                            atomicAdd(&sm.hist[key[e] >> 20], 1u);
+                });
+                __syncthreads();
+                unsigned b1, above1, n1;
+                select_bin<kBins12>(sm, k, buf, b1, above1, n1);
+                if (above1 + n1 <= (unsigned)kCap) {
+                    const unsigned mm = compact_walk(sm, walk, b1 << 20, buf);
+                    finish_row(
+                        sm, [&](auto&& f) { for_cand(sm, mm < (unsigned)kCap ? mm : (unsigned)kCap, f); },
+                        b1, above1, k, out, buf);
+                } else {
+                    finish_row(sm, walk, b1, above1, k, out, buf);
+                }
             }
         }
         for (unsigned c = taken + threadIdx.x; c < k; c += kNT)

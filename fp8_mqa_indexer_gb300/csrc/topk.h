@@ -50,6 +50,7 @@ struct CandTopkParams {
     int* rem_hi;
     unsigned* thr;            // [rows] threshold keys
     float* thr_f;             // [rows] the same thresholds as fp32 values
+    unsigned* t0;             // [rows] selection hint: a key about 1.4 topk keys clear (0: none)
     int* indices;             // [rows, topk] int32 output
 };
 

@@ -299,13 +299,13 @@ def test_fused_topk_zero_rows_is_a_no_op(lib):
 
 def test_fused_topk_workspace_size(lib):
     # one fp32 slot per key (rows padded to 128 keys), one mask word per 32
-    # keys (and a scratch row of them), four range words and two thresholds
-    # per row, each part 256-aligned
+    # keys (and a scratch row of them), four range words, two thresholds and a
+    # selection hint per row, each part 256-aligned
     def r256(x):
         return (x + 255) // 256 * 256
     for S_q, S_kv in ((1, 1), (4, 256), (2048, 32768), (17, 3001), (3, 0)):
         ldo = (max(S_kv, 1) + 127) // 128 * 128
         want = (r256(S_q * ldo * 4) + r256((S_q + 1) * ldo // 32 * 4) + r256(16 * S_q)
-                + r256(4 * S_q) + r256(4 * S_q))
+                + r256(4 * S_q) + r256(4 * S_q) + r256(4 * S_q))
         assert mqa.mqa_logits_topk_workspace_size(S_q, S_kv) == want
     assert lib.mqa_logits_topk_workspace_size(-1, 5) == 0

@@ -148,6 +148,12 @@ def test_exact_ties(dev):
     for i in range(40):
         n = max(int(case.k_end[i]), 0)
         assert np.array_equal(got[i][:min(n, 100)], np.arange(min(n, 100)))
+    # rows longer than the shared list, all equal: every estimate fails and
+    # the selection walks the candidates for each digit
+    case = wl.dense_case(6, 9000, 64, 128, seed=932, ranges="full", clean=False, name="long ties")
+    case.weights.zero_()
+    got = check_against_written_logits(case, dev, 1000)
+    assert np.array_equal(got, np.tile(np.arange(1000, dtype=np.int32), (6, 1)))
     # coarse inputs: many equal logits, not all
     case = wl.dense_case(40, 5000, 32, 64, seed=931, ranges="full", clamp=0.5, clean=False,
                          name="coarse")
