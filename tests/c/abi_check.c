@@ -55,6 +55,30 @@ int main(void)
     expect("paged topk width", paged_mqa_topk_indices(f, i, i, 2, 2, 1024, 1000, 16, NULL),
            MQA_ERR_INVALID_ARG);
     {
+        /* fused logits + top-k: the workspace size is a pure function; the
+         * call rejects a short workspace, a clean flag and topk = 0 */
+        const size_t ws = mqa_logits_topk_workspace_size(4, 256);
+        if (ws == 0 || ws != mqa_logits_topk_workspace_size(4, 256) ||
+            mqa_logits_topk_workspace_size(-1, 256) != 0) {
+            printf("FAIL fused workspace size %zu\n", ws);
+            ++failures;
+        }
+        static char wsbuf[256] __attribute__((aligned(256)));
+        expect("fused short workspace",
+               mqa_logits_topk(p, p, f, f, i, i, i, wsbuf, 256, 4, 256, 64, 128, 16, 0, NULL),
+               MQA_ERR_INVALID_ARG);
+        expect("fused clean flag",
+               mqa_logits_topk(p, p, f, f, i, i, i, wsbuf, ws, 4, 256, 64, 128, 16, MQA_CLEAN, NULL),
+               MQA_ERR_INVALID_ARG);
+        expect("fused topk=0",
+               mqa_logits_topk(p, p, f, f, i, i, i, wsbuf, ws, 4, 256, 64, 128, 0, 0, NULL),
+               MQA_ERR_INVALID_ARG);
+        expect("fused S_q = 0",
+               mqa_logits_topk(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 0, 256, 64, 128,
+                               16, 0, NULL),
+               MQA_OK);
+    }
+    {
         const uint32_t *u = (const uint32_t *)buf;
         expect("mx D=64", mqa_logits_mx(p, u, p, u, f, i, i, f, 4, 256, 64, 64, 256, MQA_CLEAN, NULL),
                MQA_ERR_UNSUPPORTED);
