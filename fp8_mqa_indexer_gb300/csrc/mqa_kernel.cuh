@@ -38,9 +38,10 @@
 //    kind::mxf8f6f4; dense calls transpose the key scales in the producer,
 //    paged calls copy them by TMA with the pages and the MMA warp transposes.
 //  * Candidate instances (output type CandOut) serve the fused logits + top-k
-//    call: a logit of a row's range is written (at its own column) only when
-//    it is not below the row's threshold, and each 32-key line gets a 32-bit
-//    mask of the keys written; nothing else is written (no -inf fill).
+//    call: a logit of a row's range is kept only when it is not below the
+//    row's threshold; the kept logits of each 32-key line are written packed
+//    at the front of the line (zero-padded to a 32-byte boundary) with a
+//    32-bit mask of their keys; nothing else is written (no -inf fill).
 //  * Pipelines: a ring of key tiles (+ their scales and a small work record),
 //    two query-block buffers (+ weights and per-token ranges) and two TMEM
 //    accumulators of 256 columns; every hand-off is an mbarrier, every wait is
@@ -96,8 +97,8 @@ struct __align__(16) TokRow {
     long long pad;   // candidate instances: the row's threshold (fp32 bits, low half)
 };
 
-// Output type of the candidate instances: the kept fp32 logits at their own
-// columns and, per 32-key line, a mask of their keys.
+// Output type of the candidate instances: per 32-key line, the kept fp32
+// logits packed at the front of the line and a mask of their keys.
 struct CandOut {};
 
 struct Params {
@@ -458,18 +459,25 @@ struct Epilogue {
         const int j = st.info.t * kBlockKV + row;
         if constexpr (kCand) {
             // The warp's 32 lanes are the 32 keys of one line (row = 32 quad +
-            // lane): one ballot gives the line's mask.  "not below" keeps NaNs: a superset of the keys at or
+            // lane): one ballot gives the line's mask and each kept logit's
+            // place.  "not below" keeps NaNs: a superset of the keys at or
             // above the threshold's order key is all the selection needs.
             const bool take =
                 j >= t.vlo && j < t.vhi && !(v < __uint_as_float((unsigned)t.pad));
             const unsigned m = __ballot_sync(0xffffffffu, take);
-            const int l0 = j - (row & 31);   // first key of the line
-            if (take)
-                static_cast<float*>(p.logits)[t.off + j] = v;
+            const int lane = row & 31;
+            const int cnt = __popc(m);
+            float* line = static_cast<float*>(p.logits) + t.off + (j - lane);
+            if (take)   // packed at the front of the line, in key order
+                line[__popc(m & ((1u << lane) - 1u))] = v;
+            // zeros up to the next 32-byte boundary: whole sectors only, so no
+            // partly written sector is filled from DRAM
+            if (lane >= cnt && lane < ((cnt + 7) & ~7))
+                line[lane] = 0.f;
             // every line of the tile gets a mask (a row's masks are read only
             // over the range this launch covers for it)
-            if ((row & 31) == 0)
-                p.cand_mask[(t.off >> 5) + (l0 >> 5)] = m;
+            if (lane == 0)
+                p.cand_mask[(t.off >> 5) + ((j - lane) >> 5)] = m;
         } else {
             // one predicated store: the logit, -inf (clean) or nothing
             if (j >= t.slo && j < t.shi)

@@ -745,10 +745,9 @@ __global__ void __launch_bounds__(kNT, kTopkCtasPerSm) topk_kernel(TopkParams p)
 
 // ------------------------------------------------ fused logits + top-k
 // The candidate form of a row with range [lo, hi) split at s: keys [s, hi)
-// (the prefix) have their logits at their own columns; in [lo, s) (the
-// remainder) only the keys whose bits are set in their line's mask (line L:
-// keys [32 L, 32 L + 32)) have their logits there, the other columns hold
-// garbage.
+// (the prefix) have their logits at their own columns; line L of [lo, s) (the
+// remainder; keys [32 L, 32 L + 32)) holds, packed at its front in key order,
+// the logits of the keys whose bits are set in the line's mask.
 struct CandView {
     const float* vals;      // the row's values
     const unsigned* mask;   // the row's line masks
@@ -798,13 +797,18 @@ __device__ __forceinline__ void for_cand_row(const CandView& r, F&& f)
                         }
                     }
                 }
-            } else {   // remainder: candidates at their own columns
-                const unsigned bits = (m[g] >> (int)(c & 31)) & 0xfu;
-                if (bits) {
-                    const float4 x = load4(r.vals + c);
-                    key[4 * g] = order_key(x.x), key[4 * g + 1] = order_key(x.y);
-                    key[4 * g + 2] = order_key(x.z), key[4 * g + 3] = order_key(x.w);
-                    okm |= bits << (4 * g);
+            } else {   // remainder: candidates packed at the front of the line
+                const int pos = (int)(c & 31);
+                const float* line = r.vals + (c & ~31ll);
+                const unsigned bits = (m[g] >> pos) & 0xfu;
+                unsigned rank = __popc(m[g] & ((1u << pos) - 1u));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if ((bits >> j) & 1u) {
+                        key[4 * g + j] = order_key(__ldg(line + rank));
+                        ++rank;
+                        okm |= 1u << (4 * g + j);
+                    }
                 }
             }
         }

@@ -29,8 +29,8 @@ cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t stream);
 // remainder [lo, s).  The plain logits kernel writes every logit of the
 // prefix at its own column; the threshold kernel sets thr[i] to the order key
 // of the prefix's topk-th largest logit (thr_f[i]: that logit); the candidate
-// logits kernel then writes the remainder's logits not below thr_f[i], at
-// their own columns, with a mask of their keys per 32-key line; the select
+// logits kernel then writes the remainder's logits not below thr_f[i], packed
+// at the front of each 32-key line, with a mask of their keys; the select
 // kernel takes the topk
 // largest of the prefix's logits and the remainder's candidates.  Rows with at
 // most topk keys have empty prefix and remainder.
@@ -41,8 +41,8 @@ struct CandTopkParams {
     int n_cols;               // keys (S_kv)
     int topk;
     long long ldo;            // candidate row stride in floats, a multiple of 128
-    float* vals;              // [rows, ldo] logits at their own columns (the prefix's, and
-                              // the remainder's that its masks name)
+    float* vals;              // [rows, ldo] prefix logits at their own columns; remainder
+                              // line L packs its kept logits at 32 L
     unsigned* mask;           // [rows + 1, ldo / 32] keys kept in each remainder line
     int* pre_lo;              // [rows] prefix ranges
     int* pre_hi;
