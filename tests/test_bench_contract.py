@@ -13,7 +13,7 @@ KEYS = {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_
 
 
 @pytest.mark.parametrize("workload", ["dense_tiny", "paged_b64_n2_h64_d128", "topk_2k_32k_k2048",
-                                      "mx_2k_32k_h64_d128"])
+                                      "mx_2k_32k_h64_d128", "fused_topk_2k_32k_h64_d128_k2048"])
 def test_reference_arm_prints_one_contract_line(workload):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--workload", workload, "--steps", "1", "--warmup", "0", "--ref-budget", "0.3"],
