@@ -125,6 +125,18 @@ def test_ragged_rows(dev, S_kv, topk):
     check_within_oracle_bound(case, got, topk)
 
 
+def test_topk_above_the_shared_list(dev):
+    # topk 5000 > the 4096-entry shared list: rows with a remainder take the
+    # selection's full digit path over the candidates
+    S_kv = 20000
+    ks = [0, 0, 0, 100, 3, 0, 7000, 0, 0, 15000]
+    ke = [S_kv, 19999, 12000, S_kv, 10007, 5001, S_kv, 4999, 0, S_kv]
+    case = wl.dense_case(len(ks), S_kv, 64, 128, seed=990, ranges="custom", k_start=ks, k_end=ke,
+                         clean=False, name="topk 5000")
+    got = check_against_written_logits(case, dev, 5000)
+    check_within_oracle_bound(case, got, 5000)
+
+
 @pytest.mark.parametrize("H,D", [(8, 64), (32, 64), (64, 64), (8, 128), (32, 128)])
 def test_every_instance(dev, H, D):
     case = wl.dense_case(70, 2500, H, D, seed=910 + H + D, ranges="causal_tail", clean=False,
