@@ -361,14 +361,19 @@ MQA_API mqa_status paged_mqa_topk_indices(const float *logits, const int32_t *co
  *   workspace  device memory of at least mqa_logits_topk_workspace_size(S_q,
  *            S_kv) bytes, 256-byte aligned, owned by the caller; its contents
  *            on entry do not matter and on return are unspecified.  It holds
- *            one fp32 slot per logit, but only the candidates are written:
- *            for each row the logits of a tail of its range (max(2 topk,
- *            sqrt(len topk)) keys, at a 128-key boundary) and those of the
- *            rest at or above the topk-th largest logit of that tail.
+ *            one fp32 slot per key of every row (rows padded to a multiple of
+ *            128 keys), a 32-bit mask per 32 keys and a few words per row, but
+ *            only the candidates are written: for each row the logits of a
+ *            tail of its range (max(2 topk, sqrt(len topk)) keys, at a 128-key
+ *            boundary) and those of the rest not below the topk-th largest
+ *            logit of that tail.
  *   flags: MQA_WEIGHTS_BF16 or 0 (others are rejected).
  * The result equals mqa_topk_indices applied to the mqa_logits output for the
  * same inputs, bit for bit (both compute each logit with the same
- * arithmetic).  Five kernels on `stream`; no host synchronisation.
+ * arithmetic).  Five kernels on `stream`; no host synchronisation.  Errors:
+ * invalid sizes, pointers, alignment or flags return MQA_ERR_INVALID_ARG and
+ * unsupported H or D MQA_ERR_UNSUPPORTED before anything is launched; a
+ * kernel wait that runs out is reported by mqa_device_status.
  */
 MQA_API size_t mqa_logits_topk_workspace_size(int S_q, int S_kv);
 MQA_API mqa_status mqa_logits_topk(const void *q, const void *kv, const float *kv_scale,
