@@ -8,8 +8,9 @@ cases are also checked against the oracle's own logits: every selected key
 must be, within the oracle's error bound, at least as large as every key left
 out.  Cases cover ragged, empty, inverted and clipped ranges, rows shorter
 than, equal to and just longer than topk, rows whose tail holds the whole
-range, exact ties, negative key scales, every (H, D) instance, bf16 weights, a
-workspace full of garbage, and the 2048 x 32768 and 8192 x 65536 workloads.
+range, exact ties, topk above the shared list, negative key scales, every
+(H, D) instance, bf16 weights, a workspace full of garbage, replay from a CUDA
+graph, and the 2048 x 32768 and 8192 x 65536 workloads.
 """
 import numpy as np
 import pytest
@@ -248,3 +249,31 @@ def test_full_workloads_equal_the_unfused_pipeline(dev, name):
     Lr = L[rows].cpu().numpy()
     want = oracle_topk_rows(Lr, case.k_start[rows], case.k_end[rows], 2048, case.S_kv)
     assert np.array_equal(got[rows], want)
+
+
+def test_captured_in_a_cuda_graph(dev):
+    """The call makes no host synchronisation and no allocation, so it can be
+    captured in a CUDA graph; replays give the eager result."""
+    case = wl.dense_case(96, 12000, 64, 128, seed=995, ranges="causal_tail", clean=False,
+                         name="graph")
+    d = to_dev(case, dev)
+    ws = torch.empty(mqa.mqa_logits_topk_workspace_size(96, 12000), dtype=torch.uint8, device=dev)
+    out = torch.full((96, 700), -7, dtype=torch.int32, device=dev)
+    eager = fused(d, 700, ws)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # warm-up on the capture stream
+        mqa.mqa_logits_topk(d["q"], d["kv"], d["s"], d["w"], d["ks"], d["ke"], 700, out,
+                            workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mqa.mqa_logits_topk(d["q"], d["kv"], d["s"], d["w"], d["ks"], d["ke"], 700, out,
+                            workspace=ws)
+    for _ in range(3):
+        out.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), eager)
+    assert mqa.device_status() == 0
