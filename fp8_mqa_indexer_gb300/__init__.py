@@ -24,7 +24,7 @@ __all__ = [
     "paged_mqa_logits_noalloc", "paged_mqa_logits_mx", "mqa_topk_indices", "paged_mqa_topk_indices",
     "mqa_logits_topk", "mqa_logits_topk_workspace_size",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "library_path", "load_library",
-    "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS", "MQA_OUT_BF16",
+    "MQA_CLEAN", "MQA_COMPRESSED", "MQA_CHECK_BOUNDS", "MQA_OUT_BF16", "MQA_KV_FUSED",
 ]
 
 MQA_CLEAN = 1
@@ -33,6 +33,7 @@ MQA_CHECK_BOUNDS = 4
 MQA_MXFP4 = 8
 MQA_OUT_BF16 = 16
 MQA_WEIGHTS_BF16 = 32
+MQA_KV_FUSED = 64
 
 STATUS_NAMES = {0: "MQA_OK", 1: "MQA_ERR_INVALID_ARG", 2: "MQA_ERR_UNSUPPORTED", 3: "MQA_ERR_CUDA",
                 4: "MQA_ERR_TIMEOUT", 5: "MQA_ERR_BAD_INPUT"}
@@ -299,16 +300,21 @@ def _weights_flag(weights) -> int:
 
 def _paged_inputs(q, kv_cache, kv_scales, weights, context_lens, block_table, next_n):
     """Type and shape checks shared by the two paged calls; returns
-    (R, H, D, B, next_n, num_blocks, block_kv, max_blocks)."""
+    (R, H, D, B, next_n, num_blocks, block_kv, max_blocks).  kv_scales None:
+    the fused layout (kv_cache uint8 [num_blocks, block_kv * (D + 4)])."""
     import torch
     f8 = _fp8_types()
     _dev(q, "q", f8)
-    _dev(kv_cache, "kv_cache", f8)
-    _dev(kv_scales, "kv_scales", (torch.float32,))
+    if kv_scales is None:
+        _dev(kv_cache, "kv_cache", (torch.uint8,))
+    else:
+        _dev(kv_cache, "kv_cache", f8)
+        _dev(kv_scales, "kv_scales", (torch.float32,))
     _dev(weights, "weights", (torch.float32, torch.bfloat16))
     _dev(context_lens, "context_lens", (torch.int32,))
     _dev(block_table, "block_table", (torch.int32,))
-    return paged_shapes(tuple(q.shape), tuple(kv_cache.shape), tuple(kv_scales.shape),
+    return paged_shapes(tuple(q.shape), tuple(kv_cache.shape),
+                        None if kv_scales is None else tuple(kv_scales.shape),
                         tuple(weights.shape), tuple(context_lens.shape), tuple(block_table.shape),
                         next_n)
 
@@ -319,20 +325,30 @@ def paged_shapes(q, kv_cache, kv_scales, weights, context_lens, block_table, nex
     Returns (R, H, D, B, next_n, num_blocks, block_kv, max_blocks) or raises
     ValueError: q [B*next_n, H, D], kv_cache [num_blocks, block_kv, D],
     kv_scales [num_blocks, block_kv], weights [B*next_n, H], context_lens [B],
-    block_table [B, max_blocks].  next_n is inferred from q and context_lens
-    when not given.
+    block_table [B, max_blocks].  kv_scales None: the fused layout, kv_cache
+    [num_blocks, block_kv * (D + 4)] bytes.  next_n is inferred from q and
+    context_lens when not given.
     """
-    if len(q) != 3 or len(kv_cache) != 3 or len(block_table) != 2 or len(context_lens) != 1:
-        raise ValueError("q and kv_cache must be 3-D, block_table 2-D, context_lens 1-D")
+    fused = kv_scales is None
+    if len(q) != 3 or len(kv_cache) != (2 if fused else 3) or len(block_table) != 2 or \
+            len(context_lens) != 1:
+        raise ValueError("q must be 3-D, kv_cache 3-D (2-D when fused), block_table 2-D, "
+                         "context_lens 1-D")
     R, H, D = q
     B = context_lens[0]
     if next_n is None:
         if B == 0 or R % B:
             raise ValueError("cannot infer next_n from q and context_lens")
         next_n = R // B
-    num_blocks, block_kv, D2 = kv_cache
+    if fused:
+        num_blocks, page_bytes = kv_cache
+        if page_bytes % (D + 4):
+            raise ValueError("a fused page holds block_kv * (D + 4) bytes")
+        block_kv, D2 = page_bytes // (D + 4), D
+    else:
+        num_blocks, block_kv, D2 = kv_cache
     if D2 != D or R != B * next_n or tuple(weights) != (R, H) or \
-            tuple(kv_scales) != (num_blocks, block_kv):
+            (not fused and tuple(kv_scales) != (num_blocks, block_kv)):
         raise ValueError("shape mismatch between paged inputs (q rows must be B * next_n)")
     if block_table[0] != B:
         raise ValueError("block_table must have one row per sequence")
@@ -366,7 +382,9 @@ def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
     [num_blocks, block_kv] f32, weights [B*next_n, H] f32, context_lens [B]
     int32, block_table [B, max_blocks_per_seq] int32, schedule_meta from
     ``paged_mqa_logits_metadata``.  Returns logits [B*next_n, ldo] f32 with
-    ldo >= max_blocks_per_seq * block_kv.
+    ldo >= max_blocks_per_seq * block_kv.  kv_scales None: the fused page
+    layout (flag MQA_KV_FUSED), kv_cache uint8 [num_blocks, block_kv * (D + 4)]
+    with each page's key rows followed by their fp32 scales.
     """
     import torch
     R, H, D, B, next_n, num_blocks, block_kv, max_blocks = _paged_inputs(
@@ -377,7 +395,8 @@ def paged_mqa_logits(q, kv_cache, kv_scales, weights, context_lens, block_table,
     num_sms = schedule_meta.shape[0] - 1
     logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device, out_dtype)
     flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0) | \
-        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0) | _weights_flag(weights)
+        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0) | _weights_flag(weights) | \
+        (MQA_KV_FUSED if kv_scales is None else 0)
     with torch.cuda.device(q.device):
         _check(load_library().paged_mqa_logits(_ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights),
                                                _ptr(context_lens), _ptr(block_table), max_blocks,
@@ -443,7 +462,8 @@ def paged_mqa_logits_noalloc(q, kv_cache, kv_scales, weights, context_lens, bloc
         raise ValueError("paged_mqa_logits_noalloc needs a caller-provided logits buffer")
     logits = _paged_logits_out(logits, R, max_blocks * block_kv, q.device)
     flags = (MQA_CLEAN if clean else 0) | (MQA_CHECK_BOUNDS if check_bounds else 0) | \
-        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0) | _weights_flag(weights)
+        (MQA_OUT_BF16 if logits.dtype == torch.bfloat16 else 0) | _weights_flag(weights) | \
+        (MQA_KV_FUSED if kv_scales is None else 0)
     with torch.cuda.device(q.device):
         _check(load_library().paged_mqa_logits_noalloc(
             _ptr(q), _ptr(kv_cache), _ptr(kv_scales), _ptr(weights), _ptr(context_lens),

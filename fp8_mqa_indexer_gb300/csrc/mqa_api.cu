@@ -141,6 +141,27 @@ mqa_status make_map_vec_f32(CUtensorMap* m, const void* base, unsigned long long
     return MQA_OK;
 }
 
+// Map over [rows, cols] fp32 (or 4-byte) values whose rows start stride_bytes
+// apart (a multiple of 16), with a box of one row of `cols` values.
+mqa_status make_map_rows_f32(CUtensorMap* m, const void* base, unsigned long long cols,
+                             unsigned long long rows, unsigned long long stride_bytes,
+                             const char* what)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {stride_bytes};
+    cuuint32_t boxd[2] = {(cuuint32_t)cols, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+                    boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MQA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+    return MQA_OK;
+}
+
 bool aligned(const void* p, uintptr_t a)
 {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
@@ -682,10 +703,12 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const void* kv_sc
         num_sms = 1;
     }
     *nothing_to_do = false;
-    if (flags & ~(unsigned)(MQA_CLEAN | MQA_CHECK_BOUNDS | MQA_OUT_BF16 | MQA_WEIGHTS_BF16))
+    if (flags & ~(unsigned)(MQA_CLEAN | MQA_CHECK_BOUNDS | MQA_OUT_BF16 | MQA_WEIGHTS_BF16 |
+                            MQA_KV_FUSED))
         return fail((flags & MQA_COMPRESSED) ? MQA_ERR_UNSUPPORTED : MQA_ERR_INVALID_ARG,
-                    "paged logits take only MQA_CLEAN, MQA_CHECK_BOUNDS, MQA_OUT_BF16 and "
-                    "MQA_WEIGHTS_BF16 (flags 0x%x)", flags);
+                    "paged logits take only MQA_CLEAN, MQA_CHECK_BOUNDS, MQA_OUT_BF16, "
+                    "MQA_WEIGHTS_BF16 and MQA_KV_FUSED (flags 0x%x)", flags);
+    const bool fused = (flags & MQA_KV_FUSED) != 0;
     if (B < 0 || next_n < 1 || num_blocks < 1 || max_blocks_per_seq < 1 || num_sms < 1)
         return fail(MQA_ERR_INVALID_ARG,
                     "need B >= 0, next_n >= 1, num_blocks >= 1, max_blocks_per_seq >= 1, num_sms >= 1");
@@ -701,17 +724,21 @@ mqa_status validate_paged(const void* q, const void* kv_cache, const void* kv_sc
     if (ldo < width)
         return fail(MQA_ERR_INVALID_ARG, "ldo (%lld) < max_blocks_per_seq * block_kv (%lld)",
                     (long long)ldo, width);
-    if (width > INT_MAX - 256 || (long long)num_blocks * block_kv >= INT_MAX ||
+    // fused pages: block_kv key rows then block_kv * 4 / D rows' worth of scales
+    if (width > INT_MAX - 256 || (long long)num_blocks * (block_kv + 4 * block_kv / D) >= INT_MAX ||
         (long long)B * next_n * H >= INT_MAX)
         return fail(MQA_ERR_INVALID_ARG, "size too large");
+    if (fused && kv_scales)
+        return fail(MQA_ERR_INVALID_ARG, "kv_scales must be NULL with MQA_KV_FUSED");
     if (B == 0) {
         *nothing_to_do = true;
         return MQA_OK;
     }
-    if (!q || !kv_cache || !kv_scales || !weights || !context_lens || !block_table ||
+    if (!q || !kv_cache || (!fused && !kv_scales) || !weights || !context_lens || !block_table ||
         !schedule_meta || !logits)
         return fail(MQA_ERR_INVALID_ARG, "null pointer");
-    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(kv_scales, 16) || !aligned(weights, 16))
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || (!fused && !aligned(kv_scales, 16)) ||
+        !aligned(weights, 16))
         return fail(MQA_ERR_INVALID_ARG,
                     "q, kv_cache, kv_scales and weights must be 16-byte aligned");
     if (!aligned(logits, (flags & MQA_OUT_BF16) ? 2 : 4) || !aligned(context_lens, 4) ||
@@ -735,6 +762,9 @@ mqa_status paged_call(const void* q, const void* kv_cache, const float* kv_scale
                       bool fp4 = false)
 {
     const bool mx = kv_sf != nullptr;
+    const bool fused = (flags & MQA_KV_FUSED) != 0;
+    if (mx && fused)
+        return fail(MQA_ERR_UNSUPPORTED, "MQA_KV_FUSED is for FP8 keys with fp32 scales");
     bool nothing = false;
     mqa_status v0 = validate_paged(q, kv_cache, mx ? (const void*)kv_sf : (const void*)kv_scales,
                                    weights, context_lens, block_table, max_blocks_per_seq,
@@ -786,12 +816,20 @@ mqa_status paged_call(const void* q, const void* kv_cache, const float* kv_scale
     const CUtensorMapDataType edt =
         fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const unsigned long long row_bytes = fp4 ? (unsigned long long)D / 2 : 0;
-    if ((s = make_map_2d(&a.tm_kv, kv_cache, edt, 1, (unsigned long long)num_blocks * block_kv, D,
+    // Keys: rows of D bytes, page b's first at row b * page_rows.  Scales: a
+    // [num_blocks, block_kv] map, row b at byte b * scale_stride (fused pages:
+    // right after the page's keys).
+    const long long page_rows = fused ? block_kv + 4LL * block_kv / D : block_kv;
+    const void* scale_base = fused ? static_cast<const void*>(static_cast<const char*>(kv_cache) +
+                                                              (size_t)block_kv * D)
+                           : mx ? (const void*)kv_sf
+                                : (const void*)kv_scales;
+    const unsigned long long scale_stride =
+        fused ? (unsigned long long)block_kv * (D + 4) : (unsigned long long)block_kv * 4;
+    if ((s = make_map_2d(&a.tm_kv, kv_cache, edt, 1, (unsigned long long)num_blocks * page_rows, D,
                          block_kv, D, swz, "kv_cache", row_bytes)) != MQA_OK ||
-        // MX: a valid map over the key scale words, never used for copies
-        (s = make_map_vec_f32(&a.tm_scale, mx ? (const void*)kv_sf : (const void*)kv_scales,
-                              (unsigned long long)num_blocks * block_kv, block_kv, "kv_scales")) !=
-            MQA_OK)
+        (s = make_map_rows_f32(&a.tm_scale, scale_base, block_kv, num_blocks, scale_stride,
+                               "kv_scales")) != MQA_OK)
         return s;
     Params& p = a.p;
     p.logits = logits;
@@ -805,6 +843,7 @@ mqa_status paged_call(const void* q, const void* kv_cache, const float* kv_scale
     p.block_kv = block_kv;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = num_blocks;
+    p.kv_page_rows = (int)page_rows;
     p.width = width;
     p.width_i = (int)width;
     p.blk_stride = next_n;

@@ -120,6 +120,7 @@ struct Params {
     int block_kv;
     int max_blocks;
     int num_blocks;          // physical blocks of the pool (bounds the scale-word loads)
+    int kv_page_rows;        // paged: rows of D bytes from one page's keys to the next's
     // shared
     long long width;     // logical columns of an uncompressed row
     int width_i;         // the same, as an int (below 2^31 - 256)
@@ -953,10 +954,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < 4; ++k) {
                             if (k < ppt && ids[k] >= 0) {
                                 tma_load_2d(smem_u32(sm.kv[stage]) + k * p.block_kv * D, &tm_kv, bar, 0,
-                                            ids[k] * p.block_kv);
-                                // the slots' fp32 scales, or (MX) their scale words
+                                            ids[k] * p.kv_page_rows);
+                                // the slots' fp32 scales, or (MX) their scale words:
+                                // row ids[k] of the [num_blocks, block_kv] scale map
                                 tma_load_2d(smem_u32(&sm.scale[stage][k * p.block_kv]), &tm_scale, bar,
-                                            ids[k] * p.block_kv, 0);
+                                            0, ids[k]);
                             }
                         }
                     }

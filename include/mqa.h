@@ -85,7 +85,11 @@ enum {
      * weights of the same values.  For mqa_logits, mqa_logits_scheduled,
      * mqa_logits_mx and the paged calls ("[PR #435] ...", section
      * "Validation": FP32/BF16 weights). */
-    MQA_WEIGHTS_BF16 = 32u
+    MQA_WEIGHTS_BF16 = 32u,
+    /* Paged FP8 calls: each page of kv_cache holds its block_kv key rows (D
+     * E4M3 bytes each) followed by their block_kv fp32 scales, block_kv * (D
+     * + 4) bytes in all; kv_scales must be NULL. */
+    MQA_KV_FUSED = 64u
 };
 
 /*
@@ -213,6 +217,9 @@ MQA_API mqa_status paged_mqa_logits_metadata(const int32_t *context_lens, int B,
  *                r = b * next_n + t is query t of sequence b
  *   kv_cache     [num_blocks, block_kv, D] FP8 E4M3 bytes, 16-byte aligned
  *   kv_scales    [num_blocks, block_kv] fp32, 16-byte aligned
+ *                (with MQA_KV_FUSED: kv_cache is [num_blocks, block_kv * (D +
+ *                4)] bytes, a page's key rows then their scales, and
+ *                kv_scales is NULL; the same logits as the separate layout)
  *   weights      [B * next_n, H] fp32 (bf16 with MQA_WEIGHTS_BF16), 16-byte
  *                aligned
  *   context_lens [B] int32
@@ -233,7 +240,7 @@ MQA_API mqa_status paged_mqa_logits_metadata(const int32_t *context_lens, int B,
  *                length; the kernel runs one CTA per entry).  Not in the pages'
  *                call, where the schedule tensor carries its own shape.
  *   flags        MQA_CLEAN | MQA_CHECK_BOUNDS | MQA_OUT_BF16 | MQA_WEIGHTS_BF16
- *                (MQA_COMPRESSED is rejected)
+ *                | MQA_KV_FUSED (MQA_COMPRESSED is rejected)
  */
 MQA_API mqa_status paged_mqa_logits(const void *q, const void *kv_cache, const float *kv_scales,
                             const void *weights, const int32_t *context_lens,

@@ -48,6 +48,9 @@ int main(void)
     expect("paged compressed", paged_mqa_logits(p, p, f, f, i, i, 16, i, f, 2, 2, 64, 128, 64, 40, 8,
                                                 1024, MQA_CLEAN | MQA_COMPRESSED, NULL),
            MQA_ERR_UNSUPPORTED);
+    expect("paged fused with scales", paged_mqa_logits(p, p, f, f, i, i, 16, i, f, 2, 2, 64, 128, 64,
+                                                       40, 8, 1024, MQA_CLEAN | MQA_KV_FUSED, NULL),
+           MQA_ERR_INVALID_ARG);
     expect("noalloc ldo", paged_mqa_logits_noalloc(p, p, f, f, i, i, 16, f, 2, 2, 64, 128, 64, 40,
                                                    1000, MQA_CLEAN, NULL),
            MQA_ERR_INVALID_ARG);

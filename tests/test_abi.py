@@ -93,6 +93,8 @@ def call_paged(lib, **kw):
     (dict(flags=2), 2), (dict(flags=3), 2), (dict(flags=8), 1), (dict(D=32), 2), (dict(H=8), 2),
     (dict(next_n=65), 2), (dict(block_kv=16), 2), (dict(ldo=1000), 1), (dict(num_sms=0), 1),
     (dict(next_n=0), 1), (dict(B=-1), 1), (dict(meta=None), 1), (dict(kv_cache=F + 1), 1),
+    # MQA_KV_FUSED (64): the scales live in the pages, so kv_scales must be NULL
+    (dict(flags=1 | 64), 1), (dict(flags=1 | 64 | 2), 2), (dict(flags=1 | 64, kv_scales=None, q=None), 1),
 ])
 def test_paged_rejects_invalid_arguments(lib, kw, status):
     assert call_paged(lib, **kw) == status
@@ -117,7 +119,7 @@ def call_paged_mx(lib, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(D=64), 2), (dict(q_sf=None), 1), (dict(kv_sf=None), 1), (dict(q_sf=F + 2), 1),
     (dict(flags=1 | 8), 1), (dict(flags=2), 2), (dict(H=8), 2), (dict(block_kv=48), 2),
-    (dict(ldo=1000), 1),
+    (dict(ldo=1000), 1), (dict(flags=1 | 64), 2),
 ])
 def test_paged_mx_rejects_invalid_arguments(lib, kw, status):
     assert call_paged_mx(lib, **kw) == status

@@ -22,6 +22,16 @@ def test_consistent_shapes_pass():
     assert mqa.paged_shapes(**GOOD)[4] == 2          # next_n inferred
 
 
+def test_fused_page_shapes():
+    # kv_scales None: kv_cache [num_blocks, block_kv * (D + 4)] bytes
+    fused = dict(GOOD, kv_cache=(40, 64 * 132), kv_scales=None)
+    assert mqa.paged_shapes(**fused, next_n=2) == (8, 64, 128, 4, 2, 40, 64, 16)
+    with pytest.raises(ValueError):                  # not a whole number of D + 4 rows
+        mqa.paged_shapes(**dict(fused, kv_cache=(40, 64 * 132 + 4)), next_n=2)
+    with pytest.raises(ValueError):                  # a 3-D cache without scales
+        mqa.paged_shapes(**dict(fused, kv_cache=(40, 64, 128)), next_n=2)
+
+
 @pytest.mark.parametrize("kw", [
     dict(next_n=1),                                  # q rows != B * next_n
     dict(next_n=3),
