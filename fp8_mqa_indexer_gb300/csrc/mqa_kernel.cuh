@@ -176,8 +176,10 @@ struct __align__(1024) Smem {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t mma_done;
+    uint64_t neg_bar;        // dense: the epilogue warps' scale scan is done
     uint32_t tmem_base;
     int abort_flag;
+    int any_neg;             // dense: some key scale is negative
     int start_b;
     int start_t;
     int n_units;
@@ -656,7 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&sm.acc_empty[k]), n_epi);
         }
         mbar_init(smem_u32(&sm.mma_done), 1);
+        mbar_init(smem_u32(&sm.neg_bar), kNumEpiWarps);
         sm.abort_flag = 0;
+        sm.any_neg = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -793,21 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm.start_t = t0;
         }
     }
-    // Any negative key scale?  Without one (the usual case: scales are
-    // quantisation factors) the epilogue runs the ReLU-by-FMNMX form only and
-    // skips the per-unit sign vote.  The paged pool is not scanned.
-    int any_neg = PAGED ? 1 : 0;
-    if (!PAGED && !MX) {
-        const int n4 = p.S_kv >> 2;
-        const float4* s4 = reinterpret_cast<const float4*>(p.kv_scale);
-        for (int k = tid; k < n4; k += kThreads) {
-            const float4 v = __ldg(s4 + k);
-            any_neg |= (v.x < 0.f) | (v.y < 0.f) | (v.z < 0.f) | (v.w < 0.f);
-        }
-        for (int k = (n4 << 2) + tid; k < p.S_kv; k += kThreads)
-            any_neg |= __ldg(p.kv_scale + k) < 0.f;
-    }
-    any_neg = __syncthreads_or(any_neg);
+    __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = sm.tmem_base;
@@ -1145,6 +1135,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ================================================= epilogue
         regs_inc<kRegsEpi>();
+        // Any negative key scale?  Without one (the usual case: scales are
+        // quantisation factors) the epilogue runs the ReLU-by-FMNMX form only
+        // and skips the per-unit sign vote.  The paged pool is not scanned; MX
+        // calls have no fp32 scale.  The dense scan is the epilogue warps'
+        // (all 16 of them: dense units are 256 columns wide), so it overlaps
+        // the producer's first copies; their answer meets in shared memory.
+        int any_neg = PAGED ? 1 : 0;
+        if constexpr (!PAGED && !MX) {
+            const int et = tid - 32 * kEpiWarp0;
+            const int n4 = p.S_kv >> 2;
+            const float4* s4 = reinterpret_cast<const float4*>(p.kv_scale);
+            int neg = 0;
+            for (int k = et; k < n4; k += 32 * kNumEpiWarps) {
+                const float4 v = __ldg(s4 + k);
+                neg |= (v.x < 0.f) | (v.y < 0.f) | (v.z < 0.f) | (v.w < 0.f);
+            }
+            for (int k = (n4 << 2) + et; k < p.S_kv; k += 32 * kNumEpiWarps)
+                neg |= __ldg(p.kv_scale + k) < 0.f;
+            if (__any_sync(0xffffffffu, neg) && lane == 0)
+                atomicOr(&sm.any_neg, 1);
+            __syncwarp();
+            mbar_arrive_one_per_warp(smem_u32(&sm.neg_bar));
+            any_neg = warp_wait_fast(smem_u32(&sm.neg_bar), 0, wctx)
+                          ? *reinterpret_cast<volatile int*>(&sm.any_neg)
+                          : 1;   // timed out: the abort flag ends the run anyway
+        }
         // Warp group g owns accumulator columns [kEpiCols g, kEpiCols (g + 1)):
         // tokens [g kEpiCols / H, (g + 1) kEpiCols / H) of the unit's query block.
         const int g = (warp - kEpiWarp0) >> 2;
