@@ -797,7 +797,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm.start_t = t0;
         }
     }
-    __syncthreads();
+    // Candidate instances scan the key scales here, with every thread (in
+    // their epilogue the scan measured slower: its registers crowd the
+    // candidate store); the other dense instances scan in the epilogue warps.
+    constexpr bool kScanFirst = !PAGED && !MX && std::is_same<OutT, CandOut>::value;
+    int neg_first = 0;
+    if constexpr (kScanFirst) {
+        const int n4 = p.S_kv >> 2;
+        const float4* s4 = reinterpret_cast<const float4*>(p.kv_scale);
+        for (int k = tid; k < n4; k += kThreads) {
+            const float4 v = __ldg(s4 + k);
+            neg_first |= (v.x < 0.f) | (v.y < 0.f) | (v.z < 0.f) | (v.w < 0.f);
+        }
+        for (int k = (n4 << 2) + tid; k < p.S_kv; k += kThreads)
+            neg_first |= __ldg(p.kv_scale + k) < 0.f;
+    }
+    neg_first = __syncthreads_or(neg_first);
     tc_fence_after();
 
     const uint32_t tmem_base = sm.tmem_base;
@@ -1141,8 +1156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // calls have no fp32 scale.  The dense scan is the epilogue warps'
         // (all 16 of them: dense units are 256 columns wide), so it overlaps
         // the producer's first copies; their answer meets in shared memory.
-        int any_neg = PAGED ? 1 : 0;
-        if constexpr (!PAGED && !MX) {
+        int any_neg = PAGED ? 1 : neg_first;
+        if constexpr (!PAGED && !MX && !kScanFirst) {
             const int et = tid - 32 * kEpiWarp0;
             const int n4 = p.S_kv >> 2;
             const float4* s4 = reinterpret_cast<const float4*>(p.kv_scale);
