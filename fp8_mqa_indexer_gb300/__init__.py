@@ -454,7 +454,8 @@ def paged_mqa_logits_noalloc(q, kv_cache, kv_scales, weights, context_lens, bloc
     """Paged decode MQA logits with the work schedule kept in the library's own
     fixed device array (C ABI ``paged_mqa_logits_noalloc``): no schedule buffer
     and no allocation.  ``logits`` must be given ([B*next_n, ldo] float32);
-    the inputs are checked exactly as for ``paged_mqa_logits``."""
+    the inputs are checked exactly as for ``paged_mqa_logits`` (kv_scales None:
+    the fused page layout)."""
     import torch
     R, H, D, B, next_n, num_blocks, block_kv, max_blocks = _paged_inputs(
         q, kv_cache, kv_scales, weights, context_lens, block_table, next_n)
